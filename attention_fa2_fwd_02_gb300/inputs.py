@@ -1,0 +1,133 @@
+"""Seeded synthetic inputs and the workload shapes.
+
+This module is shared by the tests, the benchmark and the smoke check.  It
+holds no attention arithmetic: it only draws i.i.d. N(0, 1) values from a
+seeded CPU generator and rounds them to the storage dtype, so that the GPU
+path and the fp64 oracle read exactly the same numbers.
+
+The workloads mirror the pages' own inputs, which are all ``torch.randn``
+draws: the 96 x 512 x 128 fp32 batch of "Extend Thunder with CUDA-Python"
+(opening section), the (4, 32, 8192, {64,128}) bf16 shapes of "Blackwell
+Attention Example" (section "Main Function"), and the axial grid of the
+axial-attention transcript (B=4, H=W=32, 4 heads of dim 16).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+def normal(shape, seed: int, dtype=torch.float32) -> torch.Tensor:
+    """i.i.d. N(0,1) on the CPU from a seeded generator, rounded to ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn(tuple(shape), generator=g, dtype=torch.float32)
+    return x.to(dtype)
+
+
+def qkv(q_shape, kv_shape, seed: int, dtype=torch.float32):
+    """Q, K, V drawn with seeds 3*seed, 3*seed+1, 3*seed+2."""
+    return (normal(q_shape, 3 * seed, dtype),
+            normal(kv_shape, 3 * seed + 1, dtype),
+            normal(kv_shape, 3 * seed + 2, dtype))
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention problem in the SDPA layout [B, H, N, d]."""
+    name: str
+    B: int
+    H: int
+    N_q: int
+    N_k: int
+    d: int
+    dtype: torch.dtype
+    causal: bool
+    scale: float
+    seed: int
+
+    @property
+    def flops(self) -> float:
+        """4 * B * H * N_q * N_k * d, halved for causal attention."""
+        f = 4.0 * self.B * self.H * self.N_q * self.N_k * self.d
+        return f / 2 if self.causal else f
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == torch.bfloat16 else 4
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """Q, K, V read once; O written once (input dtype); LSE written (fp32)."""
+        e = self.elem_bytes
+        q = self.B * self.H * self.N_q * self.d * e
+        kv = 2 * self.B * self.H * self.N_k * self.d * e
+        o = q
+        lse = self.B * self.H * self.N_q * 4
+        return float(q + kv + o + lse)
+
+    def make(self):
+        return qkv((self.B, self.H, self.N_q, self.d),
+                   (self.B, self.H, self.N_k, self.d), self.seed, self.dtype)
+
+
+def _w(name, B, H, Nq, Nk, d, dtype, causal, scale=None, seed=0):
+    return Workload(name, B, H, Nq, Nk, d, dtype, causal,
+                    1.0 / math.sqrt(d) if scale is None else scale, seed)
+
+
+# The five configurations (non-causal and causal variants where both are run).
+WORKLOADS = {
+    "tiny_nc": _w("tiny_nc", 1, 1, 64, 64, 64, torch.float32, False, seed=1),
+    "tiny_causal": _w("tiny_causal", 1, 1, 64, 64, 64, torch.float32, True, seed=1),
+    "tutorial_nc": _w("tutorial_nc", 96, 1, 512, 512, 128, torch.float32, False, seed=2),
+    "tutorial_causal": _w("tutorial_causal", 96, 1, 512, 512, 128, torch.float32, True, seed=2),
+    "large_nc": _w("large_nc", 4, 32, 8192, 8192, 128, torch.bfloat16, False, seed=4),
+    "large_causal": _w("large_causal", 4, 32, 8192, 8192, 128, torch.bfloat16, True, seed=4),
+    "cross_long_nc": _w("cross_long_nc", 2, 16, 4096, 32768, 64, torch.bfloat16, False, seed=5),
+    "long_causal": _w("long_causal", 1, 16, 32768, 32768, 128, torch.bfloat16, True, seed=6),
+}
+
+
+@dataclass(frozen=True)
+class AxialWorkload:
+    """Axial attention core over a grid x[B, Hg, Wg, heads, hd] (fp32).
+
+    Row attention: sequences of length Wg, one per (b, hg, head).
+    Column attention: sequences of length Hg, one per (b, wg, head).
+    Both read Q, K, V of shape [B, Hg, Wg, heads, hd] in place (strided).
+    """
+    name: str = "axial"
+    B: int = 4
+    Hg: int = 32
+    Wg: int = 32
+    heads: int = 4
+    hd: int = 16
+    scale: float = 0.25
+    seed: int = 3
+
+    @property
+    def shape(self):
+        return (self.B, self.Hg, self.Wg, self.heads, self.hd)
+
+    @property
+    def flops(self) -> float:
+        """Row plus column attention: 4 * (#sequences) * L^2 * hd each."""
+        row = 4.0 * self.B * self.Hg * self.heads * self.Wg * self.Wg * self.hd
+        col = 4.0 * self.B * self.Wg * self.heads * self.Hg * self.Hg * self.hd
+        return row + col
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """Per direction: Q, K, V read, O written (fp32), LSE written (fp32)."""
+        n = self.B * self.Hg * self.Wg * self.heads
+        per_dir = 4 * n * self.hd * 4 + n * 4
+        return 2.0 * per_dir
+
+    def make(self):
+        return qkv(self.shape, self.shape, self.seed, torch.float32)
+
+
+AXIAL = AxialWorkload()

@@ -1,0 +1,122 @@
+"""fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and
+this package imports nothing from the product package: the two share no code.
+
+The arithmetic lives in ``attention_oracle.c`` (plain C, fp64, untiled; its
+header states the definition and the passages it follows).  This module only
+compiles that file with gcc, loads it with ctypes and loops over the leading
+(batch, head) dimensions.
+
+Reading of the pages it encodes ("Extend Thunder with CUDA-Python",
+flash_attention_reference; "Blackwell Attention Example", kernel docstring):
+
+* O = softmax(scale * Q K^T) V per (batch, head) slice, SDPA layout [..., N, d];
+* LSE = log sum_j exp(s_ij), natural log of the scaled scores;
+* causal: key j visible to query row i iff j <= i (top-left alignment).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "attention_oracle.c"
+_LIB_PATH = _HERE / "_build" / "liboracle.so"
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> Path:
+    """Compile ``attention_oracle.c`` into ``oracle/_build/liboracle.so``."""
+    _LIB_PATH.parent.mkdir(parents=True, exist_ok=True)
+    if (not force and _LIB_PATH.exists()
+            and _LIB_PATH.stat().st_mtime >= _SRC.stat().st_mtime):
+        return _LIB_PATH
+    tmp = _LIB_PATH.with_suffix(f".so.tmp{os.getpid()}")
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           str(_SRC), "-o", str(tmp), "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(str(build()))
+            f = lib.oracle_attention_slice
+            f.restype = ctypes.c_int
+            f.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p,
+            ]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Host threads the oracle's parallel loop uses."""
+    return int(_load().oracle_num_threads())
+
+
+def _as_f32(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor (bf16 widens exactly to fp32)
+        x = x.detach().cpu().float().numpy()
+    x = np.asarray(x)
+    if x.dtype != np.float32:
+        x32 = x.astype(np.float32)
+        if not np.array_equal(x32.astype(x.dtype), x):
+            raise ValueError("oracle inputs must be exactly representable in fp32")
+        x = x32
+    return x
+
+
+def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
+    """fp64 attention of every (batch..., head) slice.
+
+    Q: [..., N_q, d]; K, V: [..., N_k, d] with the same leading dims.
+    rows: optional 1-D sequence of query rows to evaluate in every slice.
+    Returns (O, LSE) as float64 numpy arrays [..., n_rows, d] and [..., n_rows].
+    """
+    Q, K, V = _as_f32(Q), _as_f32(K), _as_f32(V)
+    if Q.ndim < 2 or K.shape != V.shape or Q.shape[:-2] != K.shape[:-2] \
+            or Q.shape[-1] != K.shape[-1]:
+        raise ValueError(f"bad shapes Q{Q.shape} K{K.shape} V{V.shape}")
+    lead = Q.shape[:-2]
+    N_q, d = Q.shape[-2:]
+    N_k = K.shape[-2]
+    if rows is None:
+        rows_arr = None
+        n_rows = N_q
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        n_rows = rows_arr.size
+    Qs = np.ascontiguousarray(Q.reshape(-1, N_q, d))
+    Ks = np.ascontiguousarray(K.reshape(-1, N_k, d))
+    Vs = np.ascontiguousarray(V.reshape(-1, N_k, d))
+    O = np.empty((Qs.shape[0], n_rows, d), dtype=np.float64)
+    L = np.empty((Qs.shape[0], n_rows), dtype=np.float64)
+    lib = _load()
+    rows_ptr = None if rows_arr is None else rows_arr.ctypes.data
+    for s in range(Qs.shape[0]):
+        rc = lib.oracle_attention_slice(
+            Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d,
+            N_q, N_k, d, float(scale), int(bool(is_causal)),
+            rows_ptr, n_rows, O[s].ctypes.data, L[s].ctypes.data)
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_slice failed with {rc}")
+    return O.reshape(*lead, n_rows, d), L.reshape(*lead, n_rows)

@@ -1,0 +1,118 @@
+/*
+ * attention_oracle.c -- plain fp64 CPU attention, TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the correctness oracle for the GPU FlashAttention-2 forward.
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg may load it; the product path never does.  It shares no code, header or
+ * constant with the CUDA sources.
+ *
+ * What it computes is the plain definition of scaled dot-product attention
+ * that the FlashAttention-2 forward reaches exactly (up to rounding order):
+ *
+ *   s_ij   = scale * sum_k Q[i,k] K[j,k]        for every visible key j
+ *   LSE_i  = log sum_j exp(s_ij)                (natural log)
+ *   O[i,:] = sum_j exp(s_ij - LSE_i) V[j,:]
+ *
+ * Sources:
+ *  - "Extend Thunder with CUDA-Python", section "Extend Thunder with
+ *    CUDA-Python", function flash_attention_reference: the forward is
+ *    softmax(scale * Q K^T) V over the SDPA layout [batch..., N, d]; the second
+ *    output is L = m + log(l), the natural-log log-sum-exp of the scaled
+ *    scores; the default scale is 1/sqrt(d); with is_causal the key index j
+ *    is visible to query row i only when i >= j (query and key rows both
+ *    counted from 0, i.e. top-left alignment when N_q != N_k).
+ *  - "Blackwell Attention Example", section "Attention Kernel Implementation",
+ *    docstring of blackwell_attention_kernel: Attention(Q,K,V) =
+ *    softmax(Q K^T * scale) V with Q [..., seq_q, d] and K, V [..., seq_k, d].
+ *
+ * The evaluation is untiled: for each requested query row all visible scores
+ * are formed in fp64, their maximum m is taken, and l = sum exp(s - m);
+ * then O = sum exp(s - m) V / l and LSE = m + log(l).  Subtracting m is the
+ * usual exact rewriting of the softmax (it cancels in the ratio) and keeps
+ * exp() in range; it is not the tiled online-softmax of the method.
+ *
+ * Inputs are fp32 arrays (every bf16 and fp32 value the GPU sees is exactly
+ * representable in fp32); all arithmetic is fp64.  Rows are independent and
+ * are spread over OpenMP threads when the library is built with -fopenmp.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Number of threads the parallel loop below uses (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/*
+ * One (batch, head) slice.
+ *   Q: N_q rows of d floats, row i at Q + i*q_row_stride (elements).
+ *   K, V: N_k rows, row j at K + j*k_row_stride, V + j*v_row_stride.
+ *   rows[0..n_rows): the query rows to evaluate (NULL = all N_q rows in order).
+ *   O: n_rows x d doubles, row r at O + r*d.   LSE: n_rows doubles.
+ * Returns 0 on success, -1 on bad arguments, -2 if scratch allocation failed.
+ */
+int oracle_attention_slice(const float* Q, int64_t q_row_stride,
+                           const float* K, int64_t k_row_stride,
+                           const float* V, int64_t v_row_stride,
+                           int64_t N_q, int64_t N_k, int64_t d,
+                           double scale, int is_causal,
+                           const int64_t* rows, int64_t n_rows,
+                           double* O, double* LSE) {
+  if (!Q || !K || !V || !O || !LSE || N_q < 0 || N_k <= 0 || d <= 0 || n_rows < 0)
+    return -1;
+  if (!rows && n_rows != N_q) return -1;
+  int failed = 0;
+
+#pragma omp parallel
+  {
+    double* s = (double*)malloc((size_t)N_k * sizeof(double));
+    if (!s) {
+#pragma omp atomic write
+      failed = 2;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n_rows; ++r) {
+      if (!s) continue;
+      int64_t i = rows ? rows[r] : r;
+      double* o = O + r * d;
+      if (i < 0 || i >= N_q) {
+#pragma omp atomic write
+        failed = 1;
+        continue;
+      }
+      /* visible keys: all of them, or j <= i under the causal mask */
+      int64_t n_vis = N_k;
+      if (is_causal && i + 1 < N_k) n_vis = i + 1;
+
+      const float* q = Q + i * q_row_stride;
+      double m = -INFINITY;
+      for (int64_t j = 0; j < n_vis; ++j) {
+        const float* k = K + j * k_row_stride;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += (double)q[c] * (double)k[c];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+      }
+      double l = 0.0;
+      for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t j = 0; j < n_vis; ++j) {
+        double p = exp(s[j] - m);
+        const float* v = V + j * v_row_stride;
+        l += p;
+        for (int64_t c = 0; c < d; ++c) o[c] += p * (double)v[c];
+      }
+      for (int64_t c = 0; c < d; ++c) o[c] /= l;
+      LSE[r] = m + log(l);
+    }
+    free(s);
+  }
+  return failed == 1 ? -1 : (failed == 2 ? -2 : 0);
+}

@@ -1,0 +1,260 @@
+"""GB300-native FlashAttention-2 forward: the Python binding of ``libfa.so``.
+
+The binding only marshals arguments: every step of the computation runs in
+the library's CUDA kernels (C ABI in ``include/fa.h``).  PyTorch supplies
+device memory and the current stream.  There is no CPU or PyTorch fallback:
+if the library is missing, every call raises.
+
+    O, LSE = fwd(Q, K, V, scale=None, is_causal=False)
+
+Q: [B, H, N_q, d], K and V: [B, H, N_k, d] CUDA tensors (bf16 or fp32; any
+strides with a contiguous last dim).  O has Q's dtype, LSE is fp32 [B, H, N_q]
+(natural log).  The default scale is 1/sqrt(d), as in "Extend Thunder with
+CUDA-Python" (flash_attention_reference) and "Blackwell Attention Example"
+(blackwell_attention).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+from pathlib import Path
+
+import torch
+
+__all__ = ["fwd", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
+           "LIB_PATH", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
+           "FA_ERR_TIMEOUT"]
+
+LIB_PATH = Path(__file__).resolve().parent / "_build" / "libfa.so"
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_BF16, FA_FP32 = 0, 1
+
+
+class FaTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride", ctypes.c_int64 * 4)]
+
+
+class FaProblem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N_q", ctypes.c_int64),
+                ("N_k", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("Q", FaTensor), ("K", FaTensor), ("V", FaTensor), ("O", FaTensor),
+                ("LSE", ctypes.c_void_p), ("lse_stride", ctypes.c_int64 * 3),
+                ("scale", ctypes.c_float), ("is_causal", ctypes.c_int)]
+
+
+class FaError(RuntimeError):
+    """A non-OK status from libfa.so."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, ptxas_verbose: bool = False) -> Path:
+    """Compile libfa.so for sm_103a (nvcc) into this package's _build/."""
+    from ._build import build as _b
+    return _b(force=force, ptxas_verbose=ptxas_verbose)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "attention_fa2_fwd_02_gb300.build() (no fallback exists)")
+            L = ctypes.CDLL(str(LIB_PATH))
+            P = ctypes.POINTER
+            L.fa_fwd.restype = ctypes.c_int
+            L.fa_fwd.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                 ctypes.c_int64, ctypes.c_int64, P(FaTensor), P(FaTensor),
+                                 P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
+                                 ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p]
+            L.fa_fwd_grouped.restype = ctypes.c_int
+            L.fa_fwd_grouped.argtypes = [ctypes.c_int, ctypes.c_int, P(FaProblem), ctypes.c_void_p]
+            L.fa_check.restype = ctypes.c_int
+            L.fa_check.argtypes = [ctypes.c_void_p]
+            L.fa_status_string.restype = ctypes.c_char_p
+            L.fa_status_string.argtypes = [ctypes.c_int]
+            L.fa_last_error.restype = ctypes.c_char_p
+            L.fa_last_error.argtypes = []
+            L.fa_debug_set.restype = None
+            L.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_int]
+            L.fa_version.restype = ctypes.c_int
+            L.fa_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _raise_on(status: int) -> None:
+    if status != FA_OK:
+        L = lib()
+        msg = L.fa_last_error().decode()
+        raise FaError(status, f"{L.fa_status_string(status).decode()}: {msg}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _as4(t: torch.Tensor) -> torch.Tensor:
+    if t.dim() == 4:
+        return t
+    if t.dim() == 3:
+        return t.unsqueeze(0)
+    if t.dim() == 2:
+        return t.unsqueeze(0).unsqueeze(0)
+    raise ValueError(f"expected a 2-, 3- or 4-D tensor, got {tuple(t.shape)}")
+
+
+def _ft(t: torch.Tensor) -> FaTensor:
+    s = t.stride()
+    return FaTensor(ctypes.c_void_p(t.data_ptr()), (ctypes.c_int64 * 4)(*s))
+
+
+def _stream_ptr(device: torch.device, stream=None) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
+    if not (Q.is_cuda and K.is_cuda and V.is_cuda):
+        raise ValueError("Q, K, V must be CUDA tensors (this library has no CPU path)")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise TypeError("Q, K, V must share one dtype")
+    if not (Q.device == K.device == V.device):
+        raise ValueError("Q, K, V must be on one device")
+    q4, k4, v4 = _as4(Q), _as4(K), _as4(V)
+    B, H, N_q, d = q4.shape
+    if k4.shape != v4.shape or k4.shape[0] != B or k4.shape[1] != H or k4.shape[3] != d:
+        raise ValueError(f"shape mismatch: Q{tuple(Q.shape)} K{tuple(K.shape)} V{tuple(V.shape)}")
+    N_k = k4.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(Q.shape, dtype=Q.dtype, device=Q.device)
+    o4 = _as4(out)
+    if o4.shape != q4.shape or out.dtype != Q.dtype or out.device != Q.device:
+        raise ValueError("out must match Q's shape, dtype and device")
+    if with_lse and lse is None:
+        lse = torch.empty(Q.shape[:-1], dtype=torch.float32, device=Q.device)
+    pb = FaProblem()
+    pb.B, pb.H, pb.N_q, pb.N_k, pb.d = B, H, N_q, N_k, d
+    pb.Q, pb.K, pb.V, pb.O = _ft(q4), _ft(k4), _ft(v4), _ft(o4)
+    if lse is not None:
+        if lse.dtype != torch.float32 or lse.device != Q.device or lse.shape != Q.shape[:-1]:
+            raise ValueError("lse must be fp32 with Q's leading shape, on Q's device")
+        l3 = lse
+        while l3.dim() < 3:
+            l3 = l3.unsqueeze(0)
+        pb.LSE = ctypes.c_void_p(l3.data_ptr())
+        pb.lse_stride = (ctypes.c_int64 * 3)(*l3.stride())
+    else:
+        pb.LSE = None
+        pb.lse_stride = (ctypes.c_int64 * 3)(0, 0, 0)
+    pb.scale = float(scale)
+    pb.is_causal = 1 if is_causal else 0
+    return pb, out, lse
+
+
+def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None = None,
+        is_causal: bool = False, out: torch.Tensor | None = None,
+        lse: torch.Tensor | None = None, with_lse: bool = True, stream=None):
+    """O, LSE = softmax(scale * Q K^T) V and its log-sum-exp, on the GPU.
+
+    Asynchronous on the current (or given) stream.  Returns (O, LSE); LSE is
+    None when ``with_lse`` is False and no ``lse`` buffer is passed.
+    """
+    pb, out, lse = _problem(Q, K, V, scale, is_causal, out, lse, with_lse)
+    L = lib()
+    with torch.cuda.device(Q.device):
+        lse_stride = (ctypes.c_int64 * 3)(*pb.lse_stride)
+        st = L.fa_fwd(_dtype_code(Q), pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
+                      ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                      pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
+                      _stream_ptr(Q.device, stream))
+    _raise_on(st)
+    return out, lse
+
+
+def fwd_grouped(problems, stream=None):
+    """Several independent problems in as few launches as possible.
+
+    ``problems``: list of dicts with keys Q, K, V and optional scale,
+    is_causal, out, lse, with_lse.  Returns a list of (O, LSE).
+    """
+    if not problems:
+        return []
+    built, results = [], []
+    for pr in problems:
+        pb, out, lse = _problem(pr["Q"], pr["K"], pr["V"], pr.get("scale"),
+                                pr.get("is_causal", False), pr.get("out"), pr.get("lse"),
+                                pr.get("with_lse", True))
+        built.append(pb)
+        results.append((out, lse))
+    dt = _dtype_code(problems[0]["Q"])
+    if any(_dtype_code(p["Q"]) != dt for p in problems):
+        raise TypeError("all problems of a grouped call share one dtype")
+    dev = problems[0]["Q"].device
+    arr = (FaProblem * len(built))(*built)
+    with torch.cuda.device(dev):
+        st = lib().fa_fwd_grouped(dt, len(built), arr, _stream_ptr(dev, stream))
+    _raise_on(st)
+    return results
+
+
+def axial(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None = None,
+          with_lse: bool = False, stream=None):
+    """Row and column attention over an axial grid, in one launch.
+
+    Q, K, V: [B, Hg, Wg, heads, hd] tensors (contiguous).  Row attention runs
+    along Wg for every (b, hg, head); column attention along Hg for every
+    (b, wg, head).  Both read the inputs in place through strided views.
+    Returns ((O_row, LSE_row), (O_col, LSE_col)), O_* shaped like Q.
+    """
+    B, Hg, Wg, nh, hd = Q.shape
+
+    # .view (never .reshape): the views must alias the tensors, no copies
+    def row_view(x):  # [B*Hg, heads, Wg, (hd)]
+        return x.permute(0, 1, 3, 2, *range(4, x.dim())).view(B * Hg, nh, Wg, *x.shape[4:])
+
+    def col_view(x):  # [B, Wg*heads, Hg, (hd)]
+        return x.permute(0, 2, 3, 1, *range(4, x.dim())).view(B, Wg * nh, Hg, *x.shape[4:])
+
+    O_row = torch.empty_like(Q)
+    O_col = torch.empty_like(Q)
+    lse_row = torch.empty((B, Hg, Wg, nh), dtype=torch.float32, device=Q.device) if with_lse else None
+    lse_col = torch.empty((B, Hg, Wg, nh), dtype=torch.float32, device=Q.device) if with_lse else None
+    probs = [
+        dict(Q=row_view(Q), K=row_view(K), V=row_view(V), scale=scale, out=row_view(O_row),
+             lse=None if lse_row is None else row_view(lse_row), with_lse=with_lse),
+        dict(Q=col_view(Q), K=col_view(K), V=col_view(V), scale=scale, out=col_view(O_col),
+             lse=None if lse_col is None else col_view(lse_col), with_lse=with_lse),
+    ]
+    fwd_grouped(probs, stream=stream)
+    return (O_row, lse_row), (O_col, lse_col)
+
+
+def check(stream=None, device=None) -> None:
+    """Synchronise and raise FaError if a kernel's bounded wait expired."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = lib().fa_check(_stream_ptr(dev, stream))
+    _raise_on(st)
+
+
+def debug_set(timeout_ns: int = 0, flags: int = 0) -> None:
+    """Test hooks: device wait limit (0 = default 1 s) and fault-injection flags."""
+    lib().fa_debug_set(int(timeout_ns), int(flags))

@@ -1,0 +1,364 @@
+// fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
+// validation, TMA descriptor encoding, kernel selection and launch, and the
+// device error word behind fa_check().  Host-side only, apart from the
+// small-head kernel instantiations, which live here too.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "fa.h"
+#include "fa_launch.h"
+#include "fa_small.cuh"
+
+namespace fa {
+// Raised (atomicOr) by any kernel of this library whose bounded wait expires.
+__device__ unsigned int g_err_word;
+}  // namespace fa
+
+namespace {
+
+using namespace fa;
+
+thread_local std::string t_last_error;
+
+fa_status_t fail(fa_status_t st, const std::string& msg) {
+  t_last_error = msg;
+  return st;
+}
+
+std::string cuda_msg(const char* what, cudaError_t e) {
+  return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+}
+
+std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
+std::atomic<int> g_debug_flags{0};
+
+constexpr int kMaxDevices = 64;
+struct DevState {
+  bool ready = false;
+  int sm_count = 0;
+  unsigned int* err = nullptr;
+};
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+
+fa_status_t device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("cudaGetDevice", e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device ordinal out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail(FA_ERR_CUDA, cuda_msg("cudaDeviceGetAttribute", e));
+    if (major != 10 || minor != 3)
+      return fail(FA_ERR_UNSUPPORTED, "libfa.so is built for sm_103a (GB300); device has compute capability " +
+                                          std::to_string(major) + "." + std::to_string(minor));
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_err_word)) != cudaSuccess)
+      return fail(FA_ERR_CUDA, cuda_msg("cudaGetSymbolAddress(error word)", e));
+    s.err = static_cast<unsigned int*>(p);
+    s.ready = true;
+  }
+  *out = &s;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+enum class Path { kTensorCore, kSmall };
+
+bool tensor_ok(const fa_tensor_t& t) { return t.ptr != nullptr && t.stride[3] == 1; }
+
+// Validate one problem and choose its kernel.
+fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* path) {
+  const std::string at = "problem " + std::to_string(idx) + ": ";
+  if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, at + "unknown dtype");
+  if (pb.B <= 0 || pb.H <= 0 || pb.N_q <= 0 || pb.N_k <= 0 || pb.d <= 0)
+    return fail(FA_ERR_INVALID_ARG, at + "B, H, N_q, N_k and d must all be >= 1");
+  if (!tensor_ok(pb.Q) || !tensor_ok(pb.K) || !tensor_ok(pb.V) || !tensor_ok(pb.O))
+    return fail(FA_ERR_INVALID_ARG, at + "Q, K, V, O need a non-null pointer and stride[3] == 1");
+  if (!std::isfinite(pb.scale)) return fail(FA_ERR_INVALID_ARG, at + "scale must be finite");
+  if (pb.is_causal != 0 && pb.is_causal != 1) return fail(FA_ERR_INVALID_ARG, at + "is_causal must be 0 or 1");
+  if (pb.LSE && (pb.lse_stride[0] < 0 || pb.lse_stride[1] < 0 || pb.lse_stride[2] < 0))
+    return fail(FA_ERR_UNSUPPORTED, at + "negative LSE strides are not supported");
+  const fa_tensor_t* ts[4] = {&pb.Q, &pb.K, &pb.V, &pb.O};
+  for (auto* t : ts)
+    for (int i = 0; i < 3; ++i)
+      if (t->stride[i] < 0) return fail(FA_ERR_UNSUPPORTED, at + "negative strides are not supported");
+  if (pb.N_q >= (1ll << 31) || pb.N_k >= (1ll << 31) || pb.B >= (1ll << 31) || pb.H >= (1ll << 31))
+    return fail(FA_ERR_UNSUPPORTED, at + "sizes must be below 2^31");
+  if (pb.d == 16 || pb.d == 32) {
+    const long long items = pb.B * pb.H * ((pb.N_q + 31) / 32);
+    if (items >= (1ll << 40)) return fail(FA_ERR_UNSUPPORTED, at + "too many query blocks");
+    *path = Path::kSmall;
+    return FA_OK;
+  }
+  if (pb.d != 64 && pb.d != 128)
+    return fail(FA_ERR_UNSUPPORTED, at + "head dim " + std::to_string(pb.d) + " not supported (16, 32, 64, 128)");
+  const long long E = dtype == FA_FP32 ? 4 : 2;
+  for (auto* t : ts) {
+    if (reinterpret_cast<uintptr_t>(t->ptr) % 16 != 0)
+      return fail(FA_ERR_UNSUPPORTED, at + "tensor-core path needs 16-byte aligned base pointers");
+    for (int i = 0; i < 3; ++i)
+      if ((t->stride[i] * E) % 16 != 0)
+        return fail(FA_ERR_UNSUPPORTED, at + "tensor-core path needs strides that are multiples of 16 bytes");
+  }
+  const long long tiles = pb.B * pb.H * ((pb.N_q + 255) / 256);
+  if (tiles >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, at + "too many query tiles");
+  *path = Path::kTensorCore;
+  return FA_OK;
+}
+
+fa_status_t make_map(CUtensorMap* map, const fa_tensor_t& t, bool fp32, long long B, long long H, long long N,
+                     long long d, int box_rows, const char* name) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const long long E = fp32 ? 4 : 2;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(t.stride[2] * E), (cuuint64_t)(t.stride[1] * E),
+                           (cuuint64_t)(t.stride[0] * E)};
+  cuuint32_t box[4] = {(cuuint32_t)tc_box_inner(fp32), (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.ptr, dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FA_ERR_UNSUPPORTED, std::string("cuTensorMapEncodeTiled rejected the layout of ") + name +
+                                        " (CUresult " + std::to_string((int)r) + ")");
+  return FA_OK;
+}
+
+fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const DevState& ds, cudaStream_t stream) {
+  const bool fp32 = dtype == FA_FP32;
+  const int d = static_cast<int>(pb.d);
+  const int bn = tc_key_tile(fp32);
+  TcLaunch L;
+  fa_status_t st;
+  if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, d, 128, "Q")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, pb.K, fp32, pb.B, pb.H, pb.N_k, d, bn, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, pb.H, pb.N_k, d, bn, "V")) != FA_OK) return st;
+  TcParams& p = L.p;
+  p.B = (int)pb.B;
+  p.H = (int)pb.H;
+  p.N_q = (int)pb.N_q;
+  p.N_k = (int)pb.N_k;
+  p.causal = pb.is_causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
+  p.n_qblk = (int)((pb.N_q + 255) / 256);
+  p.n_tiles = (int)(pb.B * pb.H * p.n_qblk);
+  // Heads per schedule group: keep the K/V of a group within ~48 MB of L2.
+  const long long kv_bytes = 2ll * pb.N_k * pb.d * (fp32 ? 4 : 2);
+  long long g = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+  if (g < 1) g = 1;
+  if (g > pb.B * pb.H) g = pb.B * pb.H;
+  p.head_group = (int)g;
+  p.O = pb.O.ptr;
+  for (int i = 0; i < 3; ++i) {
+    p.o_stride[i] = pb.O.stride[i];
+    p.lse_stride[i] = pb.LSE ? pb.lse_stride[i] : 0;
+  }
+  p.LSE = pb.LSE;
+  p.err = ds.err;
+  p.timeout_ns = g_timeout_ns.load();
+  p.debug_flags = g_debug_flags.load();
+  L.grid = p.n_tiles < ds.sm_count ? p.n_tiles : ds.sm_count;
+  L.stream = stream;
+  cudaError_t e;
+  if (fp32)
+    e = d == 128 ? launch_tc_fp32_d128(L) : launch_tc_fp32_d64(L);
+  else
+    e = d == 128 ? launch_tc_bf16_d128(L) : launch_tc_bf16_d64(L);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("tensor-core kernel launch", e));
+  return FA_OK;
+}
+
+bool row_aligned16(const fa_tensor_t& t, long long E) {
+  if (reinterpret_cast<uintptr_t>(t.ptr) % 16 != 0) return false;
+  for (int i = 0; i < 3; ++i)
+    if ((t.stride[i] * E) % 16 != 0) return false;
+  return true;
+}
+
+template <typename T, int D>
+cudaError_t launch_small_typed(const SmallParams& P, cudaStream_t stream) {
+  constexpr int smem = small_smem_bytes<T, D>();
+  cudaError_t e = cudaFuncSetAttribute(fa_small_fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (P.n_items + 3) / 4;
+  fa_small_fwd_kernel<T, D><<<(unsigned)blocks, 128, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+// One launch for up to kSmallMaxGroup problems of the same dtype and head dim.
+fa_status_t launch_small(fa_dtype_t dtype, int d, const std::vector<const fa_problem_t*>& probs,
+                         cudaStream_t stream) {
+  const long long E = dtype == FA_FP32 ? 4 : 2;
+  SmallParams P{};
+  P.n_problems = (int)probs.size();
+  long long items = 0;
+  for (size_t i = 0; i < probs.size(); ++i) {
+    const fa_problem_t& pb = *probs[i];
+    SmallProblem& s = P.prob[i];
+    s.Q = pb.Q.ptr;
+    s.K = pb.K.ptr;
+    s.V = pb.V.ptr;
+    s.O = pb.O.ptr;
+    s.LSE = pb.LSE;
+    for (int k = 0; k < 3; ++k) {
+      s.qs[k] = pb.Q.stride[k];
+      s.ks[k] = pb.K.stride[k];
+      s.vs[k] = pb.V.stride[k];
+      s.os[k] = pb.O.stride[k];
+      s.ls[k] = pb.LSE ? pb.lse_stride[k] : 0;
+    }
+    s.B = (int)pb.B;
+    s.H = (int)pb.H;
+    s.N_q = (int)pb.N_q;
+    s.N_k = (int)pb.N_k;
+    s.causal = pb.is_causal;
+    s.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
+    s.n_qblk = (int)((pb.N_q + 31) / 32);
+    s.vec_ok = row_aligned16(pb.Q, E) && row_aligned16(pb.K, E) && row_aligned16(pb.V, E) &&
+               row_aligned16(pb.O, E);
+    s.item_begin = items;
+    items += pb.B * pb.H * s.n_qblk;
+  }
+  P.n_items = items;
+  if ((items + 3) / 4 >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query blocks in one launch");
+  cudaError_t e;
+  if (dtype == FA_FP32)
+    e = d == 16 ? launch_small_typed<float, 16>(P, stream) : launch_small_typed<float, 32>(P, stream);
+  else
+    e = d == 16 ? launch_small_typed<__nv_bfloat16, 16>(P, stream)
+                : launch_small_typed<__nv_bfloat16, 32>(P, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("small-head kernel launch", e));
+  return FA_OK;
+}
+
+fa_status_t run_problems(fa_dtype_t dtype, int n, const fa_problem_t* problems, void* stream_ptr) {
+  if (n < 0 || (n > 0 && !problems)) return fail(FA_ERR_INVALID_ARG, "bad problem list");
+  std::vector<Path> paths(n);
+  for (int i = 0; i < n; ++i) {
+    fa_status_t st = validate(dtype, problems[i], i, &paths[i]);
+    if (st != FA_OK) return st;
+  }
+  if (n == 0) return FA_OK;
+  DevState* ds = nullptr;
+  fa_status_t st = device_state(&ds);
+  if (st != FA_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  for (int d : {16, 32}) {
+    std::vector<const fa_problem_t*> group;
+    for (int i = 0; i < n; ++i) {
+      if (paths[i] != Path::kSmall || problems[i].d != d) continue;
+      group.push_back(&problems[i]);
+      if ((int)group.size() == kSmallMaxGroup) {
+        if ((st = launch_small(dtype, d, group, stream)) != FA_OK) return st;
+        group.clear();
+      }
+    }
+    if (!group.empty() && (st = launch_small(dtype, d, group, stream)) != FA_OK) return st;
+  }
+  for (int i = 0; i < n; ++i)
+    if (paths[i] == Path::kTensorCore && (st = launch_tensor_core(dtype, problems[i], *ds, stream)) != FA_OK)
+      return st;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                   const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale, int is_causal,
+                   const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* stream) {
+  if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
+  if (LSE && !lse_stride) return fail(FA_ERR_INVALID_ARG, "lse_stride must not be NULL when LSE is given");
+  fa_problem_t pb{};
+  pb.B = B;
+  pb.H = H;
+  pb.N_q = N_q;
+  pb.N_k = N_k;
+  pb.d = d;
+  pb.Q = *Q;
+  pb.K = *K;
+  pb.V = *V;
+  pb.O = *O;
+  pb.LSE = LSE;
+  for (int i = 0; i < 3; ++i) pb.lse_stride[i] = LSE ? lse_stride[i] : 0;
+  pb.scale = scale;
+  pb.is_causal = is_causal;
+  return run_problems(dtype, 1, &pb, stream);
+}
+
+fa_status_t fa_fwd_grouped(fa_dtype_t dtype, int n, const fa_problem_t* problems, void* stream) {
+  return run_problems(dtype, n, problems, stream);
+}
+
+fa_status_t fa_check(void* stream_ptr) {
+  DevState* ds = nullptr;
+  fa_status_t st = device_state(&ds);
+  if (st != FA_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("cudaStreamSynchronize", e));
+  unsigned int word = 0;
+  if ((e = cudaMemcpyAsync(&word, ds->err, sizeof(word), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+    return fail(FA_ERR_CUDA, cuda_msg("reading the device error word", e));
+  if (word == 0) return FA_OK;
+  if ((e = cudaMemsetAsync(ds->err, 0, sizeof(word), stream)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+    return fail(FA_ERR_CUDA, cuda_msg("clearing the device error word", e));
+  char buf[128];
+  std::snprintf(buf, sizeof(buf), "a bounded device wait expired (error word 0x%08x)", word);
+  return fail(FA_ERR_TIMEOUT, buf);
+}
+
+const char* fa_status_string(fa_status_t status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported arguments";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* fa_last_error(void) { return t_last_error.c_str(); }
+
+void fa_debug_set(uint64_t timeout_ns, int debug_flags) {
+  g_timeout_ns.store(timeout_ns ? timeout_ns : 1000000000ull);
+  g_debug_flags.store(debug_flags);
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// fa_launch.h -- internal interface between the C-ABI front end (fa_api.cu)
+// and the translation units that instantiate the tensor-core kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_tc.cuh"
+
+namespace fa {
+
+// Everything a tensor-core launch needs, prepared and validated on the host.
+struct TcLaunch {
+  CUtensorMap tmQ, tmK, tmV;
+  TcParams p;
+  int grid;
+  cudaStream_t stream;
+};
+
+// Kernel variants: (element type, head dim).  Each returns the CUDA error of
+// the launch (cudaSuccess when it was queued).
+cudaError_t launch_tc_bf16_d128(const TcLaunch& L);
+cudaError_t launch_tc_bf16_d64(const TcLaunch& L);
+cudaError_t launch_tc_fp32_d128(const TcLaunch& L);
+cudaError_t launch_tc_fp32_d64(const TcLaunch& L);
+
+// Tile geometry shared with the instantiations in fa_tc_bf16.cu and
+// fa_tc_fp32.cu: key-tile width and TMA box width (one 128-byte swizzle row).
+constexpr int tc_key_tile(bool fp32) { return fp32 ? 64 : 128; }
+constexpr int tc_box_inner(bool fp32) { return fp32 ? 32 : 64; }
+
+}  // namespace fa

@@ -1,0 +1,536 @@
+// fa_tc.cuh -- FlashAttention-2 forward on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA) for sm_103a.
+//
+// What it computes (per (b, h), query row i): the online softmax of
+// "Extend Thunder with CUDA-Python" (flash_attention_reference: S = scale Q K^T
+// tile by tile, running max m and sum l, O rescaled by exp(m_old - m_new),
+// final O / l and L = m + log l) in the base-2 form of "Blackwell Attention
+// Example" (section "Attention Kernel Implementation": log2(e) folded into the
+// scale, exp2 for P and for the correction factor), with the top-left causal
+// mask of the former.
+//
+// Design for GB300 (differs from both pages' kernels):
+//  * one CTA per SM, persistent; a CTA tile is 256 query rows of one (b, h),
+//    split into two 128-row halves ("stages") whose softmax runs on two
+//    warpgroups in ping-pong while the tensor core works on the other half;
+//  * warp roles: warpgroups 0/1 = softmax of stage 0/1, warpgroup 2 = epilogue
+//    (O / l, output stores, LSE), warp 12 = TMA loads, warp 13 = MMA issue;
+//  * Q tiles and a ring of K/V tiles arrive by TMA (128-byte swizzle) and are
+//    handed over with mbarriers;
+//  * S = Q K^T (both K-major in shared memory) and O += P V (P from tensor
+//    memory, V MN-major in shared memory) are tcgen05.mma with fp32
+//    accumulators in tensor memory; P overwrites S in place;
+//  * lazy rescaling: the running max only moves when a row's max grows by more
+//    than kTau (log2 units); the exact result is unchanged (m cancels in O/l
+//    and LSE uses the m actually applied), P stays <= 2^kTau;
+//  * every wait is bounded (Watchdog): a stuck pipeline ends the launch with
+//    an error word instead of a hang.
+#pragma once
+
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+constexpr float kTau = 8.0f;              // lazy-rescale threshold, log2 units
+constexpr float kLn2 = 0.69314718055994531f;
+
+struct TcParams {
+  int B, H, N_q, N_k;
+  int causal;
+  float scale_log2;       // scale * log2(e)
+  int n_qblk;             // ceil(N_q / 256)
+  int n_tiles;            // B * H * n_qblk
+  int head_group;         // heads per schedule group (K/V L2 locality)
+  void* O;
+  long long o_stride[3];  // elements: b, h, n
+  float* LSE;
+  long long lse_stride[3];
+  unsigned int* err;
+  unsigned long long timeout_ns;
+  int debug_flags;
+};
+
+template <typename T, int D_, int BN_, int NSLOT_>
+struct TcCfg {
+  using Elem = T;
+  static constexpr bool kTF32 = sizeof(T) == 4;
+  static constexpr int E = sizeof(T);
+  static constexpr int D = D_;
+  static constexpr int BN = BN_;
+  static constexpr int NSLOT = NSLOT_;
+  static constexpr int BM = 128;                  // rows per stage = TMEM lanes
+  static constexpr int kPanelElems = 128 / E;     // elements per 128-byte swizzle row
+  static constexpr int kPanels = D / kPanelElems;
+  static constexpr int kKStep = 32 / E;           // K extent of one MMA instruction
+  static constexpr uint32_t kQPanelBytes = BM * 128;
+  static constexpr uint32_t kKVPanelBytes = BN * 128;
+  static constexpr uint32_t kQBytes = BM * D * E;
+  static constexpr uint32_t kKVBytes = BN * D * E;
+  // tensor-memory columns: S0 | S1 | O0 | O1   (P_s overwrites S_s)
+  __host__ __device__ static constexpr uint32_t col_s(int s) { return s ? BN : 0; }
+  __host__ __device__ static constexpr uint32_t col_o(int s) { return 2 * BN + (s ? D : 0); }
+  static constexpr uint32_t kTmemCols = 512;
+  // shared memory
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffKV = 2 * kQBytes;
+  static constexpr uint32_t kOffBar = kOffKV + NSLOT * kKVBytes;
+  static constexpr int kNumBars = 16 + 2 * NSLOT + 1;
+  static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffMisc = kOffStats + 2 * BM * 8;
+  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
+  static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
+  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, 1);
+  static constexpr int kThreads = 512;
+
+  static_assert(D % kPanelElems == 0, "head dim must fill whole swizzle rows");
+  static_assert(BN % 32 == 0 && BN <= 256, "key tile");
+  static_assert(2 * BN + 2 * D <= 512, "tensor memory budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct Bars {
+  uint64_t* q_full;     // [2] TMA -> MMA
+  uint64_t* q_empty;    // [2] MMA -> TMA
+  uint64_t* s_full;     // [2] MMA -> softmax
+  uint64_t* p_full;     // [2] softmax -> MMA  (128 arrivals)
+  uint64_t* o_full;     // [2] MMA -> epilogue (last P.V of a tile done)
+  uint64_t* o_empty;    // [2] epilogue -> MMA (128 arrivals)
+  uint64_t* st_full;    // [2] softmax -> epilogue: row stats written (128 arrivals)
+  uint64_t* st_empty;   // [2] epilogue -> softmax (128 arrivals)
+  uint64_t* kv_full;    // [NSLOT]
+  uint64_t* kv_empty;   // [NSLOT]
+  uint64_t* teardown;   // [1]
+};
+
+struct TileInfo {
+  int b, h, q0, n_kv;
+};
+
+// Tile order: heads are taken in groups of `head_group`; inside a group the
+// query blocks of all its heads are interleaved, last (longest under the
+// causal mask) first, so that concurrently running CTAs share K/V in L2 and
+// the causal work is handed out longest-first.
+__device__ __forceinline__ TileInfo tile_info(const TcParams& p, int t, int BN) {
+  const int BH = p.B * p.H;
+  const int per_group = p.head_group * p.n_qblk;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int heads = min(p.head_group, BH - g * p.head_group);
+  const int qi = r / heads;
+  const int bh = g * p.head_group + (r - qi * heads);
+  const int qb = p.causal ? (p.n_qblk - 1 - qi) : qi;
+  TileInfo ti;
+  ti.b = bh / p.H;
+  ti.h = bh - ti.b * p.H;
+  ti.q0 = qb * 256;
+  int kv_end = p.N_k;
+  if (p.causal) kv_end = min(kv_end, min(ti.q0 + 256, p.N_q));
+  ti.n_kv = (kv_end + BN - 1) / BN;
+  return ti;
+}
+
+// All 32 lanes wait; the warp proceeds together or aborts together.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Watchdog& wd,
+                                          unsigned int where) {
+  bool ok = mbar_wait(bar, parity, wd, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------- load warp
+template <class C>
+__device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             const TcParams& p, uint8_t* smem, const Bars& bars, const Watchdog& wd) {
+  const uint64_t pol_q = l2_policy_evict_first();
+  const uint64_t pol_kv = l2_policy_evict_last();
+  uint32_t it = 0;
+  uint32_t kv_armed[C::NSLOT];
+  uint32_t q_armed[2] = {0, 0};
+#pragma unroll
+  for (int s = 0; s < C::NSLOT; ++s) kv_armed[s] = 0;
+  bool ok = true;
+  uint32_t tile_k = 0;
+
+  auto load_q = [&](int stage, const TileInfo& ti) -> bool {
+    if (!mbar_wait(&bars.q_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x10 + stage)) return false;
+    mbar_arrive_expect_tx(&bars.q_full[stage], C::kQBytes);
+    uint8_t* dst = smem + C::kOffQ + stage * C::kQBytes;
+#pragma unroll
+    for (int pn = 0; pn < C::kPanels; ++pn)
+      tma_load_4d(tmQ, &bars.q_full[stage], dst + pn * C::kQPanelBytes, pn * C::kPanelElems,
+                  ti.q0 + stage * C::BM, ti.h, ti.b, pol_q);
+    ++q_armed[stage];
+    return true;
+  };
+  auto load_kv = [&](const CUtensorMap* map, int j, const TileInfo& ti, bool withhold) -> bool {
+    const uint32_t slot = it % C::NSLOT;
+    if (!mbar_wait(&bars.kv_empty[slot], ((it / C::NSLOT) & 1u) ^ 1u, wd, 0x12)) return false;
+    ++it;
+    if (withhold) return true;  // test hook: this tile never arrives
+    mbar_arrive_expect_tx(&bars.kv_full[slot], C::kKVBytes);
+    uint8_t* dst = smem + C::kOffKV + slot * C::kKVBytes;
+#pragma unroll
+    for (int pn = 0; pn < C::kPanels; ++pn)
+      tma_load_4d(map, &bars.kv_full[slot], dst + pn * C::kKVPanelBytes, pn * C::kPanelElems,
+                  j * C::BN, ti.h, ti.b, pol_kv);
+    ++kv_armed[slot];
+    return true;
+  };
+
+  for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++tile_k) {
+    const TileInfo ti = tile_info(p, t, C::BN);
+    const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
+    ok = load_q(0, ti) && load_kv(tmK, 0, ti, false) && load_q(1, ti) &&
+         load_kv(tmV, 0, ti, false);
+    for (int j = 1; ok && j < ti.n_kv; ++j)
+      ok = load_kv(tmK, j, ti, inject && j == 1) && load_kv(tmV, j, ti, false);
+  }
+  if (!ok) {
+    // Let copies already in flight land before the CTA's shared memory goes away.
+    const uint64_t limit = 100000000ull;  // 100 ms
+#pragma unroll
+    for (int s = 0; s < C::NSLOT; ++s)
+      if (kv_armed[s]) mbar_drain(&bars.kv_full[s], (kv_armed[s] - 1) & 1u, limit);
+    for (int s = 0; s < 2; ++s)
+      if (q_armed[s]) mbar_drain(&bars.q_full[s], (q_armed[s] - 1) & 1u, limit);
+  }
+}
+
+// -------------------------------------------------------------- MMA warp
+template <class C>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll 1
+  for (int kk = 0; kk < C::D / C::kKStep; ++kk) {
+    const uint32_t byte = kk * 32;
+    const uint32_t pn = byte / 128, in = byte % 128;
+    const uint64_t a = sdesc_sw128<16, 1024>(q_addr + pn * C::kQPanelBytes + in);
+    const uint64_t b = sdesc_sw128<16, 1024>(k_addr + pn * C::kKVPanelBytes + in);
+    mma_ss<C::kTF32>(tmem_s, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
+                                         bool accumulate) {
+#pragma unroll 1
+  for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
+    // V is [BN keys][D] with D contiguous: MN-major B operand.  LBO = distance
+    // between 128-byte column panels, SBO = distance between 8-key row groups.
+    const uint64_t b = sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr + kk * C::kKStep * 128);
+    mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <class C>
+__device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const Bars& bars,
+                            const Watchdog& wd) {
+  const uint32_t q_addr[2] = {smem_u32(smem + C::kOffQ), smem_u32(smem + C::kOffQ + C::kQBytes)};
+  const uint32_t kv_base = smem_u32(smem + C::kOffKV);
+  uint32_t it = 0, tile_k = 0;
+  uint32_t p_par[2] = {0, 0};
+  bool ok = true;
+
+  auto kv_wait = [&](uint32_t i) -> bool {
+    return mbar_wait(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
+  };
+  auto slot_addr = [&](uint32_t i) -> uint32_t { return kv_base + (i % C::NSLOT) * C::kKVBytes; };
+
+  for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++tile_k) {
+    const TileInfo ti = tile_info(p, t, C::BN);
+    const uint32_t par_k = tile_k & 1u;
+    const int n = ti.n_kv;
+    // S_s(0) = Q_s K_0^T for both stages
+    if (!(ok = mbar_wait(&bars.q_full[0], par_k, wd, 0x21) && kv_wait(it))) break;
+    tc_fence_after();
+    issue_qk<C>(tmem + C::col_s(0), q_addr[0], slot_addr(it));
+    tc_commit(&bars.s_full[0]);
+    if (n == 1) tc_commit(&bars.q_empty[0]);
+    if (!(ok = mbar_wait(&bars.q_full[1], par_k, wd, 0x22))) break;
+    tc_fence_after();
+    issue_qk<C>(tmem + C::col_s(1), q_addr[1], slot_addr(it));
+    tc_commit(&bars.s_full[1]);
+    if (n == 1) tc_commit(&bars.q_empty[1]);
+    tc_commit(&bars.kv_empty[it % C::NSLOT]);
+    ++it;
+    // steady state: O_s += P_s(j-1) V_{j-1}, then S_s(j) = Q_s K_j^T
+    for (int j = 1; ok && j <= n; ++j) {
+      const uint32_t iv = it, ik = it + 1;
+      const bool last = (j == n);
+      if (!(ok = kv_wait(iv) && (last || kv_wait(ik)))) break;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!(ok = mbar_wait(&bars.p_full[s], p_par[s], wd, 0x23 + s))) break;
+        p_par[s] ^= 1u;
+        if (j == 1 && !(ok = mbar_wait(&bars.o_empty[s], par_k ^ 1u, wd, 0x25 + s))) break;
+        tc_fence_after();
+        issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), slot_addr(iv), j > 1);
+        if (s == 1) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
+        if (last) {
+          tc_commit(&bars.o_full[s]);
+        } else {
+          issue_qk<C>(tmem + C::col_s(s), q_addr[s], slot_addr(ik));
+          tc_commit(&bars.s_full[s]);
+          if (j == n - 1) tc_commit(&bars.q_empty[s]);
+        }
+      }
+      if (!ok) break;
+      if (last) {
+        it += 1;
+      } else {
+        tc_commit(&bars.kv_empty[ik % C::NSLOT]);
+        it += 2;
+      }
+    }
+  }
+  if (!ok) {
+    // Make sure every MMA already issued has finished before TMEM is released.
+    tc_commit(&bars.teardown[0]);
+    mbar_drain(&bars.teardown[0], 0, 100000000ull);
+  }
+}
+
+// --------------------------------------------------------- softmax warpgroups
+template <class C>
+__device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, const Bars& bars,
+                                float2* stats, const Watchdog& wd) {
+  const int wq = (threadIdx.x / 32) & 3;
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_base + C::col_s(stage);
+  const uint32_t tO = tmem + lane_base + C::col_o(stage);
+  const float sc = p.scale_log2;
+  uint32_t s_par = 0, tile_k = 0;
+
+  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tile_k) {
+    const TileInfo ti = tile_info(p, t, C::BN);
+    const int q = ti.q0 + stage * C::BM + row;
+    const int vis_end = p.causal ? min(p.N_k, q + 1) : p.N_k;  // keys < vis_end are visible
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < ti.n_kv; ++j) {
+      if (!warp_wait(&bars.s_full[stage], s_par, wd, 0x30 + stage)) return;
+      s_par ^= 1u;
+      tc_fence_after();
+      uint32_t s[C::BN];
+#pragma unroll
+      for (int c = 0; c < C::BN; c += 32) tmem_ld32(tS + c, s + c);
+      tmem_ld_wait32(s);
+#pragma unroll
+      for (int c = 32; c < C::BN; c += 32) reg_fence32(s + c);
+
+      const int lim = vis_end - j * C::BN;  // columns c < lim are visible
+      const bool need_mask = __any_sync(0xffffffffu, lim < C::BN);
+      float mx;
+      if (sc >= 0.f) {
+        mx = -INFINITY;
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, c < lim ? __uint_as_float(s[c]) : -INFINITY);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        }
+        mx = (mx == -INFINITY) ? -INFINITY : mx * sc;
+      } else {
+        mx = INFINITY;
+#pragma unroll
+        for (int c = 0; c < C::BN; ++c) mx = fminf(mx, c < lim ? __uint_as_float(s[c]) : INFINITY);
+        mx = (mx == INFINITY) ? -INFINITY : mx * sc;
+      }
+      // lazy rescale: move the applied max only when it grows by more than kTau
+      const float m_new = fmaxf(m_run, mx);
+      const bool bump = m_new > m_run + kTau;
+      float alpha = 1.f;
+      if (bump) {
+        alpha = ex2(m_run - m_new);  // 0 on the first tile (m_run = -inf)
+        m_run = m_new;
+      }
+      l_run *= alpha;
+      if (j > 0 && __any_sync(0xffffffffu, bump)) {
+        // O_s holds sum_{i<j} P_i V_i and no P.V is in flight (S_s(j) was
+        // issued after P_s(j-1).V and its completion was just observed).
+#pragma unroll 1
+        for (int c = 0; c < C::D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait32(o);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(tO + c, o);
+        }
+      }
+      const float neg_m = -m_run;
+      float sum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < C::BN; c0 += 32) {
+        float e[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int c = c0 + k;
+          float v = ex2(fmaf(__uint_as_float(s[c]), sc, neg_m));
+          if (need_mask && c >= lim) v = 0.f;
+          e[k] = v;
+          sum += v;
+        }
+        if constexpr (C::kTF32) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) pw[k] = __float_as_uint(e[k]);
+          tmem_st32(tS + c0, pw);
+        } else {
+          uint32_t pw[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
+          tmem_st16(tS + c0 / 2, pw);
+        }
+      }
+      l_run += sum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[stage]);
+    }
+    // hand the row statistics to the epilogue: 1/l and LSE (natural log)
+    if (!warp_wait(&bars.st_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x32 + stage)) return;
+    stats[stage * C::BM + row] = make_float2(1.f / l_run, (m_run + __log2f(l_run)) * kLn2);
+    mbar_arrive(&bars.st_full[stage]);
+  }
+}
+
+// ------------------------------------------------------- epilogue warpgroup
+template <class C>
+__device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& bars,
+                                 const float2* stats, const Watchdog& wd) {
+  using T = typename C::Elem;
+  const int wq = (threadIdx.x / 32) & 3;
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  uint32_t tile_k = 0;
+  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tile_k) {
+    const TileInfo ti = tile_info(p, t, C::BN);
+#pragma unroll 1
+    for (int s = 0; s < 2; ++s) {
+      if (!warp_wait(&bars.o_full[s], tile_k & 1u, wd, 0x40 + s)) return;
+      if (!warp_wait(&bars.st_full[s], tile_k & 1u, wd, 0x42 + s)) return;
+      tc_fence_after();
+      const float2 st = stats[s * C::BM + row];
+      mbar_arrive(&bars.st_empty[s]);
+      const int q = ti.q0 + s * C::BM + row;
+      const bool valid = q < p.N_q;
+      T* orow = reinterpret_cast<T*>(p.O) + ti.b * p.o_stride[0] + ti.h * p.o_stride[1] +
+                static_cast<long long>(q) * p.o_stride[2];
+      const uint32_t tO = tmem + lane_base + C::col_o(s);
+#pragma unroll 1
+      for (int c = 0; c < C::D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c, o);
+        tmem_ld_wait32(o);
+        if (valid) {
+          if constexpr (C::kTF32) {
+            float4* dst = reinterpret_cast<float4*>(orow + c);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
+                                   __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * st.x, __uint_as_float(o[8 * k + 1]) * st.x);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * st.x, __uint_as_float(o[8 * k + 3]) * st.x);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * st.x, __uint_as_float(o[8 * k + 5]) * st.x);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * st.x, __uint_as_float(o[8 * k + 7]) * st.x);
+              dst[k] = w;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.o_empty[s]);
+      if (valid && p.LSE)
+        p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <class C>
+__global__ void __launch_bounds__(512, 1)
+fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  Bars bars;
+  bars.q_full = bar + 0;
+  bars.q_empty = bar + 2;
+  bars.s_full = bar + 4;
+  bars.p_full = bar + 6;
+  bars.o_full = bar + 8;
+  bars.o_empty = bar + 10;
+  bars.st_full = bar + 12;
+  bars.st_empty = bar + 14;
+  bars.kv_full = bar + 16;
+  bars.kv_empty = bar + 16 + C::NSLOT;
+  bars.teardown = bar + 16 + 2 * C::NSLOT;
+  float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.s_full[s], 1);
+      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.o_full[s], 1);
+      mbar_init(&bars.o_empty[s], 128);
+      mbar_init(&bars.st_full[s], 128);
+      mbar_init(&bars.st_empty[s], 128);
+    }
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    mbar_init(&bars.teardown[0], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 12 && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == 13) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Watchdog wd{abort_flag, p.err, p.timeout_ns};
+
+  const int wg = warp / 4;
+  if (wg == 3) {
+    setmaxnreg_dec<56>();
+    if (warp == 12 && lane == 0) tc_load_role<C>(&tmQ, &tmK, &tmV, p, smem, bars, wd);
+    if (warp == 13 && lane == 0) tc_mma_role<C>(p, smem, tmem, bars, wd);
+  } else if (wg == 2) {
+    setmaxnreg_dec<72>();
+    tc_epilogue_role<C>(p, tmem, bars, stats, wd);
+  } else {
+    setmaxnreg_inc<192>();
+    tc_softmax_role<C>(p, wg, tmem, bars, stats, wd);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,26 @@
+// fa_tc_fp32.cu -- fp32-input (tcgen05 kind::tf32) instantiations of the
+// tensor-core forward kernel.  fp32 tiles are twice the bytes of bf16 ones,
+// so key tiles are 64 wide to keep two 128-row Q tiles plus a K/V ring in
+// shared memory.
+#include "fa_launch.h"
+
+namespace fa {
+
+using CfgFp32D128 = TcCfg<float, 128, 64, 2>;
+using CfgFp32D64 = TcCfg<float, 64, 64, 4>;
+static_assert(CfgFp32D128::BN == tc_key_tile(true) && CfgFp32D64::BN == tc_key_tile(true), "geometry");
+static_assert(CfgFp32D128::kPanelElems == tc_box_inner(true), "geometry");
+
+template <class C>
+static cudaError_t launch(const TcLaunch& L) {
+  cudaError_t e = cudaFuncSetAttribute(fa_tc_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  fa_tc_fwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_fp32_d128(const TcLaunch& L) { return launch<CfgFp32D128>(L); }
+cudaError_t launch_tc_fp32_d64(const TcLaunch& L) { return launch<CfgFp32D64>(L); }
+
+}  // namespace fa

@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""FlashAttention-2 forward benchmark on GB300: TFLOP/s and fraction of the
+tensor-core roofline, one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one forward pass (one launch of the library's kernel) over the
+workload's synthetic inputs, resident in HBM.  Default workload: B=4, H=32,
+N_q=N_k=8192, d=128, bf16, non-causal, scale 1/sqrt(128).  FLOPs per step =
+4*B*H*N_q*N_k*d (halved when causal).  With N GPUs (torchrun) every rank runs
+its own copy of the workload (independent problems, no collective on the data
+path): weak scaling, value = FLOPs of all ranks / slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (the correctness reference) on
+the host cores, on a bounded sample of rows of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25   # dense tf32 / bf16 nominal tensor rates
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="large_nc")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "attention_fa2_fwd_02_gb300" / "csrc").glob("*")):
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = ROOT / "profiles" / "dram_traffic.json"
+    if not p.exists():
+        return None
+    try:
+        d = json.loads(p.read_text())
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    ent = d.get("workloads", {}).get(workload)
+    return None if ent is None else float(ent["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        target = str(self.dev)
+        try:
+            bus = torch.cuda.get_device_properties(self.dev).pci_bus_id  # type: ignore[attr-defined]
+            if bus:
+                target = bus
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", target],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], parts[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return world, rank, local, dist
+    return 1, 0, 0, None
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_desc(w) -> dict:
+    from attention_fa2_fwd_02_gb300.inputs import AxialWorkload
+    if isinstance(w, AxialWorkload):
+        return {"workload": f"axial attention core x[{w.B},{w.Hg},{w.Wg},{w.heads},{w.hd}] fp32, "
+                            f"row + column, scale {w.scale}",
+                "shape": list(w.shape), "scale": w.scale, "causal": False}
+    kind = "causal" if w.causal else "non-causal"
+    dt = "bf16" if w.dtype == torch.bfloat16 else "fp32"
+    return {"workload": f"{w.name}: B={w.B} H={w.H} N_q={w.N_q} N_k={w.N_k} d={w.d} {dt} {kind}, "
+                        f"scale={w.scale:.6g}",
+            "B": w.B, "H": w.H, "N_q": w.N_q, "N_k": w.N_k, "d": w.d, "dtype": dt,
+            "causal": w.causal, "scale": w.scale}
+
+
+def get_workload(name):
+    from attention_fa2_fwd_02_gb300.inputs import AXIAL, WORKLOADS
+    if name == "axial":
+        return AXIAL
+    if name not in WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)} or axial")
+    return WORKLOADS[name]
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_sample(w, Q, K, V, budget_s: float, rows_per_call: int = 512):
+    """Run the oracle (as it stands) on rows of the workload until ~budget_s
+    seconds of CPU work; return (flops, seconds, description)."""
+    import oracle
+    oracle.build()
+    from attention_fa2_fwd_02_gb300.inputs import AxialWorkload
+    if isinstance(w, AxialWorkload):
+        qr = Q.permute(0, 1, 3, 2, 4).reshape(-1, w.Wg, w.hd)
+        kr = K.permute(0, 1, 3, 2, 4).reshape(-1, w.Wg, w.hd)
+        vr = V.permute(0, 1, 3, 2, 4).reshape(-1, w.Wg, w.hd)
+        qc = Q.permute(0, 2, 3, 1, 4).reshape(-1, w.Hg, w.hd)
+        kc = K.permute(0, 2, 3, 1, 4).reshape(-1, w.Hg, w.hd)
+        vc = V.permute(0, 2, 3, 1, 4).reshape(-1, w.Hg, w.hd)
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.attention(qr, kr, vr, w.scale)
+            oracle.attention(qc, kc, vc, w.scale)
+            reps += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return w.flops * reps, dt, f"{reps} full row+column passes of the axial workload"
+    g = np.random.default_rng(0)
+    flops = 0.0
+    n_rows = 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = int(g.integers(w.B)), int(g.integers(w.H))
+        r0 = int(g.integers(0, max(1, w.N_q - rows_per_call + 1)))
+        rows = np.arange(r0, min(w.N_q, r0 + rows_per_call))
+        oracle.attention(Q[b, h], K[b, h], V[b, h], w.scale, w.causal, rows=rows)
+        nvis = np.minimum(rows + 1, w.N_k) if w.causal else np.full(rows.size, w.N_k)
+        flops += float(4.0 * w.d * nvis.sum())
+        n_rows += rows.size
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops, dt, f"{n_rows} query rows ({rows_per_call}-row blocks of random (b,h) slices)"
+
+
+def run_reference(args, w):
+    """--impl reference: the oracle on the host cores, each step a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    Q, K, V = w.make()
+    steps, warm = args.steps, max(3, args.warmup)
+    # size one step so that the whole run takes about two minutes
+    f, dt, _ = oracle_sample(w, Q, K, V, budget_s=0.5)
+    rate = f / dt
+    per_step_s = max(0.02, 120.0 / (steps + warm))
+    from attention_fa2_fwd_02_gb300.inputs import AxialWorkload
+    if isinstance(w, AxialWorkload):
+        sample_desc = "full axial workload (row + column) per step"
+        def step():
+            oracle_sample(w, Q, K, V, budget_s=0.0)
+        step_flops = w.flops
+    else:
+        rows = max(1, min(w.N_q, int(rate * per_step_s / (4.0 * w.d * w.N_k))))
+        g = np.random.default_rng(1)
+        sample_desc = f"{rows} query rows of one random (b,h) slice per step"
+        def step():
+            b, h = int(g.integers(w.B)), int(g.integers(w.H))
+            oracle.attention(Q[b, h], K[b, h], V[b, h], w.scale, w.causal, rows=np.arange(rows))
+        nvis = np.minimum(np.arange(rows) + 1, w.N_k) if w.causal else np.full(rows, w.N_k)
+        step_flops = float(4.0 * w.d * nvis.sum())
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    el = time.perf_counter() - t0
+    val = step_flops * steps / el / 1e12
+    line = {
+        "impl": "reference", "metric": "attention fwd TFLOP/s", "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_desc(w),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+def main():
+    args = parse_args()
+    w = get_workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    import attention_fa2_fwd_02_gb300 as fa
+    from attention_fa2_fwd_02_gb300.inputs import AxialWorkload
+
+    world, rank, local, dist = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.build()
+    warm = max(3, args.warmup)
+    steps = max(1, args.steps)
+    axial = isinstance(w, AxialWorkload)
+    Qh, Kh, Vh = w.make()
+    Qd, Kd, Vd = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = getattr(props, "L2_cache_size", 0) or 129 * 2**20
+    in_bytes = sum(x.numel() * x.element_size() for x in (Qd, Kd, Vd))
+    flush = None
+    if in_bytes <= l2_bytes:
+        flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+
+    if axial:
+        O_row = torch.empty_like(Qd)
+
+        def step():
+            return fa.axial(Qd, Kd, Vd, scale=w.scale, with_lse=True)
+    else:
+        Od = torch.empty_like(Qd)
+        Ld = torch.empty(Qd.shape[:-1], dtype=torch.float32, device=dev)
+
+        def step():
+            return fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, out=Od, lse=Ld)
+
+    for _ in range(warm):
+        if flush is not None:
+            flush.zero_()
+        step()
+    fa.check()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading before the load starts
+    t_start.record(stream)
+    for k in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    fa.check()
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = statistics.mean(launch_ms)
+    wall_ms = t_start.elapsed_time(t_end)
+    # with an L2 flush between steps the step time is the kernel time only
+    step_ms = kernel_ms if flush is not None else wall_ms / steps
+    step_ms = max_over_ranks(step_ms, dist)
+    flops = w.flops
+    value = flops * world / (step_ms * 1e-3) / 1e12
+
+    # --------------------------------------------------------- roofline
+    peaks, peak_src = load_peaks()
+    traffic = recorded_traffic(args.workload)
+    if axial:
+        bytes_per_launch = w.algorithmic_bytes
+        achieved = bytes_per_launch / (kernel_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} hbm_gbs (of {peak_src})"}
+    else:
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        base = float(peaks["bf16_tflops"])
+        if w.dtype == torch.bfloat16:
+            peak, note = base, f"bf16_tflops burst (of {peak_src})"
+        else:
+            peak = base * NOMINAL_TF32_OVER_BF16
+            note = f"bf16_tflops burst x nominal tf32/bf16 ratio 1.1/2.25 (of {peak_src})"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": note}
+
+    # ------------------------------------------------------ end to end
+    e2e = None
+    if not args.no_e2e:
+        Qp, Kp, Vp = (x.pin_memory() for x in (Qh, Kh, Vh))
+        Op = torch.empty(Qh.shape, dtype=Qh.dtype).pin_memory()
+        Lp = torch.empty(Qh.shape[:-1], dtype=torch.float32).pin_memory()
+        if axial:
+            Op2 = torch.empty_like(Op)
+            Lp2 = torch.empty_like(Lp.new_empty(Qh.shape[:-1]))
+
+        def e2e_step():
+            Qd.copy_(Qp, non_blocking=True)
+            Kd.copy_(Kp, non_blocking=True)
+            Vd.copy_(Vp, non_blocking=True)
+            if axial:
+                (o1, l1), (o2, l2) = step()
+                Op.copy_(o1, non_blocking=True)
+                Op2.copy_(o2, non_blocking=True)
+                Lp.copy_(l1, non_blocking=True)
+                Lp2.copy_(l2, non_blocking=True)
+            else:
+                step()
+                Op.copy_(Od, non_blocking=True)
+                Lp.copy_(Ld, non_blocking=True)
+
+        e_steps = max(3, min(steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, dist)
+        h2d = in_bytes
+        d2h = Op.numel() * Op.element_size() + Lp.numel() * 4
+        if axial:
+            d2h *= 2
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        fa.check()
+
+    # ---------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        f, dt, desc = oracle_sample(w, Qh, Kh, Vh, budget_s=args.cpu_seconds)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"{desc}; {dt:.1f} s of fp64 CPU work"}
+
+    if rank == 0:
+        cfg = workload_desc(w)
+        cfg["l2"] = ("inputs larger than L2: %.0f MB vs %.0f MB" % (in_bytes / 2**20, l2_bytes / 2**20)
+                     if flush is None else "L2 flushed (%.0f MB write) between steps" % (flush.numel() * 4 / 2**20))
+        cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
+        line = {
+            "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if (not axial and w.dtype == torch.bfloat16) else ("f32" if axial else "tf32"),
+            "data": "synthetic (seeded i.i.d. N(0,1))", "config": cfg,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": steps, "kernel_ms": kernel_ms,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,144 @@
+/*
+ * fa.h -- C ABI of libfa.so: the FlashAttention-2 forward pass on one GB300
+ * (sm_103a), as hand-written CUDA kernels.
+ *
+ * The operation (sources: "Extend Thunder with CUDA-Python", function
+ * flash_attention_reference, and "Blackwell Attention Example", section
+ * "Attention Kernel Implementation", blackwell_attention_kernel):
+ *
+ *   for every batch b < B, head h < H, query row i < N_q:
+ *     s_ij      = scale * sum_{c<d} Q[b,h,i,c] * K[b,h,j,c]    (keys j < N_k)
+ *     visible j = all j < N_k, or only j <= i when is_causal (top-left
+ *                 alignment: query and key rows both counted from 0)
+ *     LSE[b,h,i] = log sum_{visible j} exp(s_ij)               (natural log)
+ *     O[b,h,i,:] = sum_{visible j} exp(s_ij - LSE[b,h,i]) * V[b,h,j,:]
+ *
+ * computed tile by tile with an online softmax (running row max m and running
+ * sum l, O rescaled when m grows), ending with O/l and LSE = m + log(l).
+ * Arithmetic: S and O accumulate in fp32; the softmax numerator P is rounded
+ * to the input type before P.V (bf16 inputs) or fed as tf32 (fp32 inputs);
+ * O is written in the input type, LSE in fp32.
+ *
+ * Ownership: the caller allocates Q, K, V, O and LSE in device memory and owns
+ * the stream.  A call allocates no device memory and is asynchronous on
+ * `stream` (a cudaStream_t; NULL = the legacy default stream).  The library is
+ * thread-safe; calls on the same stream run in order.
+ *
+ * Errors: every entry point returns a status and never aborts the process.
+ * Argument errors are found on the host before anything is launched.  A
+ * device-side pipeline wait that exceeds its time limit (a bounded wait, never
+ * a hang) makes the kernel stop, raise a device error word and exit cleanly;
+ * fa_check() reports it as FA_ERR_TIMEOUT.  The text of the last error of the
+ * calling thread is available from fa_last_error().
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, stride[3] != 1, non-finite scale */
+  FA_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for (head dim, alignment) */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed (launch, attribute, device query) */
+  FA_ERR_TIMEOUT = 4       /* a kernel's bounded pipeline wait expired; its outputs are undefined */
+} fa_status_t;
+
+typedef enum {
+  FA_BF16 = 0,  /* Q, K, V, O bf16; tensor-core kind::f16 */
+  FA_FP32 = 1   /* Q, K, V, O fp32; tensor-core kind::tf32 (d = 64, 128) or CUDA-core fp32 (d = 16, 32) */
+} fa_dtype_t;
+
+/* A [B, H, N, d] view: element [b,h,n,c] lives at
+ * ptr + (b*stride[0] + h*stride[1] + n*stride[2] + c*stride[3]) elements.
+ * stride[3] must be 1 (each row of d values is contiguous). */
+typedef struct {
+  void* ptr;
+  int64_t stride[4];
+} fa_tensor_t;
+
+/*
+ * fa_fwd -- O, LSE = attention(Q, K, V, scale, is_causal).
+ *
+ *   dtype          element type of Q, K, V and O (LSE is always fp32).
+ *   B, H           batch and head counts (>= 1); Q, K, V, O share them.
+ *   N_q, N_k       query and key/value sequence lengths (>= 1).
+ *   d              head dimension of Q, K, V and O (the same for V).
+ *   Q              [B, H, N_q, d] device view.
+ *   K, V           [B, H, N_k, d] device views.
+ *   scale          multiplier of Q.K (finite; 1/sqrt(d) is the usual choice).
+ *   is_causal      0 or 1; top-left causal mask (key j visible iff j <= i).
+ *   O              [B, H, N_q, d] device view, written.  Must not overlap the inputs.
+ *   LSE            fp32 [B, H, N_q] device array written at
+ *                  LSE + b*lse_stride[0] + h*lse_stride[1] + i*lse_stride[2],
+ *                  or NULL to skip it (lse_stride is then ignored).
+ *   stream         cudaStream_t to launch on.
+ *
+ * Supported: d in {64, 128} on the tensor-core path (bf16 or fp32), which also
+ * needs 16-byte aligned Q/K/V/O base pointers and strides[0..2] * element size
+ * that are multiples of 16 bytes (FA_ERR_UNSUPPORTED otherwise); d in {16, 32}
+ * on the small-head path (any alignment, N_k <= 1024).  Any N_q, N_k >= 1: the
+ * tail of a tile is masked, not required to divide.
+ */
+fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k,
+                   int64_t d, const fa_tensor_t* Q, const fa_tensor_t* K,
+                   const fa_tensor_t* V, float scale, int is_causal,
+                   const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                   void* stream);
+
+/* One problem of a grouped call: the arguments of fa_fwd, by value. */
+typedef struct {
+  int64_t B, H, N_q, N_k, d;
+  fa_tensor_t Q, K, V, O;
+  float* LSE;
+  int64_t lse_stride[3];
+  float scale;
+  int is_causal;
+} fa_problem_t;
+
+/*
+ * fa_fwd_grouped -- several independent problems of one dtype.
+ *
+ * Problems that take the small-head path (d in {16, 32}) all run in ONE
+ * launch; this is how the row and the column attention of the axial workload
+ * (both strided views of the same [B, H, W, heads, hd] tensors) are computed
+ * together.  Any other problem is launched on its own, in order, on `stream`.
+ * Validation of every problem happens before any launch; n = 0 is a no-op.
+ */
+fa_status_t fa_fwd_grouped(fa_dtype_t dtype, int n, const fa_problem_t* problems, void* stream);
+
+/*
+ * fa_check -- synchronise `stream`, then read and clear the device error word
+ * raised by kernels launched from this library on the current device.
+ * Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait expired in some launch since
+ * the last check) or FA_ERR_CUDA (the stream reported an error).
+ */
+fa_status_t fa_check(void* stream);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status_t status);
+
+/* Detail of the last non-OK status returned to the calling thread ("" if none). */
+const char* fa_last_error(void);
+
+/*
+ * Test hooks (process-wide; not for production use).
+ *   timeout_ns   limit of every device-side pipeline wait (0 = default, 1 s).
+ *   debug_flags  bit 0: the tensor-core kernel's load warp withholds one K/V
+ *                tile in block 0, so the consumer's bounded wait runs out and
+ *                the launch ends with FA_ERR_TIMEOUT instead of a hang.
+ */
+void fa_debug_set(uint64_t timeout_ns, int debug_flags);
+
+/* ABI version of this header (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,120 @@
+"""The C-ABI library: it builds for sm_103a, loads, exports every function the
+header declares, and rejects bad arguments on the host (no GPU needed: the
+validation runs before any device call, and no kernel is launched)."""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import attention_fa2_fwd_02_gb300 as fa
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def L():
+    fa.build()
+    return fa.lib()
+
+
+def _declared_functions():
+    text = (ROOT / "include" / "fa.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_api():
+    names = _declared_functions()
+    assert {"fa_fwd", "fa_fwd_grouped", "fa_check", "fa_status_string", "fa_last_error",
+            "fa_debug_set", "fa_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), f"libfa.so does not export {name}"
+
+
+def test_library_is_built_for_sm103a():
+    # the object files are compiled with exactly one -gencode for sm_103a
+    from attention_fa2_fwd_02_gb300 import _build
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert fa.LIB_PATH.exists()
+
+
+def test_status_strings(L):
+    assert L.fa_status_string(0) == b"ok"
+    assert L.fa_status_string(4) == b"device wait timed out"
+    assert L.fa_version() == 100
+
+
+def _t(ptr, strides):
+    return fa.FaTensor(ctypes.c_void_p(ptr), (ctypes.c_int64 * 4)(*strides))
+
+
+def _call(L, dtype=fa.FA_BF16, B=1, H=1, Nq=256, Nk=256, d=128, qptr=0x10000, strides=None,
+          scale=0.1, causal=0, lse=None):
+    s = strides or (Nq * d, Nq * d, d, 1)
+    Q = _t(qptr, s)
+    K = _t(0x20000, s)
+    V = _t(0x30000, s)
+    O = _t(0x40000, s)
+    ls = (ctypes.c_int64 * 3)(Nq, Nq, 1)
+    return L.fa_fwd(dtype, B, H, Nq, Nk, d, ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V),
+                    scale, causal, ctypes.byref(O), lse, ls, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=0), fa.FA_ERR_INVALID_ARG),
+    (dict(qptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(strides=(256 * 128, 256 * 128, 128, 2)), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(qptr=0x10002), fa.FA_ERR_UNSUPPORTED),                     # misaligned base
+    (dict(strides=(256 * 128, 256 * 128, 129, 1)), fa.FA_ERR_UNSUPPORTED),  # odd row stride
+    (dict(strides=(256 * 128, -128, 128, 1)), fa.FA_ERR_UNSUPPORTED),
+])
+def test_host_validation(L, kw, status):
+    assert _call(L, **kw) == status
+    assert L.fa_last_error() != b""
+
+
+def test_null_tensor_struct(L):
+    ls = (ctypes.c_int64 * 3)(1, 1, 1)
+    assert L.fa_fwd(0, 1, 1, 1, 1, 128, None, None, None, 1.0, 0, None, None, ls, None) == \
+        fa.FA_ERR_INVALID_ARG
+
+
+def test_grouped_validates_every_problem_first(L):
+    good = fa.FaProblem()
+    good.B = good.H = 1
+    good.N_q = good.N_k = 64
+    good.d = 16
+    for name in ("Q", "K", "V", "O"):
+        setattr(good, name, _t(0x10000, (64 * 16, 64 * 16, 16, 1)))
+    good.LSE = None
+    good.scale = 0.25
+    bad = fa.FaProblem()
+    ctypes.pointer(bad)[0] = good
+    bad.d = 0
+    arr = (fa.FaProblem * 2)(good, bad)
+    # the bad second problem is reported before anything is launched
+    assert L.fa_fwd_grouped(fa.FA_FP32, 2, arr, None) == fa.FA_ERR_INVALID_ARG
+    assert b"problem 1" in L.fa_last_error()
+    assert L.fa_fwd_grouped(fa.FA_FP32, 0, None, None) == fa.FA_OK
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        fa.fwd(x, x, x)

@@ -157,7 +157,7 @@ fa_status_t make_map(CUtensorMap* map, const fa_tensor_t& t, bool fp32, long lon
 fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const DevState& ds, cudaStream_t stream) {
   const bool fp32 = dtype == FA_FP32;
   const int d = static_cast<int>(pb.d);
-  const int bn = tc_key_tile(fp32);
+  const int bn = tc_key_tile(fp32, d);
   TcLaunch L;
   fa_status_t st;
   if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, d, 128, "Q")) != FA_OK) return st;

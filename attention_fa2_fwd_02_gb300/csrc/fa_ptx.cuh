@@ -265,6 +265,13 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// fp32 -> tf32 (10-bit mantissa) rounded to nearest, ties away from zero; the
+// result is an fp32 bit pattern whose low 13 bits are zero.
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
 // Two fp32 -> packed bf16x2 with round-to-nearest-even (lo in the low half).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

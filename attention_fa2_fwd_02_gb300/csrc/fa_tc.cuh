@@ -70,22 +70,33 @@ struct TcCfg {
   __host__ __device__ static constexpr uint32_t col_s(int s) { return s ? BN : 0; }
   __host__ __device__ static constexpr uint32_t col_o(int s) { return 2 * BN + (s ? D : 0); }
   static constexpr uint32_t kTmemCols = 512;
+  // fp32 inputs: the tensor core takes a tf32 B operand only K-major, so each
+  // V tile is transposed in shared memory into a double-buffered [D][BN] copy
+  // (keys contiguous) before P.V; bf16 V is used in place, MN-major.  The
+  // tensor core also truncates fp32 operands to tf32, so Q, K and V are first
+  // rounded to nearest in shared memory (epilogue warpgroup) and P is rounded
+  // before it is stored.
+  static constexpr bool kVt = kTF32;
+  static constexpr uint32_t kVtBytes = kVt ? D * BN * E : 0;
+  static constexpr uint32_t kVtPanelBytes = D * 128;  // 128-byte column of keys, all D rows
   // shared memory
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQBytes;
-  static constexpr uint32_t kOffBar = kOffKV + NSLOT * kKVBytes;
-  static constexpr int kNumBars = 16 + 2 * NSLOT + 1;
+  static constexpr uint32_t kOffVt = kOffKV + NSLOT * kKVBytes;
+  static constexpr uint32_t kOffBar = kOffVt + 2 * kVtBytes;
+  static constexpr int kNumBars = 22 + 3 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMisc = kOffStats + 2 * BM * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
-  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, 1);
+  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, kVt ? 0u : 1u);
   static constexpr int kThreads = 512;
 
   static_assert(D % kPanelElems == 0, "head dim must fill whole swizzle rows");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
   static_assert(2 * BN + 2 * D <= 512, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(!kVt || NSLOT % 2 == 0, "K and V tiles must alternate ring slots");
 };
 
 struct Bars {
@@ -97,6 +108,10 @@ struct Bars {
   uint64_t* o_empty;    // [2] epilogue -> MMA (128 arrivals)
   uint64_t* st_full;    // [2] softmax -> epilogue: row stats written (128 arrivals)
   uint64_t* st_empty;   // [2] epilogue -> softmax (128 arrivals)
+  uint64_t* vt_full;    // [2] transposer -> MMA (V^T buffer ready; fp32 inputs only)
+  uint64_t* vt_empty;   // [2] MMA -> transposer
+  uint64_t* q_ready;    // [2] Q rounded to tf32 -> MMA (fp32 inputs only)
+  uint64_t* kv_ready;   // [NSLOT] K tile rounded to tf32 -> MMA (fp32 inputs only)
   uint64_t* kv_full;    // [NSLOT]
   uint64_t* kv_empty;   // [NSLOT]
   uint64_t* teardown;   // [1]
@@ -213,9 +228,16 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
                                          bool accumulate) {
 #pragma unroll 1
   for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
-    // V is [BN keys][D] with D contiguous: MN-major B operand.  LBO = distance
-    // between 128-byte column panels, SBO = distance between 8-key row groups.
-    const uint64_t b = sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr + kk * C::kKStep * 128);
+    uint64_t b;
+    if constexpr (C::kVt) {
+      // V^T is [D][BN] with keys contiguous: K-major, like K in Q.K^T.
+      const uint32_t byte = kk * 32;
+      b = sdesc_sw128<16, 1024>(v_addr + (byte / 128) * C::kVtPanelBytes + byte % 128);
+    } else {
+      // V is [BN keys][D] with D contiguous: MN-major B operand.  LBO = distance
+      // between 128-byte column panels, SBO = distance between 8-key row groups.
+      b = sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr + kk * C::kKStep * 128);
+    }
     mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -225,12 +247,16 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
                             const Watchdog& wd) {
   const uint32_t q_addr[2] = {smem_u32(smem + C::kOffQ), smem_u32(smem + C::kOffQ + C::kQBytes)};
   const uint32_t kv_base = smem_u32(smem + C::kOffKV);
-  uint32_t it = 0, tile_k = 0;
+  const uint32_t vt_base = smem_u32(smem + C::kOffVt);
+  uint32_t it = 0, tile_k = 0, vcount = 0;
   uint32_t p_par[2] = {0, 0};
   bool ok = true;
 
+  // K tiles and Q tiles: straight from TMA (bf16) or after tf32 rounding (fp32)
+  uint64_t* const k_bar = C::kVt ? bars.kv_ready : bars.kv_full;
+  uint64_t* const q_bar = C::kVt ? bars.q_ready : bars.q_full;
   auto kv_wait = [&](uint32_t i) -> bool {
-    return mbar_wait(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
+    return mbar_wait(&k_bar[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
   };
   auto slot_addr = [&](uint32_t i) -> uint32_t { return kv_base + (i % C::NSLOT) * C::kKVBytes; };
 
@@ -239,12 +265,12 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     const uint32_t par_k = tile_k & 1u;
     const int n = ti.n_kv;
     // S_s(0) = Q_s K_0^T for both stages
-    if (!(ok = mbar_wait(&bars.q_full[0], par_k, wd, 0x21) && kv_wait(it))) break;
+    if (!(ok = mbar_wait(&q_bar[0], par_k, wd, 0x21) && kv_wait(it))) break;
     tc_fence_after();
     issue_qk<C>(tmem + C::col_s(0), q_addr[0], slot_addr(it));
     tc_commit(&bars.s_full[0]);
     if (n == 1) tc_commit(&bars.q_empty[0]);
-    if (!(ok = mbar_wait(&bars.q_full[1], par_k, wd, 0x22))) break;
+    if (!(ok = mbar_wait(&q_bar[1], par_k, wd, 0x22))) break;
     tc_fence_after();
     issue_qk<C>(tmem + C::col_s(1), q_addr[1], slot_addr(it));
     tc_commit(&bars.s_full[1]);
@@ -255,15 +281,22 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     for (int j = 1; ok && j <= n; ++j) {
       const uint32_t iv = it, ik = it + 1;
       const bool last = (j == n);
-      if (!(ok = kv_wait(iv) && (last || kv_wait(ik)))) break;
+      const uint32_t vb = vcount & 1u;
+      bool v_ready;
+      if constexpr (C::kVt)
+        v_ready = mbar_wait(&bars.vt_full[vb], (vcount >> 1) & 1u, wd, 0x27);
+      else
+        v_ready = kv_wait(iv);
+      if (!(ok = v_ready && (last || kv_wait(ik)))) break;
+      const uint32_t v_addr = C::kVt ? vt_base + vb * C::kVtBytes : slot_addr(iv);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (!(ok = mbar_wait(&bars.p_full[s], p_par[s], wd, 0x23 + s))) break;
         p_par[s] ^= 1u;
         if (j == 1 && !(ok = mbar_wait(&bars.o_empty[s], par_k ^ 1u, wd, 0x25 + s))) break;
         tc_fence_after();
-        issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), slot_addr(iv), j > 1);
-        if (s == 1) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
+        issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), v_addr, j > 1);
+        if (s == 1) tc_commit(C::kVt ? &bars.vt_empty[vb] : &bars.kv_empty[iv % C::NSLOT]);
         if (last) {
           tc_commit(&bars.o_full[s]);
         } else {
@@ -273,6 +306,7 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
         }
       }
       if (!ok) break;
+      ++vcount;
       if (last) {
         it += 1;
       } else {
@@ -319,22 +353,38 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
 
       const int lim = vis_end - j * C::BN;  // columns c < lim are visible
       const bool need_mask = __any_sync(0xffffffffu, lim < C::BN);
+      // Row max with kAcc independent chains (a single chain of BN dependent
+      // max operations would put its full latency on the critical path).
+      constexpr int kAcc = 8;
+      float acc[kAcc];
       float mx;
       if (sc >= 0.f) {
-        mx = -INFINITY;
+#pragma unroll
+        for (int a = 0; a < kAcc; ++a) acc[a] = -INFINITY;
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, c < lim ? __uint_as_float(s[c]) : -INFINITY);
+          for (int c = 0; c < C::BN; ++c)
+            acc[c % kAcc] = fmaxf(acc[c % kAcc], c < lim ? __uint_as_float(s[c]) : -INFINITY);
         } else {
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+          for (int c = 0; c < C::BN; ++c) acc[c % kAcc] = fmaxf(acc[c % kAcc], __uint_as_float(s[c]));
         }
-        mx = (mx == -INFINITY) ? -INFINITY : mx * sc;
-      } else {
-        mx = INFINITY;
 #pragma unroll
-        for (int c = 0; c < C::BN; ++c) mx = fminf(mx, c < lim ? __uint_as_float(s[c]) : INFINITY);
-        mx = (mx == INFINITY) ? -INFINITY : mx * sc;
+        for (int w = kAcc / 2; w > 0; w /= 2)
+#pragma unroll
+          for (int a = 0; a < w; ++a) acc[a] = fmaxf(acc[a], acc[a + w]);
+        mx = (acc[0] == -INFINITY) ? -INFINITY : acc[0] * sc;
+      } else {
+#pragma unroll
+        for (int a = 0; a < kAcc; ++a) acc[a] = INFINITY;
+#pragma unroll
+        for (int c = 0; c < C::BN; ++c)
+          acc[c % kAcc] = fminf(acc[c % kAcc], c < lim ? __uint_as_float(s[c]) : INFINITY);
+#pragma unroll
+        for (int w = kAcc / 2; w > 0; w /= 2)
+#pragma unroll
+          for (int a = 0; a < w; ++a) acc[a] = fminf(acc[a], acc[a + w]);
+        mx = (acc[0] == INFINITY) ? -INFINITY : acc[0] * sc;
       }
       // lazy rescale: move the applied max only when it grows by more than kTau
       const float m_new = fmaxf(m_run, mx);
@@ -359,7 +409,8 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
         }
       }
       const float neg_m = -m_run;
-      float sum = 0.f;
+#pragma unroll
+      for (int a = 0; a < kAcc; ++a) acc[a] = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
         float e[32];
@@ -368,8 +419,9 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
           const int c = c0 + k;
           float v = ex2(fmaf(__uint_as_float(s[c]), sc, neg_m));
           if (need_mask && c >= lim) v = 0.f;
+          if constexpr (C::kTF32) v = to_tf32(v);  // l sums exactly the P that P.V uses
           e[k] = v;
-          sum += v;
+          acc[k % kAcc] += v;
         }
         if constexpr (C::kTF32) {
           uint32_t pw[32];
@@ -383,6 +435,11 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
           tmem_st16(tS + c0 / 2, pw);
         }
       }
+#pragma unroll
+      for (int w = kAcc / 2; w > 0; w /= 2)
+#pragma unroll
+        for (int a = 0; a < w; ++a) acc[a] += acc[a + w];
+      const float sum = acc[0];
       l_run += sum;
       tmem_st_wait();
       tc_fence_before();
@@ -396,17 +453,103 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
 }
 
 // ------------------------------------------------------- epilogue warpgroup
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// fp32 inputs: V tile at ring index iv ([BN keys][D], 128-byte swizzled panels
+// of 32 d-values, as TMA wrote it) -> V^T buffer ([D][BN], panels of 32 keys).
+// Lane = key: each thread reads 16 bytes of its key row (the swizzle puts the
+// 8 rows of a phase on distinct banks) and writes 4 rows of V^T, where the 32
+// lanes fill one 128-byte row (no bank conflicts either).  The four warps
+// split the head dim.  Releases the ring slot and publishes the V^T buffer.
 template <class C>
-__device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& bars,
+__device__ __forceinline__ bool transpose_v(uint8_t* smem, const Bars& bars, uint32_t iv,
+                                            uint32_t vcount, const Watchdog& wd) {
+  const uint32_t slot = iv % C::NSLOT;
+  const uint32_t vb = vcount & 1u;
+  if (!warp_wait(&bars.kv_full[slot], (iv / C::NSLOT) & 1u, wd, 0x50)) return false;
+  if (!warp_wait(&bars.vt_empty[vb], ((vcount >> 1) & 1u) ^ 1u, wd, 0x51)) return false;
+  const uint8_t* src = smem + C::kOffKV + slot * C::kKVBytes;
+  uint8_t* dst = smem + C::kOffVt + vb * C::kVtBytes;
+  const int wq = (threadIdx.x / 32) & 3;
+  const int lane = threadIdx.x & 31;
+  constexpr int kDPerWarp = C::D / 4;
+  const uint32_t wchunk = lane / 4, within = (lane % 4) * 4;
+#pragma unroll
+  for (int g = 0; g < C::BN / 32; ++g) {
+    const int k = g * 32 + lane;
+#pragma unroll 4
+    for (int n0 = wq * kDPerWarp; n0 < (wq + 1) * kDPerWarp; n0 += 4) {
+      const int pn = n0 / 32, chunk = (n0 % 32) / 4;
+      const float4 v = *reinterpret_cast<const float4*>(src + pn * C::kKVPanelBytes + k * 128 +
+                                                        ((chunk ^ (k & 7)) << 4));
+      const float vv[4] = {to_tf32(v.x), to_tf32(v.y), to_tf32(v.z), to_tf32(v.w)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int nn = n0 + e;
+        *reinterpret_cast<float*>(dst + g * C::kVtPanelBytes + nn * 128 + ((wchunk ^ (nn & 7)) << 4) +
+                                  within) = vv[e];
+      }
+    }
+  }
+  fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+  named_barrier_sync(1, 128);
+  if ((threadIdx.x & 127) == 0) {
+    mbar_arrive(&bars.kv_empty[slot]);
+    mbar_arrive(&bars.vt_full[vb]);
+  }
+  return true;
+}
+
+// fp32 inputs: round a TMA-filled buffer to tf32 in place (elementwise, so the
+// swizzle does not matter; consecutive threads touch consecutive 16 bytes),
+// then publish it to the MMA warp through `ready`.
+__device__ __forceinline__ void round_tf32_publish(uint8_t* buf, uint32_t bytes, uint64_t* ready) {
+  for (uint32_t off = (threadIdx.x & 127) * 16; off < bytes; off += 128 * 16) {
+    float4* q = reinterpret_cast<float4*>(buf + off);
+    float4 v = *q;
+    v.x = to_tf32(v.x);
+    v.y = to_tf32(v.y);
+    v.z = to_tf32(v.z);
+    v.w = to_tf32(v.w);
+    *q = v;
+  }
+  fence_proxy_async_smem();
+  named_barrier_sync(1, 128);
+  if ((threadIdx.x & 127) == 0) mbar_arrive(ready);
+}
+
+template <class C>
+__device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const Bars& bars,
                                  const float2* stats, const Watchdog& wd) {
   using T = typename C::Elem;
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  uint32_t tile_k = 0;
+  uint32_t tile_k = 0, it = 0, vcount = 0;
   for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tile_k) {
     const TileInfo ti = tile_info(p, t, C::BN);
+    if constexpr (C::kVt) {
+      // same order as the load warp: Q_0, K_0, Q_1, V_0, then K_j, V_j
+      auto do_q = [&](int s) -> bool {
+        if (!warp_wait(&bars.q_full[s], tile_k & 1u, wd, 0x52 + s)) return false;
+        round_tf32_publish(smem + C::kOffQ + s * C::kQBytes, C::kQBytes, &bars.q_ready[s]);
+        return true;
+      };
+      auto do_k = [&](uint32_t i) -> bool {
+        const uint32_t slot = i % C::NSLOT;
+        if (!warp_wait(&bars.kv_full[slot], (i / C::NSLOT) & 1u, wd, 0x54)) return false;
+        round_tf32_publish(smem + C::kOffKV + slot * C::kKVBytes, C::kKVBytes, &bars.kv_ready[slot]);
+        return true;
+      };
+      if (!(do_q(0) && do_k(it) && do_q(1))) return;
+      for (int j = 0; j < ti.n_kv; ++j, it += 2, ++vcount) {
+        if (j > 0 && !do_k(it)) return;
+        if (!transpose_v<C>(smem, bars, it + 1, vcount, wd)) return;
+      }
+    }
 #pragma unroll 1
     for (int s = 0; s < 2; ++s) {
       if (!warp_wait(&bars.o_full[s], tile_k & 1u, wd, 0x40 + s)) return;
@@ -470,9 +613,13 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   bars.o_empty = bar + 10;
   bars.st_full = bar + 12;
   bars.st_empty = bar + 14;
-  bars.kv_full = bar + 16;
-  bars.kv_empty = bar + 16 + C::NSLOT;
-  bars.teardown = bar + 16 + 2 * C::NSLOT;
+  bars.vt_full = bar + 16;
+  bars.vt_empty = bar + 18;
+  bars.q_ready = bar + 20;
+  bars.kv_full = bar + 22;
+  bars.kv_empty = bar + 22 + C::NSLOT;
+  bars.kv_ready = bar + 22 + 2 * C::NSLOT;
+  bars.teardown = bar + 22 + 3 * C::NSLOT;
   float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -489,10 +636,14 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&bars.o_empty[s], 128);
       mbar_init(&bars.st_full[s], 128);
       mbar_init(&bars.st_empty[s], 128);
+      mbar_init(&bars.vt_full[s], 1);
+      mbar_init(&bars.vt_empty[s], 1);
+      mbar_init(&bars.q_ready[s], 1);
     }
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.kv_ready[s], 1);
     }
     mbar_init(&bars.teardown[0], 1);
     *abort_flag = 0;
@@ -520,7 +671,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (warp == 13 && lane == 0) tc_mma_role<C>(p, smem, tmem, bars, wd);
   } else if (wg == 2) {
     setmaxnreg_dec<72>();
-    tc_epilogue_role<C>(p, tmem, bars, stats, wd);
+    tc_epilogue_role<C>(p, smem, tmem, bars, stats, wd);
   } else {
     setmaxnreg_inc<192>();
     tc_softmax_role<C>(p, wg, tmem, bars, stats, wd);

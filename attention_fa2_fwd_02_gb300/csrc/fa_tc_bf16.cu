@@ -8,7 +8,7 @@ namespace fa {
 
 using CfgBf16D128 = TcCfg<__nv_bfloat16, 128, 128, 4>;
 using CfgBf16D64 = TcCfg<__nv_bfloat16, 64, 128, 6>;
-static_assert(CfgBf16D128::BN == tc_key_tile(false) && CfgBf16D64::BN == tc_key_tile(false), "geometry");
+static_assert(CfgBf16D128::BN == tc_key_tile(false, 128) && CfgBf16D64::BN == tc_key_tile(false, 64), "geometry");
 static_assert(CfgBf16D128::kPanelElems == tc_box_inner(false), "geometry");
 
 template <class C>

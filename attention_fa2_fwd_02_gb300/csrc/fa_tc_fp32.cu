@@ -1,14 +1,15 @@
 // fa_tc_fp32.cu -- fp32-input (tcgen05 kind::tf32) instantiations of the
-// tensor-core forward kernel.  fp32 tiles are twice the bytes of bf16 ones,
-// so key tiles are 64 wide to keep two 128-row Q tiles plus a K/V ring in
-// shared memory.
+// tensor-core forward kernel.  fp32 tiles are twice the bytes of bf16 ones and
+// V also needs a transposed copy (tf32 B operands are K-major only), so key
+// tiles are 32 (d = 128) or 64 (d = 64) wide to keep two 128-row Q tiles, the
+// K/V ring and the V^T buffers in shared memory.
 #include "fa_launch.h"
 
 namespace fa {
 
-using CfgFp32D128 = TcCfg<float, 128, 64, 2>;
+using CfgFp32D128 = TcCfg<float, 128, 32, 2>;
 using CfgFp32D64 = TcCfg<float, 64, 64, 4>;
-static_assert(CfgFp32D128::BN == tc_key_tile(true) && CfgFp32D64::BN == tc_key_tile(true), "geometry");
+static_assert(CfgFp32D128::BN == tc_key_tile(true, 128) && CfgFp32D64::BN == tc_key_tile(true, 64), "geometry");
 static_assert(CfgFp32D128::kPanelElems == tc_box_inner(true), "geometry");
 
 template <class C>

@@ -187,6 +187,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
+// One lane of a converged warp (the same lane every time) returns true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator.
 // ab_fmt: 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32).  major: 0 = K-major,
 // 1 = MN-major.  N >> 3 at bit 17, M >> 4 at bit 24.

@@ -91,6 +91,12 @@ struct TcCfg {
   static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
   static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, kVt ? 0u : 1u);
   static constexpr int kThreads = 512;
+  // Register split (setmaxnreg) of the 4 warpgroups; 128 registers x 512
+  // threads at launch, so the shares must add up to 4 x 128.
+  static constexpr uint32_t kRegSoftmax = 184;
+  static constexpr uint32_t kRegEpilogue = kTF32 ? 88 : 64;  // fp32: also rounds and transposes
+  static constexpr uint32_t kRegProducer = kTF32 ? 56 : 80;  // load warp + MMA warp
+  static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 4 * 128, "register split");
 
   static_assert(D % kPanelElems == 0, "head dim must fill whole swizzle rows");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
@@ -157,11 +163,9 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
                              const TcParams& p, uint8_t* smem, const Bars& bars, const Watchdog& wd) {
   const uint64_t pol_q = l2_policy_evict_first();
   const uint64_t pol_kv = l2_policy_evict_last();
-  uint32_t it = 0;
-  uint32_t kv_armed[C::NSLOT];
-  uint32_t q_armed[2] = {0, 0};
-#pragma unroll
-  for (int s = 0; s < C::NSLOT; ++s) kv_armed[s] = 0;
+  uint32_t it = 0;          // ring entries handed out so far
+  uint32_t withheld = ~0u;  // ring entry skipped by the test hook, if any
+  uint32_t q_armed0 = 0, q_armed1 = 0;
   bool ok = true;
   uint32_t tile_k = 0;
 
@@ -173,21 +177,23 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(tmQ, &bars.q_full[stage], dst + pn * C::kQPanelBytes, pn * C::kPanelElems,
                   ti.q0 + stage * C::BM, ti.h, ti.b, pol_q);
-    ++q_armed[stage];
+    if (stage == 0) ++q_armed0; else ++q_armed1;
     return true;
   };
   auto load_kv = [&](const CUtensorMap* map, int j, const TileInfo& ti, bool withhold) -> bool {
     const uint32_t slot = it % C::NSLOT;
     if (!mbar_wait(&bars.kv_empty[slot], ((it / C::NSLOT) & 1u) ^ 1u, wd, 0x12)) return false;
     ++it;
-    if (withhold) return true;  // test hook: this tile never arrives
+    if (withhold) {  // test hook: this tile never arrives
+      withheld = it - 1;
+      return true;
+    }
     mbar_arrive_expect_tx(&bars.kv_full[slot], C::kKVBytes);
     uint8_t* dst = smem + C::kOffKV + slot * C::kKVBytes;
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(map, &bars.kv_full[slot], dst + pn * C::kKVPanelBytes, pn * C::kPanelElems,
                   j * C::BN, ti.h, ti.b, pol_kv);
-    ++kv_armed[slot];
     return true;
   };
 
@@ -201,62 +207,80 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
   }
   if (!ok) {
     // Let copies already in flight land before the CTA's shared memory goes away.
+    // Only the last NSLOT ring entries can still be in flight.
     const uint64_t limit = 100000000ull;  // 100 ms
-#pragma unroll
-    for (int s = 0; s < C::NSLOT; ++s)
-      if (kv_armed[s]) mbar_drain(&bars.kv_full[s], (kv_armed[s] - 1) & 1u, limit);
-    for (int s = 0; s < 2; ++s)
-      if (q_armed[s]) mbar_drain(&bars.q_full[s], (q_armed[s] - 1) & 1u, limit);
+    for (uint32_t i = it > C::NSLOT ? it - C::NSLOT : 0; i < it; ++i)
+      if (i != withheld) mbar_drain(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, limit);
+    if (q_armed0) mbar_drain(&bars.q_full[0], (q_armed0 - 1) & 1u, limit);
+    if (q_armed1) mbar_drain(&bars.q_full[1], (q_armed1 - 1) & 1u, limit);
   }
 }
 
 // -------------------------------------------------------------- MMA warp
+// The descriptor of each operand is built once per call; every k-step adds a
+// compile-time offset to its start-address field (16-byte units; operands
+// live below 256 KB so the 14-bit field never carries).  The loops unroll, the
+// instruction descriptors are immediates and the values are warp-uniform, so
+// issuing costs a few instructions per MMA.
+// Copy of a value the compiler may not hoist or rematerialise: keeps the
+// per-k-step descriptors of loop-invariant operands (Q) from being precomputed
+// into registers for the whole tile loop.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(x));
+  return x;
+}
+
 template <class C>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
-#pragma unroll 1
+  const uint64_t a0 = sdesc_sw128<16, 1024>(opaque(q_addr));
+  const uint64_t b0 = sdesc_sw128<16, 1024>(k_addr);
+#pragma unroll
   for (int kk = 0; kk < C::D / C::kKStep; ++kk) {
-    const uint32_t byte = kk * 32;
-    const uint32_t pn = byte / 128, in = byte % 128;
-    const uint64_t a = sdesc_sw128<16, 1024>(q_addr + pn * C::kQPanelBytes + in);
-    const uint64_t b = sdesc_sw128<16, 1024>(k_addr + pn * C::kKVPanelBytes + in);
-    mma_ss<C::kTF32>(tmem_s, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+    constexpr uint32_t kStep = 32;  // bytes of K per MMA
+    const uint32_t byte = kk * kStep;
+    const uint32_t a_off = ((byte / 128) * C::kQPanelBytes + byte % 128) >> 4;
+    const uint32_t b_off = ((byte / 128) * C::kKVPanelBytes + byte % 128) >> 4;
+    mma_ss<C::kTF32>(tmem_s, a0 + a_off, b0 + b_off, C::kIdescS, kk > 0 ? 1u : 0u);
   }
 }
 
 template <class C>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
                                          bool accumulate) {
-#pragma unroll 1
+  // bf16: V is [BN keys][D] with D contiguous, an MN-major B operand (LBO =
+  // distance between 128-byte column panels, SBO = between 8-key row groups).
+  // fp32: V^T is [D][BN] with keys contiguous, K-major like K in Q.K^T.
+  const uint64_t b0 = C::kVt ? sdesc_sw128<16, 1024>(v_addr)
+                             : sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr);
+#pragma unroll
   for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
-    uint64_t b;
+    uint32_t b_off;
     if constexpr (C::kVt) {
-      // V^T is [D][BN] with keys contiguous: K-major, like K in Q.K^T.
       const uint32_t byte = kk * 32;
-      b = sdesc_sw128<16, 1024>(v_addr + (byte / 128) * C::kVtPanelBytes + byte % 128);
+      b_off = ((byte / 128) * C::kVtPanelBytes + byte % 128) >> 4;
     } else {
-      // V is [BN keys][D] with D contiguous: MN-major B operand.  LBO = distance
-      // between 128-byte column panels, SBO = distance between 8-key row groups.
-      b = sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr + kk * C::kKStep * 128);
+      b_off = (kk * C::kKStep * 128) >> 4;
     }
-    mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b0 + b_off, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// Executed by the whole MMA warp: waits are warp-wide, one elected lane (always
+// the same one, so its tcgen05.commit covers every MMA) issues.
 template <class C>
 __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const Bars& bars,
                             const Watchdog& wd) {
-  const uint32_t q_addr[2] = {smem_u32(smem + C::kOffQ), smem_u32(smem + C::kOffQ + C::kQBytes)};
+  const uint32_t q_addr0 = smem_u32(smem + C::kOffQ);
   const uint32_t kv_base = smem_u32(smem + C::kOffKV);
   const uint32_t vt_base = smem_u32(smem + C::kOffVt);
   uint32_t it = 0, tile_k = 0, vcount = 0;
   uint32_t p_par[2] = {0, 0};
   bool ok = true;
-
   // K tiles and Q tiles: straight from TMA (bf16) or after tf32 rounding (fp32)
   uint64_t* const k_bar = C::kVt ? bars.kv_ready : bars.kv_full;
   uint64_t* const q_bar = C::kVt ? bars.q_ready : bars.q_full;
   auto kv_wait = [&](uint32_t i) -> bool {
-    return mbar_wait(&k_bar[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
+    return warp_wait(&k_bar[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
   };
   auto slot_addr = [&](uint32_t i) -> uint32_t { return kv_base + (i % C::NSLOT) * C::kKVBytes; };
 
@@ -265,17 +289,19 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     const uint32_t par_k = tile_k & 1u;
     const int n = ti.n_kv;
     // S_s(0) = Q_s K_0^T for both stages
-    if (!(ok = mbar_wait(&q_bar[0], par_k, wd, 0x21) && kv_wait(it))) break;
-    tc_fence_after();
-    issue_qk<C>(tmem + C::col_s(0), q_addr[0], slot_addr(it));
-    tc_commit(&bars.s_full[0]);
-    if (n == 1) tc_commit(&bars.q_empty[0]);
-    if (!(ok = mbar_wait(&q_bar[1], par_k, wd, 0x22))) break;
-    tc_fence_after();
-    issue_qk<C>(tmem + C::col_s(1), q_addr[1], slot_addr(it));
-    tc_commit(&bars.s_full[1]);
-    if (n == 1) tc_commit(&bars.q_empty[1]);
-    tc_commit(&bars.kv_empty[it % C::NSLOT]);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (!(ok = warp_wait(&q_bar[s], par_k, wd, 0x21 + s) && (s == 1 || kv_wait(it)))) break;
+      tc_fence_after();
+      if (elect_one()) {
+        issue_qk<C>(tmem + C::col_s(s), q_addr0 + s * C::kQBytes, slot_addr(it));
+        tc_commit(&bars.s_full[s]);
+        if (n == 1) tc_commit(&bars.q_empty[s]);
+        if (s == 1) tc_commit(&bars.kv_empty[it % C::NSLOT]);
+      }
+      __syncwarp();
+    }
+    if (!ok) break;
     ++it;
     // steady state: O_s += P_s(j-1) V_{j-1}, then S_s(j) = Q_s K_j^T
     for (int j = 1; ok && j <= n; ++j) {
@@ -284,40 +310,41 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
       const uint32_t vb = vcount & 1u;
       bool v_ready;
       if constexpr (C::kVt)
-        v_ready = mbar_wait(&bars.vt_full[vb], (vcount >> 1) & 1u, wd, 0x27);
+        v_ready = warp_wait(&bars.vt_full[vb], (vcount >> 1) & 1u, wd, 0x27);
       else
         v_ready = kv_wait(iv);
       if (!(ok = v_ready && (last || kv_wait(ik)))) break;
       const uint32_t v_addr = C::kVt ? vt_base + vb * C::kVtBytes : slot_addr(iv);
+      const uint32_t k_addr = slot_addr(ik);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
-        if (!(ok = mbar_wait(&bars.p_full[s], p_par[s], wd, 0x23 + s))) break;
+        if (!(ok = warp_wait(&bars.p_full[s], p_par[s], wd, 0x23 + s))) break;
         p_par[s] ^= 1u;
-        if (j == 1 && !(ok = mbar_wait(&bars.o_empty[s], par_k ^ 1u, wd, 0x25 + s))) break;
+        if (j == 1 && !(ok = warp_wait(&bars.o_empty[s], par_k ^ 1u, wd, 0x25 + s))) break;
         tc_fence_after();
-        issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), v_addr, j > 1);
-        if (s == 1) tc_commit(C::kVt ? &bars.vt_empty[vb] : &bars.kv_empty[iv % C::NSLOT]);
-        if (last) {
-          tc_commit(&bars.o_full[s]);
-        } else {
-          issue_qk<C>(tmem + C::col_s(s), q_addr[s], slot_addr(ik));
-          tc_commit(&bars.s_full[s]);
-          if (j == n - 1) tc_commit(&bars.q_empty[s]);
+        if (elect_one()) {
+          issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), v_addr, j > 1);
+          if (s == 1) tc_commit(C::kVt ? &bars.vt_empty[vb] : &bars.kv_empty[iv % C::NSLOT]);
+          if (last) {
+            tc_commit(&bars.o_full[s]);
+          } else {
+            issue_qk<C>(tmem + C::col_s(s), q_addr0 + s * C::kQBytes, k_addr);
+            tc_commit(&bars.s_full[s]);
+            if (j == n - 1) tc_commit(&bars.q_empty[s]);
+            if (s == 1) tc_commit(&bars.kv_empty[ik % C::NSLOT]);
+          }
         }
+        __syncwarp();
       }
       if (!ok) break;
       ++vcount;
-      if (last) {
-        it += 1;
-      } else {
-        tc_commit(&bars.kv_empty[ik % C::NSLOT]);
-        it += 2;
-      }
+      it += last ? 1 : 2;
     }
   }
   if (!ok) {
     // Make sure every MMA already issued has finished before TMEM is released.
-    tc_commit(&bars.teardown[0]);
+    if (elect_one()) tc_commit(&bars.teardown[0]);
+    __syncwarp();
     mbar_drain(&bars.teardown[0], 0, 100000000ull);
   }
 }
@@ -666,14 +693,14 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   const int wg = warp / 4;
   if (wg == 3) {
-    setmaxnreg_dec<56>();
+    setmaxnreg_dec<C::kRegProducer>();
     if (warp == 12 && lane == 0) tc_load_role<C>(&tmQ, &tmK, &tmV, p, smem, bars, wd);
-    if (warp == 13 && lane == 0) tc_mma_role<C>(p, smem, tmem, bars, wd);
+    if (warp == 13) tc_mma_role<C>(p, smem, tmem, bars, wd);
   } else if (wg == 2) {
-    setmaxnreg_dec<72>();
+    setmaxnreg_dec<C::kRegEpilogue>();
     tc_epilogue_role<C>(p, smem, tmem, bars, stats, wd);
   } else {
-    setmaxnreg_inc<192>();
+    setmaxnreg_inc<C::kRegSoftmax>();
     tc_softmax_role<C>(p, wg, tmem, bars, stats, wd);
   }
   tc_fence_before();

@@ -380,8 +380,9 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
 
       const int lim = vis_end - j * C::BN;  // columns c < lim are visible
       const bool need_mask = __any_sync(0xffffffffu, lim < C::BN);
-      // Row max with kAcc independent chains (a single chain of BN dependent
-      // max operations would put its full latency on the critical path).
+      // Row max: three-input max over pairs, in kAcc independent chains (one
+      // chain of BN dependent operations would put its whole latency on the
+      // critical path).
       constexpr int kAcc = 8;
       float acc[kAcc];
       float mx;
@@ -390,11 +391,13 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
         for (int a = 0; a < kAcc; ++a) acc[a] = -INFINITY;
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c)
-            acc[c % kAcc] = fmaxf(acc[c % kAcc], c < lim ? __uint_as_float(s[c]) : -INFINITY);
+          for (int c = 0; c < C::BN; c += 2)
+            acc[(c / 2) % kAcc] = max3f(acc[(c / 2) % kAcc], c < lim ? __uint_as_float(s[c]) : -INFINITY,
+                                        c + 1 < lim ? __uint_as_float(s[c + 1]) : -INFINITY);
         } else {
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c) acc[c % kAcc] = fmaxf(acc[c % kAcc], __uint_as_float(s[c]));
+          for (int c = 0; c < C::BN; c += 2)
+            acc[(c / 2) % kAcc] = max3f(acc[(c / 2) % kAcc], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
         }
 #pragma unroll
         for (int w = kAcc / 2; w > 0; w /= 2)
@@ -405,8 +408,9 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
 #pragma unroll
         for (int a = 0; a < kAcc; ++a) acc[a] = INFINITY;
 #pragma unroll
-        for (int c = 0; c < C::BN; ++c)
-          acc[c % kAcc] = fminf(acc[c % kAcc], c < lim ? __uint_as_float(s[c]) : INFINITY);
+        for (int c = 0; c < C::BN; c += 2)
+          acc[(c / 2) % kAcc] = min3f(acc[(c / 2) % kAcc], c < lim ? __uint_as_float(s[c]) : INFINITY,
+                                      c + 1 < lim ? __uint_as_float(s[c + 1]) : INFINITY);
 #pragma unroll
         for (int w = kAcc / 2; w > 0; w /= 2)
 #pragma unroll
@@ -435,20 +439,32 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
           tmem_st32(tO + c, o);
         }
       }
-      const float neg_m = -m_run;
+      // p = 2^(s*c - m) on pairs: packed FMA for the argument, ex2 on the
+      // special-function unit, packed adds into kAcc/2 pair accumulators.
+      const float2 sc2 = make_float2(sc, sc);
+      const float2 nm2 = make_float2(-m_run, -m_run);
+      float2 sum2[kAcc / 2];
 #pragma unroll
-      for (int a = 0; a < kAcc; ++a) acc[a] = 0.f;
+      for (int a = 0; a < kAcc / 2; ++a) sum2[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c0 = 0; c0 < C::BN; c0 += 32) {
         float e[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < 32; k += 2) {
           const int c = c0 + k;
-          float v = ex2(fmaf(__uint_as_float(s[c]), sc, neg_m));
-          if (need_mask && c >= lim) v = 0.f;
-          if constexpr (C::kTF32) v = to_tf32(v);  // l sums exactly the P that P.V uses
-          e[k] = v;
-          acc[k % kAcc] += v;
+          const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+          float v0 = ex2(x.x), v1 = ex2(x.y);
+          if (need_mask) {
+            if (c >= lim) v0 = 0.f;
+            if (c + 1 >= lim) v1 = 0.f;
+          }
+          if constexpr (C::kTF32) {  // l sums exactly the P that P.V uses
+            v0 = to_tf32(v0);
+            v1 = to_tf32(v1);
+          }
+          e[k] = v0;
+          e[k + 1] = v1;
+          sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
         }
         if constexpr (C::kTF32) {
           uint32_t pw[32];
@@ -463,10 +479,10 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
         }
       }
 #pragma unroll
-      for (int w = kAcc / 2; w > 0; w /= 2)
+      for (int w = kAcc / 4; w > 0; w /= 2)
 #pragma unroll
-        for (int a = 0; a < w; ++a) acc[a] += acc[a + w];
-      const float sum = acc[0];
+        for (int a = 0; a < w; ++a) sum2[a] = fadd2(sum2[a], sum2[a + w]);
+      const float sum = sum2[0].x + sum2[0].y;
       l_run += sum;
       tmem_st_wait();
       tc_fence_before();

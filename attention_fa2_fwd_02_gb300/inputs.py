@@ -88,6 +88,12 @@ WORKLOADS = {
     "large_causal": _w("large_causal", 4, 32, 8192, 8192, 128, torch.bfloat16, True, seed=4),
     "cross_long_nc": _w("cross_long_nc", 2, 16, 4096, 32768, 64, torch.bfloat16, False, seed=5),
     "long_causal": _w("long_causal", 1, 16, 32768, 32768, 128, torch.bfloat16, True, seed=6),
+    # profiling-size cases of the same kernels: inputs still larger than the
+    # 129 MB L2, but small enough for a many-pass ncu capture
+    "prof_nc": _w("prof_nc", 1, 32, 8192, 8192, 128, torch.bfloat16, False, seed=7),
+    "prof_causal": _w("prof_causal", 1, 32, 8192, 8192, 128, torch.bfloat16, True, seed=7),
+    "prof_cross": _w("prof_cross", 1, 16, 4096, 32768, 64, torch.bfloat16, False, seed=8),
+    "prof_tutorial": _w("prof_tutorial", 96, 1, 512, 512, 128, torch.float32, False, seed=2),
 }
 
 

@@ -42,11 +42,12 @@ std::string cuda_msg(const char* what, cudaError_t e) {
 std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
 std::atomic<int> g_debug_flags{0};
 
-constexpr int kMaxDevices = 64;
 struct DevState {
   bool ready = false;
+  int device = 0;
   int sm_count = 0;
   unsigned int* err = nullptr;
+  bool small_attr[2][2] = {{false, false}, {false, false}};  // [bf16/fp32][d16/d32] opt-in set
 };
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
@@ -71,6 +72,7 @@ fa_status_t device_state(DevState** out) {
     if ((e = cudaGetSymbolAddress(&p, g_err_word)) != cudaSuccess)
       return fail(FA_ERR_CUDA, cuda_msg("cudaGetSymbolAddress(error word)", e));
     s.err = static_cast<unsigned int*>(p);
+    s.device = dev;
     s.ready = true;
   }
   *out = &s;
@@ -188,6 +190,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   p.timeout_ns = g_timeout_ns.load();
   p.debug_flags = g_debug_flags.load();
   L.grid = p.n_tiles < ds.sm_count ? p.n_tiles : ds.sm_count;
+  L.device = ds.device;
   L.stream = stream;
   cudaError_t e;
   if (fp32)
@@ -206,10 +209,18 @@ bool row_aligned16(const fa_tensor_t& t, long long E) {
 }
 
 template <typename T, int D>
-cudaError_t launch_small_typed(const SmallParams& P, cudaStream_t stream) {
+cudaError_t launch_small_typed(const SmallParams& P, DevState& ds, cudaStream_t stream) {
   constexpr int smem = small_smem_bytes<T, D>();
-  cudaError_t e = cudaFuncSetAttribute(fa_small_fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  {  // once per device, so that captured launches make no attribute call
+    std::lock_guard<std::mutex> lk(g_mu);
+    bool& ready = ds.small_attr[sizeof(T) == 4 ? 1 : 0][D == 16 ? 0 : 1];
+    if (!ready) {
+      cudaError_t e =
+          cudaFuncSetAttribute(fa_small_fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      ready = true;
+    }
+  }
   const long long blocks = (P.n_items + 3) / 4;
   fa_small_fwd_kernel<T, D><<<(unsigned)blocks, 128, smem, stream>>>(P);
   return cudaGetLastError();
@@ -217,7 +228,7 @@ cudaError_t launch_small_typed(const SmallParams& P, cudaStream_t stream) {
 
 // One launch for up to kSmallMaxGroup problems of the same dtype and head dim.
 fa_status_t launch_small(fa_dtype_t dtype, int d, const std::vector<const fa_problem_t*>& probs,
-                         cudaStream_t stream) {
+                         DevState& ds, cudaStream_t stream) {
   const long long E = dtype == FA_FP32 ? 4 : 2;
   SmallParams P{};
   P.n_problems = (int)probs.size();
@@ -253,10 +264,10 @@ fa_status_t launch_small(fa_dtype_t dtype, int d, const std::vector<const fa_pro
   if ((items + 3) / 4 >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query blocks in one launch");
   cudaError_t e;
   if (dtype == FA_FP32)
-    e = d == 16 ? launch_small_typed<float, 16>(P, stream) : launch_small_typed<float, 32>(P, stream);
+    e = d == 16 ? launch_small_typed<float, 16>(P, ds, stream) : launch_small_typed<float, 32>(P, ds, stream);
   else
-    e = d == 16 ? launch_small_typed<__nv_bfloat16, 16>(P, stream)
-                : launch_small_typed<__nv_bfloat16, 32>(P, stream);
+    e = d == 16 ? launch_small_typed<__nv_bfloat16, 16>(P, ds, stream)
+                : launch_small_typed<__nv_bfloat16, 32>(P, ds, stream);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("small-head kernel launch", e));
   return FA_OK;
 }
@@ -279,11 +290,11 @@ fa_status_t run_problems(fa_dtype_t dtype, int n, const fa_problem_t* problems, 
       if (paths[i] != Path::kSmall || problems[i].d != d) continue;
       group.push_back(&problems[i]);
       if ((int)group.size() == kSmallMaxGroup) {
-        if ((st = launch_small(dtype, d, group, stream)) != FA_OK) return st;
+        if ((st = launch_small(dtype, d, group, *ds, stream)) != FA_OK) return st;
         group.clear();
       }
     }
-    if (!group.empty() && (st = launch_small(dtype, d, group, stream)) != FA_OK) return st;
+    if (!group.empty() && (st = launch_small(dtype, d, group, *ds, stream)) != FA_OK) return st;
   }
   for (int i = 0; i < n; ++i)
     if (paths[i] == Path::kTensorCore && (st = launch_tensor_core(dtype, problems[i], *ds, stream)) != FA_OK)

@@ -10,10 +10,13 @@
 namespace fa {
 
 // Everything a tensor-core launch needs, prepared and validated on the host.
+constexpr int kMaxDevices = 64;
+
 struct TcLaunch {
   CUtensorMap tmQ, tmK, tmV;
   TcParams p;
   int grid;
+  int device;  // current device ordinal (per-device one-time setup)
   cudaStream_t stream;
 };
 

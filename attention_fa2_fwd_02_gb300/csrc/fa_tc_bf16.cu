@@ -2,6 +2,8 @@
 // forward kernel: d = 128 with a 4-deep ring of 128-key tiles, d = 64 with 6.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "fa_launch.h"
 
 namespace fa {
@@ -11,11 +13,18 @@ using CfgBf16D64 = TcCfg<__nv_bfloat16, 64, 128, 6>;
 static_assert(CfgBf16D128::BN == tc_key_tile(false, 128) && CfgBf16D64::BN == tc_key_tile(false, 64), "geometry");
 static_assert(CfgBf16D128::kPanelElems == tc_box_inner(false), "geometry");
 
+// The shared-memory opt-in is set once per device (so that a launch captured
+// into a CUDA graph makes no attribute call).
 template <class C>
 static cudaError_t launch(const TcLaunch& L) {
-  cudaError_t e = cudaFuncSetAttribute(fa_tc_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::kSmemBytes));
-  if (e != cudaSuccess) return e;
+  static std::atomic<bool> ready[kMaxDevices];
+  if (L.device < 0 || L.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!ready[L.device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(fa_tc_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    ready[L.device].store(true, std::memory_order_release);
+  }
   fa_tc_fwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
   return cudaGetLastError();
 }

@@ -89,6 +89,16 @@ def lib() -> ctypes.CDLL:
             L.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_int]
             L.fa_version.restype = ctypes.c_int
             L.fa_version.argtypes = []
+            L.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
+            L.fa_fwd_splitkv_workspace_bytes.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
+            L.fa_fwd_splitkv_choose.restype = ctypes.c_int
+            L.fa_fwd_splitkv_choose.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 5 + [ctypes.c_int]
+            L.fa_fwd_splitkv.restype = ctypes.c_int
+            L.fa_fwd_splitkv.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_int64, P(FaTensor), P(FaTensor),
+                                         P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
+                                         ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -171,20 +181,43 @@ def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
 
 def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None = None,
         is_causal: bool = False, out: torch.Tensor | None = None,
-        lse: torch.Tensor | None = None, with_lse: bool = True, stream=None):
+        lse: torch.Tensor | None = None, with_lse: bool = True, stream=None,
+        split_kv: int | None = None, workspace: torch.Tensor | None = None):
     """O, LSE = softmax(scale * Q K^T) V and its log-sum-exp, on the GPU.
 
     Asynchronous on the current (or given) stream.  Returns (O, LSE); LSE is
     None when ``with_lse`` is False and no ``lse`` buffer is passed.
+    ``split_kv``: key-range splits (None = the library's choice for this
+    device; 1 = never split).  A split run needs scratch memory: ``workspace``
+    (a CUDA uint8 tensor of at least the required bytes) or, if None, one
+    allocated here from PyTorch's allocator.
     """
     pb, out, lse = _problem(Q, K, V, scale, is_causal, out, lse, with_lse)
     L = lib()
+    code = _dtype_code(Q)
     with torch.cuda.device(Q.device):
         lse_stride = (ctypes.c_int64 * 3)(*pb.lse_stride)
-        st = L.fa_fwd(_dtype_code(Q), pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
-                      ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
-                      pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
-                      _stream_ptr(Q.device, stream))
+        n_split = 1
+        if pb.d in (64, 128):
+            n_split = (L.fa_fwd_splitkv_choose(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.is_causal)
+                       if split_kv is None else int(split_kv))
+        if n_split == 1:
+            st = L.fa_fwd(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
+                          ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                          pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
+                          _stream_ptr(Q.device, stream))
+        else:
+            need = L.fa_fwd_splitkv_workspace_bytes(pb.B, pb.H, pb.N_q, pb.d, n_split)
+            if workspace is None:
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+            if workspace.device != Q.device or workspace.numel() * workspace.element_size() < need:
+                raise ValueError(f"workspace must be a CUDA buffer of >= {need} bytes on Q's device")
+            st = L.fa_fwd_splitkv(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
+                                  ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                                  pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
+                                  n_split, ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream_ptr(Q.device, stream))
     _raise_on(st)
     return out, lse
 

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "fa.h"
+#include "fa_combine.cuh"
 #include "fa_launch.h"
 #include "fa_small.cuh"
 
@@ -156,7 +157,29 @@ fa_status_t make_map(CUtensorMap* map, const fa_tensor_t& t, bool fp32, long lon
   return FA_OK;
 }
 
-fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const DevState& ds, cudaStream_t stream) {
+// Split-KV workspace (caller-owned): fp32 partial O [n_split][B*H*N_q][d],
+// then fp32 partial LSE [n_split][B*H*N_q], each part 256-byte aligned.
+struct SplitWs {
+  float* o = nullptr;
+  float* lse = nullptr;
+};
+size_t split_ws_bytes(long long B, long long H, long long N_q, long long d, int n_split) {
+  const size_t rows = static_cast<size_t>(B) * H * N_q;
+  const size_t o = (static_cast<size_t>(n_split) * rows * d * 4 + 255) & ~size_t(255);
+  const size_t l = (static_cast<size_t>(n_split) * rows * 4 + 255) & ~size_t(255);
+  return o + l;
+}
+SplitWs split_ws_layout(void* ws, long long B, long long H, long long N_q, long long d, int n_split) {
+  const size_t rows = static_cast<size_t>(B) * H * N_q;
+  const size_t o = (static_cast<size_t>(n_split) * rows * d * 4 + 255) & ~size_t(255);
+  SplitWs w;
+  w.o = static_cast<float*>(ws);
+  w.lse = reinterpret_cast<float*>(static_cast<char*>(ws) + o);
+  return w;
+}
+
+fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const DevState& ds, cudaStream_t stream,
+                               int n_split = 1, SplitWs ws = SplitWs{}) {
   const bool fp32 = dtype == FA_FP32;
   const int d = static_cast<int>(pb.d);
   const int bn = tc_key_tile(fp32, d);
@@ -174,6 +197,10 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   p.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
   p.n_qblk = (int)((pb.N_q + 255) / 256);
   p.n_tiles = (int)(pb.B * pb.H * p.n_qblk);
+  p.n_split = n_split;
+  p.n_units = p.n_tiles * n_split;
+  p.ws_o = ws.o;
+  p.ws_lse = ws.lse;
   // Heads per schedule group: keep the K/V of a group within ~48 MB of L2.
   const long long kv_bytes = 2ll * pb.N_k * pb.d * (fp32 ? 4 : 2);
   long long g = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
@@ -189,16 +216,83 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   p.err = ds.err;
   p.timeout_ns = g_timeout_ns.load();
   p.debug_flags = g_debug_flags.load();
-  L.grid = p.n_tiles < ds.sm_count ? p.n_tiles : ds.sm_count;
+  L.grid = p.n_units < ds.sm_count ? p.n_units : ds.sm_count;
   L.device = ds.device;
   L.stream = stream;
   cudaError_t e;
-  if (fp32)
+  if (n_split > 1) {
+    if (fp32)
+      e = d == 128 ? launch_tc_fp32_d128_split(L) : launch_tc_fp32_d64_split(L);
+    else
+      e = d == 128 ? launch_tc_bf16_d128_split(L) : launch_tc_bf16_d64_split(L);
+  } else if (fp32) {
     e = d == 128 ? launch_tc_fp32_d128(L) : launch_tc_fp32_d64(L);
-  else
+  } else {
     e = d == 128 ? launch_tc_bf16_d128(L) : launch_tc_bf16_d64(L);
+  }
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("tensor-core kernel launch", e));
+  if (n_split > 1) {
+    CombineParams c{};
+    c.B = (int)pb.B;
+    c.H = (int)pb.H;
+    c.N_q = (int)pb.N_q;
+    c.N_k = (int)pb.N_k;
+    c.causal = pb.is_causal;
+    c.n_split = n_split;
+    c.bn = bn;
+    c.rows = pb.B * pb.H * pb.N_q;
+    c.ws_o = ws.o;
+    c.ws_lse = ws.lse;
+    c.O = pb.O.ptr;
+    for (int i = 0; i < 3; ++i) {
+      c.o_stride[i] = pb.O.stride[i];
+      c.lse_stride[i] = pb.LSE ? pb.lse_stride[i] : 0;
+    }
+    c.LSE = pb.LSE;
+    const unsigned blocks = (unsigned)((c.rows + 7) / 8);
+    if (fp32)
+      d == 128 ? fa_combine_kernel<float, 128><<<blocks, 256, 0, stream>>>(c)
+               : fa_combine_kernel<float, 64><<<blocks, 256, 0, stream>>>(c);
+    else
+      d == 128 ? fa_combine_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, stream>>>(c)
+               : fa_combine_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, stream>>>(c);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("combine kernel launch", e));
+  }
   return FA_OK;
+}
+
+// Split count for a problem (1 = do not split).  Work units run in waves of
+// one per SM; a tile of n key tiles costs about n + 2 key-tile times (the 2
+// covers its prologue and epilogue), so s splits take
+//     ceil(tiles * s / SMs) * (n / s + 2)
+// key-tile times.  A split is taken only if that is at least 10 % below the
+// unsplit time and every split still covers >= 1024 keys (the partial-result
+// round trip and the merge launch are not worth it for less).  Causal
+// problems are balanced by their longest-first order, and the fp32 (tf32)
+// path is not split automatically: on the measured fp32 shapes splitting was
+// slower.  Callers can still ask for a split explicitly.
+int choose_split(bool fp32, long long B, long long H, long long N_q, long long N_k, long long d, int causal,
+                 int sm_count) {
+  if (fp32 || causal || (d != 64 && d != 128) || sm_count <= 0) return 1;
+  const long long bn = tc_key_tile(fp32, (int)d);
+  const long long tiles = B * H * ((N_q + 255) / 256);
+  const long long n_kv = (N_k + bn - 1) / bn;
+  auto cost = [&](long long s) {
+    const long long waves = (tiles * s + sm_count - 1) / sm_count;
+    return static_cast<double>(waves) * (static_cast<double>(n_kv) / s + 2.0);
+  };
+  const double base = cost(1);
+  int best = 1;
+  double best_cost = base;
+  for (int s = 2; s <= 4; ++s) {
+    if (N_k / s < 1024) break;
+    const double c = cost(s);
+    if (c < best_cost) {
+      best_cost = c;
+      best = s;
+    }
+  }
+  return best_cost <= 0.9 * base ? best : 1;
 }
 
 bool row_aligned16(const fa_tensor_t& t, long long E) {
@@ -330,6 +424,62 @@ fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
 
 fa_status_t fa_fwd_grouped(fa_dtype_t dtype, int n, const fa_problem_t* problems, void* stream) {
   return run_problems(dtype, n, problems, stream);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d, int n_split) {
+  if (B <= 0 || H <= 0 || N_q <= 0 || d <= 0 || n_split <= 1 || n_split > kMaxSplit) return 0;
+  return split_ws_bytes(B, H, N_q, d, n_split);
+}
+
+int fa_fwd_splitkv_choose(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                          int is_causal) {
+  if (B <= 0 || H <= 0 || N_q <= 0 || N_k <= 0) return 1;
+  DevState* ds = nullptr;
+  if (device_state(&ds) != FA_OK) return 1;
+  return choose_split(dtype == FA_FP32, B, H, N_q, N_k, d, is_causal, ds->sm_count);
+}
+
+fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                           const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                           int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                           int n_split, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_split < 1 || n_split > kMaxSplit)
+    return fail(FA_ERR_INVALID_ARG, "n_split must be in [1, " + std::to_string(kMaxSplit) + "]");
+  if (n_split == 1)
+    return fa_fwd(dtype, B, H, N_q, N_k, d, Q, K, V, scale, is_causal, O, LSE, lse_stride, stream);
+  if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
+  if (LSE && !lse_stride) return fail(FA_ERR_INVALID_ARG, "lse_stride must not be NULL when LSE is given");
+  fa_problem_t pb{};
+  pb.B = B;
+  pb.H = H;
+  pb.N_q = N_q;
+  pb.N_k = N_k;
+  pb.d = d;
+  pb.Q = *Q;
+  pb.K = *K;
+  pb.V = *V;
+  pb.O = *O;
+  pb.LSE = LSE;
+  for (int i = 0; i < 3; ++i) pb.lse_stride[i] = LSE ? lse_stride[i] : 0;
+  pb.scale = scale;
+  pb.is_causal = is_causal;
+  Path path;
+  fa_status_t st = validate(dtype, pb, 0, &path);
+  if (st != FA_OK) return st;
+  if (path != Path::kTensorCore) return fail(FA_ERR_UNSUPPORTED, "split-KV needs the tensor-core path (d = 64, 128)");
+  if (B * H * ((N_q + 255) / 256) * n_split >= (1ll << 31))
+    return fail(FA_ERR_UNSUPPORTED, "too many split-KV work units");
+  if (!workspace) return fail(FA_ERR_INVALID_ARG, "split-KV needs a workspace");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(FA_ERR_INVALID_ARG, "the split-KV workspace must be 256-byte aligned");
+  const size_t need = split_ws_bytes(B, H, N_q, d, n_split);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "split-KV workspace too small: " + std::to_string(workspace_bytes) + " < " +
+                                        std::to_string(need) + " bytes");
+  DevState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  return launch_tensor_core(dtype, pb, *ds, static_cast<cudaStream_t>(stream), n_split,
+                            split_ws_layout(workspace, B, H, N_q, d, n_split));
 }
 
 fa_status_t fa_check(void* stream_ptr) {

@@ -26,9 +26,13 @@ cudaError_t launch_tc_bf16_d128(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d128(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d64(const TcLaunch& L);
+// split-KV variants (L.p.n_split > 1, L.p.ws_o / ws_lse set)
+cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L);
+cudaError_t launch_tc_bf16_d64_split(const TcLaunch& L);
+cudaError_t launch_tc_fp32_d128_split(const TcLaunch& L);
+cudaError_t launch_tc_fp32_d64_split(const TcLaunch& L);
 
-// Tile geometry shared with the instantiations in fa_tc_bf16.cu and
-// fa_tc_fp32.cu: key-tile width and TMA box width (one 128-byte swizzle row).
+// Tile geometry shared with the instantiations in fa_tc_*.cu: key-tile width and TMA box width (one 128-byte swizzle row).
 constexpr int tc_key_tile(bool fp32, int d) { return fp32 ? (d == 128 ? 32 : 64) : 128; }
 constexpr int tc_box_inner(bool fp32) { return fp32 ? 32 : 64; }
 

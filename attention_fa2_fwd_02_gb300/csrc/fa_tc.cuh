@@ -40,6 +40,10 @@ struct TcParams {
   float scale_log2;       // scale * log2(e)
   int n_qblk;             // ceil(N_q / 256)
   int n_tiles;            // B * H * n_qblk
+  int n_split;            // key-range splits per tile (1 = none)
+  int n_units;            // n_tiles * n_split work units
+  float* ws_o;            // split-KV partial outputs, fp32 [n_split][B*H*N_q][D]
+  float* ws_lse;          // split-KV partial LSE (natural log), [n_split][B*H*N_q]
   int head_group;         // heads per schedule group (K/V L2 locality)
   void* O;
   long long o_stride[3];  // elements: b, h, n
@@ -50,9 +54,13 @@ struct TcParams {
   int debug_flags;
 };
 
-template <typename T, int D_, int BN_, int NSLOT_>
+template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false>
 struct TcCfg {
   using Elem = T;
+  // split-KV instantiation: work units are key-range parts of a tile and write
+  // partial results to the workspace (a separate kernel, so that the plain
+  // path compiles without any of it)
+  static constexpr bool kSplit = SPLIT_;
   static constexpr bool kTF32 = sizeof(T) == 4;
   static constexpr int E = sizeof(T);
   static constexpr int D = D_;
@@ -124,14 +132,23 @@ struct Bars {
 };
 
 struct TileInfo {
-  int b, h, q0, n_kv;
+  int b, h, q0;
+  int split;   // key-range split of this work unit
+  int j0;      // first key tile of the unit
+  int n_kv;    // key tiles of the unit (0: nothing to do)
 };
 
 // Tile order: heads are taken in groups of `head_group`; inside a group the
 // query blocks of all its heads are interleaved, last (longest under the
 // causal mask) first, so that concurrently running CTAs share K/V in L2 and
-// the causal work is handed out longest-first.
-__device__ __forceinline__ TileInfo tile_info(const TcParams& p, int t, int BN) {
+// the causal work is handed out longest-first.  Work unit u is split
+// u % n_split of tile u / n_split: the tile's key tiles are cut into
+// min(n_split, #tiles) balanced ranges; the remaining splits are empty.
+template <class C>
+__device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
+  constexpr int BN = C::BN;
+  const int t = C::kSplit ? u / p.n_split : u;
+  const int split = C::kSplit ? u - t * p.n_split : 0;
   const int BH = p.B * p.H;
   const int per_group = p.head_group * p.n_qblk;
   const int g = t / per_group;
@@ -144,9 +161,23 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int t, int BN) 
   ti.b = bh / p.H;
   ti.h = bh - ti.b * p.H;
   ti.q0 = qb * 256;
+  ti.split = split;
   int kv_end = p.N_k;
   if (p.causal) kv_end = min(kv_end, min(ti.q0 + 256, p.N_q));
-  ti.n_kv = (kv_end + BN - 1) / BN;
+  const int n_tot = (kv_end + BN - 1) / BN;
+  if constexpr (!C::kSplit) {
+    ti.j0 = 0;
+    ti.n_kv = n_tot;
+    return ti;
+  }
+  const int s_eff = min(p.n_split, n_tot);
+  if (split >= s_eff) {
+    ti.j0 = 0;
+    ti.n_kv = 0;
+  } else {
+    ti.j0 = split * n_tot / s_eff;
+    ti.n_kv = (split + 1) * n_tot / s_eff - ti.j0;
+  }
   return ti;
 }
 
@@ -193,12 +224,15 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(map, &bars.kv_full[slot], dst + pn * C::kKVPanelBytes, pn * C::kPanelElems,
-                  j * C::BN, ti.h, ti.b, pol_kv);
+                  (ti.j0 + j) * C::BN, ti.h, ti.b, pol_kv);
     return true;
   };
 
-  for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++tile_k) {
-    const TileInfo ti = tile_info(p, t, C::BN);
+  uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
+  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, tile_k += counted) {
+    const TileInfo ti = tile_info<C>(p, u);
+    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    if (!counted) continue;
     const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
     ok = load_q(0, ti) && load_kv(tmK, 0, ti, false) && load_q(1, ti) &&
          load_kv(tmV, 0, ti, false);
@@ -284,8 +318,11 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
   };
   auto slot_addr = [&](uint32_t i) -> uint32_t { return kv_base + (i % C::NSLOT) * C::kKVBytes; };
 
-  for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++tile_k) {
-    const TileInfo ti = tile_info(p, t, C::BN);
+  uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
+  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, tile_k += counted) {
+    const TileInfo ti = tile_info<C>(p, u);
+    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    if (!counted) continue;
     const uint32_t par_k = tile_k & 1u;
     const int n = ti.n_kv;
     // S_s(0) = Q_s K_0^T for both stages
@@ -362,8 +399,11 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
   const float sc = p.scale_log2;
   uint32_t s_par = 0, tile_k = 0;
 
-  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tile_k) {
-    const TileInfo ti = tile_info(p, t, C::BN);
+  uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
+    const TileInfo ti = tile_info<C>(p, u);
+    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    if (!counted) continue;
     const int q = ti.q0 + stage * C::BM + row;
     const int vis_end = p.causal ? min(p.N_k, q + 1) : p.N_k;  // keys < vis_end are visible
     float m_run = -INFINITY, l_run = 0.f;
@@ -378,7 +418,7 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
 #pragma unroll
       for (int c = 32; c < C::BN; c += 32) reg_fence32(s + c);
 
-      const int lim = vis_end - j * C::BN;  // columns c < lim are visible
+      const int lim = vis_end - (ti.j0 + j) * C::BN;  // columns c < lim are visible
       const bool need_mask = __any_sync(0xffffffffu, lim < C::BN);
       // Row max: three-input max over pairs, in kAcc independent chains (one
       // chain of BN dependent operations would put its whole latency on the
@@ -490,7 +530,10 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
     }
     // hand the row statistics to the epilogue: 1/l and LSE (natural log)
     if (!warp_wait(&bars.st_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x32 + stage)) return;
-    stats[stage * C::BM + row] = make_float2(1.f / l_run, (m_run + __log2f(l_run)) * kLn2);
+    // (l_run = 0 only in a split-KV unit none of whose keys this row sees:
+    // then O = 0 and LSE = -inf, which the combine step weighs by zero)
+    const float inv_l = C::kSplit ? (l_run > 0.f ? 1.f / l_run : 0.f) : 1.f / l_run;
+    stats[stage * C::BM + row] = make_float2(inv_l, (m_run + __log2f(l_run)) * kLn2);
     mbar_arrive(&bars.st_full[stage]);
   }
 }
@@ -572,8 +615,11 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   uint32_t tile_k = 0, it = 0, vcount = 0;
-  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tile_k) {
-    const TileInfo ti = tile_info(p, t, C::BN);
+  uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
+    const TileInfo ti = tile_info<C>(p, u);
+    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    if (!counted) continue;
     if constexpr (C::kVt) {
       // same order as the load warp: Q_0, K_0, Q_1, V_0, then K_j, V_j
       auto do_q = [&](int s) -> bool {
@@ -604,13 +650,23 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
       const bool valid = q < p.N_q;
       T* orow = reinterpret_cast<T*>(p.O) + ti.b * p.o_stride[0] + ti.h * p.o_stride[1] +
                 static_cast<long long>(q) * p.o_stride[2];
+      // split-KV: this unit's normalised partial O (fp32) and LSE go to the
+      // workspace; the combine kernel merges the splits into O and LSE
+      constexpr bool partial = C::kSplit;
+      const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
       const uint32_t tO = tmem + lane_base + C::col_o(s);
 #pragma unroll 1
       for (int c = 0; c < C::D; c += 32) {
         uint32_t o[32];
         tmem_ld32(tO + c, o);
         tmem_ld_wait32(o);
-        if (valid) {
+        if (partial && valid) {
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * C::D + c);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
+                                 __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
+        } else if (valid) {
           if constexpr (C::kTF32) {
             float4* dst = reinterpret_cast<float4*>(orow + c);
 #pragma unroll
@@ -633,7 +689,9 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
       }
       tc_fence_before();
       mbar_arrive(&bars.o_empty[s]);
-      if (valid && p.LSE)
+      if (partial && valid)
+        p.ws_lse[wrow] = st.y;
+      else if (valid && p.LSE)
         p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
     }
   }

@@ -1,0 +1,35 @@
+// fa_tc_inst.cuh -- launch wrapper shared by the translation units that
+// instantiate the tensor-core kernel (one variant family per unit, so that
+// they compile in parallel).
+#pragma once
+
+#include <atomic>
+
+#include "fa_launch.h"
+
+namespace fa {
+
+// The shared-memory opt-in is set once per device (so that a launch captured
+// into a CUDA graph makes no attribute call).
+template <class C>
+static cudaError_t launch_tc(const TcLaunch& L) {
+  static std::atomic<bool> ready[kMaxDevices];
+  if (L.device < 0 || L.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!ready[L.device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(fa_tc_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    ready[L.device].store(true, std::memory_order_release);
+  }
+  fa_tc_fwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaGetLastError();
+}
+
+// Geometry of the instantiated configurations (the host side sizes its TMA
+// boxes from tc_key_tile / tc_box_inner).
+template <class C, bool FP32>
+constexpr bool tc_geometry_ok() {
+  return C::BN == tc_key_tile(FP32, C::D) && C::kPanelElems == tc_box_inner(FP32);
+}
+
+}  // namespace fa

@@ -331,15 +331,24 @@ def main():
     if in_bytes <= l2_bytes:
         flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
 
+    n_split = 1  # key-range splits the library picks for this problem
     if axial:
         def step():
             return fa.axial(Qd, Kd, Vd, scale=w.scale, with_lse=True)
     else:
         Od = torch.empty_like(Qd)
         Ld = torch.empty(Qd.shape[:-1], dtype=torch.float32, device=dev)
+        code = fa.FA_BF16 if w.dtype == torch.bfloat16 else fa.FA_FP32
+        if w.d in (64, 128):
+            n_split = fa.lib().fa_fwd_splitkv_choose(code, w.B, w.H, w.N_q, w.N_k, w.d, int(w.causal))
+        ws = None
+        if n_split > 1:  # the split path's scratch, allocated once outside the timed region
+            ws = torch.empty(fa.lib().fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.N_q, w.d, n_split),
+                             dtype=torch.uint8, device=dev)
 
         def step():
-            return fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, out=Od, lse=Ld)
+            return fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, out=Od, lse=Ld,
+                          split_kv=n_split, workspace=ws)
 
     for _ in range(warm):
         if flush is not None:
@@ -417,6 +426,9 @@ def main():
             note = f"bf16_tflops burst x nominal tf32/bf16 ratio 1.1/2.25 (of {peak_src})"
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": note}
+        if n_split > 1:  # the events bracket both launches of a split step
+            roof["timed"] = f"split-KV attention kernel (n_split={n_split}) + merge kernel"
+
 
     # ------------------------------------------------------ end to end
     e2e = None
@@ -479,6 +491,7 @@ def main():
                      if flush is None else "L2 flushed (%.0f MB write) between steps" % (flush.numel() * 4 / 2**20))
         cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
         cfg["cuda_graph"] = use_graph
+        cfg["split_kv"] = n_split
         line = {
             "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": step_ms,
@@ -486,7 +499,8 @@ def main():
             "dtype": "bf16" if (not axial and w.dtype == torch.bfloat16) else ("f32" if axial else "tf32"),
             "data": "synthetic (seeded i.i.d. N(0,1))", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": steps, "kernel_ms": kernel_ms,
+            # one kernel per step, plus the merge kernel when the keys are split
+            "gpu_launches": steps * (2 if n_split > 1 else 1), "kernel_ms": kernel_ms,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -34,6 +34,7 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -110,6 +111,45 @@ typedef struct {
  * Validation of every problem happens before any launch; n = 0 is a no-op.
  */
 fa_status_t fa_fwd_grouped(fa_dtype_t dtype, int n, const fa_problem_t* problems, void* stream);
+
+/*
+ * Split-KV forward: the same operation as fa_fwd, with the key range of every
+ * 256-row query tile cut into n_split balanced parts that run as separate
+ * work units.  It serves problems with few query tiles for the number of SMs
+ * (long keys, short queries): more units fill the last wave of the persistent
+ * grid.  Each unit writes its normalised partial output O_s (fp32) and its
+ * log-sum-exp L_s into `workspace`; a second kernel merges them with
+ * L = log sum_s e^{L_s} and O = sum_s e^{L_s - L} O_s (the rescaling identity
+ * of the online softmax in "Extend Thunder with CUDA-Python",
+ * flash_attention_reference).
+ *
+ *   n_split          1..8; 1 is exactly fa_fwd (workspace unused).  Non-causal
+ *                    and causal problems alike; a tile with fewer key tiles
+ *                    than n_split uses fewer parts.
+ *   workspace        device memory of at least
+ *                    fa_fwd_splitkv_workspace_bytes(B, H, N_q, d, n_split)
+ *                    bytes, 256-byte aligned, owned by the caller; its
+ *                    contents are scratch.  Concurrent calls need separate
+ *                    workspaces.
+ *   other arguments  as fa_fwd; only the tensor-core path (d = 64, 128)
+ *                    splits (FA_ERR_UNSUPPORTED otherwise).
+ */
+size_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d, int n_split);
+
+/* Split count for this problem on the current device (1 = do not split).
+ * It models the run as waves of one work unit per SM and takes a split only
+ * when that model is at least 10 % faster and every part keeps >= 1024 keys.
+ * Causal problems (their longest-first schedule already balances them) and
+ * FA_FP32 problems (splitting was slower on the shapes measured) return 1;
+ * fa_fwd_splitkv still accepts an explicit n_split for them.  Errors (no
+ * device, bad sizes) also return 1. */
+int fa_fwd_splitkv_choose(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                          int is_causal);
+
+fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                           const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                           int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                           int n_split, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_check -- synchronise `stream`, then read and clear the device error word

@@ -118,3 +118,33 @@ def test_python_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 8, 64)
     with pytest.raises(ValueError):
         fa.fwd(x, x, x)
+
+
+def _splitkv(L, n_split=2, ws=0x100000, ws_bytes=1 << 30, d=128, Nq=256):
+    s = (Nq * d, Nq * d, d, 1)
+    Q, K, V, O = (_t(a, s) for a in (0x10000, 0x20000, 0x30000, 0x40000))
+    ls = (ctypes.c_int64 * 3)(Nq, Nq, 1)
+    return L.fa_fwd_splitkv(fa.FA_BF16, 1, 1, Nq, Nq, d, ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V),
+                            0.1, 0, ctypes.byref(O), None, ls, n_split, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_split=0), fa.FA_ERR_INVALID_ARG),
+    (dict(n_split=9), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),            # no workspace
+    (dict(ws=0x100010), fa.FA_ERR_INVALID_ARG),     # not 256-byte aligned
+    (dict(ws_bytes=1024), fa.FA_ERR_INVALID_ARG),   # too small
+    (dict(d=16), fa.FA_ERR_UNSUPPORTED),            # small-head path does not split
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+])
+def test_splitkv_host_validation(L, kw, status):
+    assert _splitkv(L, **kw) == status
+    assert L.fa_last_error() != b""
+
+
+def test_splitkv_workspace_size(L):
+    # n_split x rows x (d fp32 + 1 fp32 LSE), each part rounded up to 256 bytes
+    rows = 2 * 3 * 100
+    want = ((2 * rows * 64 * 4 + 255) // 256) * 256 + ((2 * rows * 4 + 255) // 256) * 256
+    assert L.fa_fwd_splitkv_workspace_bytes(2, 3, 100, 64, 2) == want
+    assert L.fa_fwd_splitkv_workspace_bytes(2, 3, 100, 64, 1) == 0

@@ -37,12 +37,14 @@ def _poisoned(shape, dtype):
     return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
 
 
-def run_gpu(Q, K, V, scale, causal):
-    """Q, K, V on the host -> (O, LSE) from the GPU, as host tensors."""
+def run_gpu(Q, K, V, scale, causal, split_kv=None):
+    """Q, K, V on the host -> (O, LSE) from the GPU, as host tensors.
+    split_kv=None lets the library choose (long key ranges over few query
+    tiles are then split)."""
     Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
     O = _poisoned(Q.shape, Q.dtype)
     L = _poisoned(Q.shape[:-1], torch.float32)
-    fa.fwd(Qd, Kd, Vd, scale=scale, is_causal=causal, out=O, lse=L)
+    fa.fwd(Qd, Kd, Vd, scale=scale, is_causal=causal, out=O, lse=L, split_kv=split_kv)
     fa.check()
     return O.float().cpu().numpy(), L.cpu().numpy()
 
@@ -69,9 +71,61 @@ def test_tensor_core_ragged(oracle_mod, dtype, d, causal, nq, nk):
     seed = 1000 + nq * 7 + nk * 13 + d + (1 if causal else 0)
     Q, K, V = qkv((2, 3, nq, d), (2, 3, nk, d), seed, dtype)
     scale = 1.0 / math.sqrt(d)
-    O, L = run_gpu(Q, K, V, scale, causal)
+    O, L = run_gpu(Q, K, V, scale, causal, split_kv=1)
     O_ref, L_ref = oracle_mod.attention(Q, K, V, scale, causal)
     assert_close(O, L, O_ref, L_ref, dtype, f"{dtype} d={d} {nq}x{nk} causal={causal}")
+
+
+# ------------------------------------------------------------------ split-KV
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
+@pytest.mark.parametrize("nq,nk,split", [(300, 1000, 1), (300, 1000, 2), (257, 1000, 3), (100, 777, 5),
+                                         (513, 513, 2), (64, 129, 2), (1, 300, 3)])
+def test_split_kv_ragged(oracle_mod, dtype, d, causal, nq, nk, split):
+    """Forced split counts (1 = the plain path), ragged lengths, causal rows
+    whose keys fall outside some splits."""
+    Q, K, V = qkv((2, 2, nq, d), (2, 2, nk, d), 3000 + nq + nk + split + d, dtype)
+    scale = 1.0 / math.sqrt(d)
+    O, L = run_gpu(Q, K, V, scale, causal, split_kv=split)
+    O_ref, L_ref = oracle_mod.attention(Q, K, V, scale, causal)
+    assert_close(O, L, O_ref, L_ref, dtype, f"split={split} {dtype} d={d} {nq}x{nk} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("nq,nk", [(300, 4096), (256, 5000)])
+def test_auto_split_long_keys(oracle_mod, d, nq, nk):
+    """A few query tiles over a long key range: the library's own choice
+    splits the keys (bf16, non-causal), and the merged result matches."""
+    B, H = 1, 2
+    n = fa.lib().fa_fwd_splitkv_choose(fa.FA_BF16, B, H, nq, nk, d, 0)
+    assert n > 1
+    assert fa.lib().fa_fwd_splitkv_choose(fa.FA_BF16, B, H, nq, nk, d, 1) == 1   # causal: never
+    assert fa.lib().fa_fwd_splitkv_choose(fa.FA_FP32, B, H, nq, nk, d, 0) == 1   # tf32: never
+    Q, K, V = qkv((B, H, nq, d), (B, H, nk, d), 4000 + nq + nk + d, torch.bfloat16)
+    O, L = run_gpu(Q, K, V, 1.0 / math.sqrt(d), False, split_kv=None)
+    O_ref, L_ref = oracle_mod.attention(Q, K, V, 1.0 / math.sqrt(d), False)
+    assert_close(O, L, O_ref, L_ref, torch.bfloat16, f"auto split={n} d={d} {nq}x{nk}")
+
+
+def test_split_kv_strided_and_workspace_reuse(oracle_mod):
+    """Head-major strided storage through the split path, two calls sharing
+    one caller-provided workspace."""
+    B, H, N, Nk, d = 2, 4, 200, 900, 128
+    Qs, Ks, Vs = normal((B, N, H, d), 61, torch.bfloat16), normal((B, Nk, H, d), 62, torch.bfloat16), \
+        normal((B, Nk, H, d), 63, torch.bfloat16)
+    need = fa.lib().fa_fwd_splitkv_workspace_bytes(B, H, N, d, 3)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for causal in (False, True):
+        Od = torch.full((B, N, H, d), float("nan"), dtype=torch.bfloat16, device="cuda").transpose(1, 2)
+        Ld = _poisoned((B, H, N), torch.float32)
+        fa.fwd(Qs.cuda().transpose(1, 2), Ks.cuda().transpose(1, 2), Vs.cuda().transpose(1, 2),
+               scale=0.09, is_causal=causal, out=Od, lse=Ld, split_kv=3, workspace=ws)
+        fa.check()
+        O_ref, L_ref = oracle_mod.attention(Qs.transpose(1, 2), Ks.transpose(1, 2), Vs.transpose(1, 2),
+                                            0.09, causal)
+        assert_close(Od.float().cpu().numpy(), Ld.cpu().numpy(), O_ref, L_ref, torch.bfloat16,
+                     f"split strided causal={causal}")
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])

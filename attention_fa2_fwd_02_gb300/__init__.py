@@ -22,7 +22,7 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["fwd", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
+__all__ = ["fwd", "fwd_noalloc", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
            "LIB_PATH", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT"]
 
@@ -30,6 +30,8 @@ LIB_PATH = Path(__file__).resolve().parent / "_build" / "libfa.so"
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 FA_BF16, FA_FP32 = 0, 1
+# size of the fixed per-device scratch of fwd_noalloc (FA_SPLITKV_NOALLOC_SCRATCH_BYTES)
+SPLITKV_NOALLOC_SCRATCH_BYTES = 128 << 20
 
 
 class FaTensor(ctypes.Structure):
@@ -99,6 +101,12 @@ def lib() -> ctypes.CDLL:
                                          P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
                                          ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
+            L.fa_fwd_splitkv_noalloc.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int64, P(FaTensor), P(FaTensor),
+                                                 P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
+                                                 ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int,
+                                                 ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -218,6 +226,38 @@ def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None =
                                   n_split, ctypes.c_void_p(workspace.data_ptr()),
                                   workspace.numel() * workspace.element_size(),
                                   _stream_ptr(Q.device, stream))
+    _raise_on(st)
+    return out, lse
+
+
+def fwd_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: torch.Tensor,
+                lse: torch.Tensor | None = None, scale: float | None = None, is_causal: bool = False,
+                split_kv: int | None = None, stream=None):
+    """``fwd`` through fa_fwd_splitkv_noalloc: no device memory is allocated.
+
+    For callers that must not allocate on this path (no allocator of their
+    own, or cudaMalloc/cudaFree not allowed where they would synchronise the
+    device or could fail).  ``out`` (and ``lse``, if wanted) must be given;
+    the split-KV scratch is the library's fixed per-device buffer
+    (FA_SPLITKV_NOALLOC_SCRATCH_BYTES), so calls that overlap on the device
+    race, and a problem too large for it raises FaError.  Make the first call
+    on a device before any stream capture on it.  Returns (out, lse).
+    """
+    if out is None:
+        raise ValueError("fwd_noalloc needs a caller-provided out tensor (it allocates nothing)")
+    pb, out, lse = _problem(Q, K, V, scale, is_causal, out, lse, with_lse=False)
+    L = lib()
+    code = _dtype_code(Q)
+    with torch.cuda.device(Q.device):
+        n_split = 1
+        if pb.d in (64, 128):
+            n_split = (L.fa_fwd_splitkv_choose(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.is_causal)
+                       if split_kv is None else int(split_kv))
+        st = L.fa_fwd_splitkv_noalloc(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
+                                      ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                                      pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE,
+                                      (ctypes.c_int64 * 3)(*pb.lse_stride), n_split,
+                                      _stream_ptr(Q.device, stream))
     _raise_on(st)
     return out, lse
 

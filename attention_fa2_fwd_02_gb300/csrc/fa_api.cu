@@ -398,6 +398,10 @@ fa_status_t run_problems(fa_dtype_t dtype, int n, const fa_problem_t* problems, 
 
 }  // namespace
 
+namespace fa {
+fa_status_t report_error(fa_status_t st, const std::string& msg) { return fail(st, msg); }
+}  // namespace fa
+
 extern "C" {
 
 fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,

@@ -5,6 +5,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <string>
+
+#include "fa.h"
 #include "fa_tc.cuh"
 
 namespace fa {
@@ -31,6 +34,10 @@ cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d64_split(const TcLaunch& L);
+
+// Records `msg` as the calling thread's fa_last_error() text and returns st
+// (for entry points defined outside fa_api.cu).
+fa_status_t report_error(fa_status_t st, const std::string& msg);
 
 // Tile geometry shared with the instantiations in fa_tc_*.cu: key-tile width and TMA box width (one 128-byte swizzle row).
 constexpr int tc_key_tile(bool fp32, int d) { return fp32 ? (d == 128 ? 32 : 64) : 128; }

@@ -152,6 +152,48 @@ fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, 
                            int n_split, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory.  The source pages have no counterpart to this entry point:
+ * it exists only for how a caller manages memory, not for what is computed.
+ *
+ * Who needs it: a caller with no device allocator of its own (a plain C
+ * host program that does not want to own and size a workspace), and a caller
+ * that must not call cudaMalloc / cudaFree on its hot path, because those
+ * calls can synchronise the device, take driver locks, or fail with
+ * out-of-memory at a point where the caller cannot recover (a latency-bound
+ * serving loop, a real-time thread).  This call allocates nothing: the
+ * partial results go to one fixed scratch buffer per device that is part of
+ * the library image, FA_SPLITKV_NOALLOC_SCRATCH_BYTES (128 MiB) in size.
+ *
+ *   Arguments   as fa_fwd_splitkv, without the workspace.  n_split = 1 is
+ *               fa_fwd and uses no scratch; fa_fwd_splitkv_choose gives a
+ *               good n_split.
+ *   Size limit  a problem whose scratch need,
+ *               fa_fwd_splitkv_workspace_bytes(B, H, N_q, d, n_split), is
+ *               above FA_SPLITKV_NOALLOC_SCRATCH_BYTES is rejected on the
+ *               host with FA_ERR_UNSUPPORTED and a message giving both sizes
+ *               (nothing is launched): use fewer splits, or fa_fwd_splitkv
+ *               with your own workspace.
+ *   First call  on each device, the first call (with that device current)
+ *               looks up the scratch buffer's device address; that lookup
+ *               makes the CUDA runtime load this part of the library onto
+ *               the device.  Make that first call before any stream capture
+ *               on the device.
+ *   Races       there is ONE buffer per device.  Calls that can overlap on
+ *               the device (different streams, or different host threads
+ *               without ordering between their streams) race on it and give
+ *               wrong results.  Calls issued in order on one stream are safe.
+ *   Contents    every scratch element the merge step reads is first written
+ *               by the same call, so nothing needs clearing between calls.
+ */
+#define FA_SPLITKV_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
+
+fa_status_t fa_fwd_splitkv_noalloc(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                                   const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                                   int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                                   int n_split, void* stream);
+
+/*
  * fa_check -- synchronise `stream`, then read and clear the device error word
  * raised by kernels launched from this library on the current device.
  * Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait expired in some launch since

@@ -14,7 +14,10 @@ flash_attention_reference; "Blackwell Attention Example", kernel docstring):
 
 * O = softmax(scale * Q K^T) V per (batch, head) slice, SDPA layout [..., N, d];
 * LSE = log sum_j exp(s_ij), natural log of the scaled scores;
-* causal: key j visible to query row i iff j <= i (top-left alignment).
+* causal: key j visible to query row i iff j <= i (top-left alignment);
+* backward ("Blackwell Attention Example", section "Backward Kernel
+  Implementation"): the gradients of sum(dO * O) with respect to Q, K and V,
+  with delta_i = dO_i . O_i and dS = P (dP - delta).
 """
 from __future__ import annotations
 
@@ -64,6 +67,16 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p,
             ]
             lib.oracle_num_threads.restype = ctypes.c_int
+            g = lib.oracle_attention_bwd_slice
+            g.restype = ctypes.c_int
+            g.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ]
             _lib = lib
     return _lib
 
@@ -120,3 +133,44 @@ def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
         if rc != 0:
             raise RuntimeError(f"oracle_attention_slice failed with {rc}")
     return O.reshape(*lead, n_rows, d), L.reshape(*lead, n_rows)
+
+
+def attention_bwd(Q, K, V, dO, scale: float, is_causal: bool = False, q_rows=None, k_rows=None):
+    """fp64 gradients (dQ, dK, dV) of sum(dO * O) for every (batch..., head) slice.
+
+    Q, dO: [..., N_q, d]; K, V: [..., N_k, d].  q_rows / k_rows: optional 1-D
+    sequences of query / key rows to evaluate in every slice (default all).
+    Returns float64 numpy arrays dQ [..., n_q_rows, d], dK and dV [..., n_k_rows, d].
+    """
+    Q, K, V, dO = _as_f32(Q), _as_f32(K), _as_f32(V), _as_f32(dO)
+    if Q.ndim < 2 or K.shape != V.shape or Q.shape != dO.shape or Q.shape[:-2] != K.shape[:-2] \
+            or Q.shape[-1] != K.shape[-1]:
+        raise ValueError(f"bad shapes Q{Q.shape} K{K.shape} V{V.shape} dO{dO.shape}")
+    lead = Q.shape[:-2]
+    N_q, d = Q.shape[-2:]
+    N_k = K.shape[-2]
+
+    def rows_of(rows, n):
+        if rows is None:
+            return None, n
+        a = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        return a, a.size
+    qr, nq = rows_of(q_rows, N_q)
+    kr, nk = rows_of(k_rows, N_k)
+    Qs = np.ascontiguousarray(Q.reshape(-1, N_q, d))
+    Gs = np.ascontiguousarray(dO.reshape(-1, N_q, d))
+    Ks = np.ascontiguousarray(K.reshape(-1, N_k, d))
+    Vs = np.ascontiguousarray(V.reshape(-1, N_k, d))
+    dQ = np.empty((Qs.shape[0], nq, d), dtype=np.float64)
+    dK = np.empty((Qs.shape[0], nk, d), dtype=np.float64)
+    dV = np.empty((Qs.shape[0], nk, d), dtype=np.float64)
+    lib = _load()
+    for s in range(Qs.shape[0]):
+        rc = lib.oracle_attention_bwd_slice(
+            Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d, Gs[s].ctypes.data, d,
+            N_q, N_k, d, float(scale), int(bool(is_causal)),
+            None if qr is None else qr.ctypes.data, nq, None if kr is None else kr.ctypes.data, nk,
+            dQ[s].ctypes.data, dK[s].ctypes.data, dV[s].ctypes.data)
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_bwd_slice failed with {rc}")
+    return dQ.reshape(*lead, nq, d), dK.reshape(*lead, nk, d), dV.reshape(*lead, nk, d)

@@ -116,3 +116,148 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
   }
   return failed == 1 ? -1 : (failed == 2 ? -2 : 0);
 }
+
+/*
+ * Backward of one (batch, head) slice, fp64, from the plain definition.
+ *
+ * With P = softmax(scale * Q K^T) (causal: entries with key j > query i are
+ * zero), O = P V and an incoming gradient dO of O, the gradients of the
+ * scalar sum(dO * O) are ("Blackwell Attention Example", section "Backward
+ * Kernel Implementation": the preprocess row sum and the four products of the
+ * backward kernel, written here in natural-log form):
+ *
+ *   dV_j    = sum_i P_ij dO_i
+ *   dP_ij   = dO_i . V_j
+ *   delta_i = dO_i . O_i                     (= sum_j P_ij dP_ij)
+ *   dS_ij   = P_ij (dP_ij - delta_i)
+ *   dQ_i    = scale * sum_j dS_ij K_j
+ *   dK_j    = scale * sum_i dS_ij Q_i
+ *
+ * Untiled: first every query row's max, sum, O and delta (all rows, since dK
+ * and dV need them), then dQ for the requested query rows and dK, dV for the
+ * requested key rows, each by a plain loop over the other index.
+ *   q_rows[0..n_q_rows), k_rows[0..n_k_rows): rows to evaluate (NULL = all).
+ *   dQ: n_q_rows x d, dK and dV: n_k_rows x d doubles.
+ * Returns 0 on success, -1 on bad arguments, -2 if scratch allocation failed.
+ */
+int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
+                               const float* K, int64_t k_row_stride,
+                               const float* V, int64_t v_row_stride,
+                               const float* dO, int64_t do_row_stride,
+                               int64_t N_q, int64_t N_k, int64_t d,
+                               double scale, int is_causal,
+                               const int64_t* q_rows, int64_t n_q_rows,
+                               const int64_t* k_rows, int64_t n_k_rows,
+                               double* dQ, double* dK, double* dV) {
+  if (!Q || !K || !V || !dO || N_q <= 0 || N_k <= 0 || d <= 0 || n_q_rows < 0 || n_k_rows < 0)
+    return -1;
+  if ((!q_rows && n_q_rows != N_q) || (!k_rows && n_k_rows != N_k)) return -1;
+  if ((n_q_rows > 0 && !dQ) || (n_k_rows > 0 && (!dK || !dV))) return -1;
+  for (int64_t r = 0; q_rows && r < n_q_rows; ++r)
+    if (q_rows[r] < 0 || q_rows[r] >= N_q) return -1;
+  for (int64_t r = 0; k_rows && r < n_k_rows; ++r)
+    if (k_rows[r] < 0 || k_rows[r] >= N_k) return -1;
+
+  double* lse = (double*)malloc((size_t)N_q * sizeof(double));
+  double* delta = (double*)malloc((size_t)N_q * sizeof(double));
+  if (!lse || !delta) {
+    free(lse);
+    free(delta);
+    return -2;
+  }
+  int failed = 0;
+
+  /* row statistics: LSE_i = log sum_j exp(s_ij), O_i, delta_i = dO_i . O_i */
+#pragma omp parallel
+  {
+    double* s = (double*)malloc((size_t)N_k * sizeof(double));
+    double* o = (double*)malloc((size_t)d * sizeof(double));
+    if (!s || !o) {
+#pragma omp atomic write
+      failed = 2;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t i = 0; i < N_q; ++i) {
+      if (!s || !o) continue;
+      const int64_t n_vis = (is_causal && i + 1 < N_k) ? i + 1 : N_k;
+      const float* q = Q + i * q_row_stride;
+      double m = -INFINITY;
+      for (int64_t j = 0; j < n_vis; ++j) {
+        const float* k = K + j * k_row_stride;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += (double)q[c] * (double)k[c];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+      }
+      double l = 0.0;
+      for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t j = 0; j < n_vis; ++j) {
+        const double p = exp(s[j] - m);
+        const float* v = V + j * v_row_stride;
+        l += p;
+        for (int64_t c = 0; c < d; ++c) o[c] += p * (double)v[c];
+      }
+      const float* g = dO + i * do_row_stride;
+      double dl = 0.0;
+      for (int64_t c = 0; c < d; ++c) dl += (double)g[c] * (o[c] / l);
+      lse[i] = m + log(l);
+      delta[i] = dl;
+    }
+    free(s);
+    free(o);
+  }
+
+  /* dQ_i = scale * sum_j P_ij (dP_ij - delta_i) K_j */
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t r = 0; r < n_q_rows; ++r) {
+    if (failed) continue;
+    const int64_t i = q_rows ? q_rows[r] : r;
+    const int64_t n_vis = (is_causal && i + 1 < N_k) ? i + 1 : N_k;
+    const float* q = Q + i * q_row_stride;
+    const float* g = dO + i * do_row_stride;
+    double* out = dQ + r * d;
+    for (int64_t c = 0; c < d; ++c) out[c] = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+      const float* k = K + j * k_row_stride;
+      const float* v = V + j * v_row_stride;
+      double dot = 0.0, dp = 0.0;
+      for (int64_t c = 0; c < d; ++c) {
+        dot += (double)q[c] * (double)k[c];
+        dp += (double)g[c] * (double)v[c];
+      }
+      const double p = exp(scale * dot - lse[i]);
+      const double ds = p * (dp - delta[i]);
+      for (int64_t c = 0; c < d; ++c) out[c] += scale * ds * (double)k[c];
+    }
+  }
+
+  /* dV_j = sum_i P_ij dO_i,  dK_j = scale * sum_i dS_ij Q_i  (i sees j) */
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t r = 0; r < n_k_rows; ++r) {
+    if (failed) continue;
+    const int64_t j = k_rows ? k_rows[r] : r;
+    const float* k = K + j * k_row_stride;
+    const float* v = V + j * v_row_stride;
+    double* gk = dK + r * d;
+    double* gv = dV + r * d;
+    for (int64_t c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+    for (int64_t i = is_causal ? j : 0; i < N_q; ++i) {
+      const float* q = Q + i * q_row_stride;
+      const float* g = dO + i * do_row_stride;
+      double dot = 0.0, dp = 0.0;
+      for (int64_t c = 0; c < d; ++c) {
+        dot += (double)q[c] * (double)k[c];
+        dp += (double)g[c] * (double)v[c];
+      }
+      const double p = exp(scale * dot - lse[i]);
+      const double ds = p * (dp - delta[i]);
+      for (int64_t c = 0; c < d; ++c) {
+        gv[c] += p * (double)g[c];
+        gk[c] += scale * ds * (double)q[c];
+      }
+    }
+  }
+  free(lse);
+  free(delta);
+  return failed ? -2 : 0;
+}

@@ -22,7 +22,7 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["fwd", "fwd_noalloc", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
+__all__ = ["fwd", "fwd_noalloc", "bwd", "attention", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
            "LIB_PATH", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT"]
 
@@ -107,6 +107,12 @@ def lib() -> ctypes.CDLL:
                                                  P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
                                                  ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int,
                                                  ctypes.c_void_p]
+            L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
+            L.fa_bwd.restype = ctypes.c_int
+            L.fa_bwd.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 5 + [P(FaTensor)] * 5 +
+                                 [ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_float, ctypes.c_int] +
+                                 [P(FaTensor)] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
             _lib = L
     return _lib
 
@@ -260,6 +266,81 @@ def fwd_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: torch.Te
                                       _stream_ptr(Q.device, stream))
     _raise_on(st)
     return out, lse
+
+
+def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE: torch.Tensor,
+        dO: torch.Tensor, scale: float | None = None, is_causal: bool = False,
+        dQ: torch.Tensor | None = None, dK: torch.Tensor | None = None, dV: torch.Tensor | None = None,
+        workspace: torch.Tensor | None = None, stream=None):
+    """(dQ, dK, dV) of sum(dO * O) for O, LSE = fwd(Q, K, V, scale, is_causal).
+
+    bf16 tensors, head dim 64 or 128; LSE fp32 as ``fwd`` returns it.
+    Missing outputs and the scratch ``workspace`` (a CUDA uint8 tensor of
+    fa_bwd_workspace_bytes) are allocated here from PyTorch's allocator.
+    Asynchronous on the current (or given) stream.
+    """
+    if not all(t.is_cuda for t in (Q, K, V, O, LSE, dO)):
+        raise ValueError("Q, K, V, O, LSE, dO must be CUDA tensors (this library has no CPU path)")
+    q4, k4, v4, o4, g4 = _as4(Q), _as4(K), _as4(V), _as4(O), _as4(dO)
+    B, H, N_q, d = q4.shape
+    N_k = k4.shape[2]
+    if o4.shape != q4.shape or g4.shape != q4.shape or v4.shape != k4.shape or k4.shape[0] != B or \
+            k4.shape[1] != H or k4.shape[3] != d:
+        raise ValueError("shape mismatch between Q, K, V, O and dO")
+    if LSE.dtype != torch.float32 or LSE.shape != Q.shape[:-1]:
+        raise ValueError("LSE must be fp32 with Q's leading shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for name, t, ref in (("dQ", dQ, Q), ("dK", dK, K), ("dV", dV, V)):
+        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError(f"{name} must match the shape, dtype and device of its input")
+    L = lib()
+    need = L.fa_bwd_workspace_bytes(B, H, N_q, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    if workspace.device != Q.device or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA buffer of >= {need} bytes on Q's device")
+    l3 = LSE
+    while l3.dim() < 3:
+        l3 = l3.unsqueeze(0)
+    with torch.cuda.device(Q.device):
+        st = L.fa_bwd(_dtype_code(Q), B, H, N_q, N_k, d,
+                      ctypes.byref(_ft(q4)), ctypes.byref(_ft(k4)), ctypes.byref(_ft(v4)), ctypes.byref(_ft(o4)),
+                      ctypes.byref(_ft(g4)), ctypes.c_void_p(l3.data_ptr()), (ctypes.c_int64 * 3)(*l3.stride()),
+                      float(scale), 1 if is_causal else 0,
+                      ctypes.byref(_ft(_as4(dQ))), ctypes.byref(_ft(_as4(dK))), ctypes.byref(_ft(_as4(dV))),
+                      ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                      _stream_ptr(Q.device, stream))
+    _raise_on(st)
+    return dQ, dK, dV
+
+
+class _Attention(torch.autograd.Function):
+    """Autograd wrapper: forward through fa_fwd, backward through fa_bwd."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, scale, is_causal):
+        O, LSE = fwd(Q, K, V, scale=scale, is_causal=is_causal)
+        ctx.save_for_backward(Q, K, V, O, LSE)
+        ctx.scale, ctx.is_causal = scale, is_causal
+        return O
+
+    @staticmethod
+    def backward(ctx, dO):
+        Q, K, V, O, LSE = ctx.saved_tensors
+        dQ, dK, dV = bwd(Q, K, V, O, LSE, dO.contiguous(), scale=ctx.scale, is_causal=ctx.is_causal)
+        return dQ, dK, dV, None, None
+
+
+def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None = None,
+              is_causal: bool = False) -> torch.Tensor:
+    """softmax(scale * Q K^T) V with autograd: forward and backward on the GPU."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    return _Attention.apply(Q, K, V, float(scale), bool(is_causal))
 
 
 def fwd_grouped(problems, stream=None):

@@ -58,6 +58,11 @@ fa_status_t device_state(DevState** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("cudaGetDevice", e));
   if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device ordinal out of range");
+  // Bind the device's primary context to the calling thread: the tensor maps
+  // are encoded with a driver call, which needs a current context, and a
+  // thread that has made no runtime call yet (an autograd worker, say) has
+  // none.
+  if ((e = cudaSetDevice(dev)) != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("cudaSetDevice", e));
   std::lock_guard<std::mutex> lk(g_mu);
   DevState& s = g_dev[dev];
   if (!s.ready) {
@@ -396,6 +401,43 @@ fa_status_t run_problems(fa_dtype_t dtype, int n, const fa_problem_t* problems, 
   return FA_OK;
 }
 
+// Backward workspace (caller-owned): fp32 dQ accumulator [B*H][N_qp][d], then
+// LSE * log2(e) and delta, [B*H][N_qp] each; every part 256-byte aligned.
+// N_qp = N_q rounded up to the 128-row query tile.
+struct BwdWs {
+  float* dq_acc = nullptr;
+  float* lse2 = nullptr;
+  float* delta = nullptr;
+};
+size_t bwd_part(size_t bytes) { return (bytes + 255) & ~size_t(255); }
+size_t bwd_ws_bytes(long long B, long long H, long long N_q, long long d) {
+  const size_t rows = static_cast<size_t>(B) * H * ((N_q + 127) / 128 * 128);
+  return bwd_part(rows * d * 4) + 2 * bwd_part(rows * 4);
+}
+BwdWs bwd_ws_layout(void* ws, long long B, long long H, long long N_q, long long d) {
+  const size_t rows = static_cast<size_t>(B) * H * ((N_q + 127) / 128 * 128);
+  BwdWs w;
+  char* c = static_cast<char*>(ws);
+  w.dq_acc = reinterpret_cast<float*>(c);
+  w.lse2 = reinterpret_cast<float*>(c + bwd_part(rows * d * 4));
+  w.delta = reinterpret_cast<float*>(c + bwd_part(rows * d * 4) + bwd_part(rows * 4));
+  return w;
+}
+
+// A bf16 [B, H, N, d] view the backward reads or writes row-wise: non-null,
+// unit inner stride, non-negative strides, 16-byte aligned base and strides.
+fa_status_t check_bwd_tensor(const fa_tensor_t* t, const char* name) {
+  if (!t || !tensor_ok(*t)) return fail(FA_ERR_INVALID_ARG, std::string(name) + " needs a non-null pointer and stride[3] == 1");
+  if (reinterpret_cast<uintptr_t>(t->ptr) % 16 != 0)
+    return fail(FA_ERR_UNSUPPORTED, std::string(name) + " must be 16-byte aligned");
+  for (int i = 0; i < 3; ++i) {
+    if (t->stride[i] < 0) return fail(FA_ERR_UNSUPPORTED, std::string(name) + ": negative strides are not supported");
+    if ((t->stride[i] * 2) % 16 != 0)
+      return fail(FA_ERR_UNSUPPORTED, std::string(name) + ": strides must be multiples of 16 bytes");
+  }
+  return FA_OK;
+}
+
 }  // namespace
 
 namespace fa {
@@ -484,6 +526,116 @@ fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, 
   if ((st = device_state(&ds)) != FA_OK) return st;
   return launch_tensor_core(dtype, pb, *ds, static_cast<cudaStream_t>(stream), n_split,
                             split_ws_layout(workspace, B, H, N_q, d, n_split));
+}
+
+size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d) {
+  if (B <= 0 || H <= 0 || N_q <= 0 || d <= 0 || N_q >= (1ll << 31)) return 0;
+  return bwd_ws_bytes(B, H, N_q, d);
+}
+
+fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                   const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, const fa_tensor_t* O,
+                   const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale, int is_causal,
+                   const fa_tensor_t* dQ, const fa_tensor_t* dK, const fa_tensor_t* dV, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
+  if (!LSE || !lse_stride) return fail(FA_ERR_INVALID_ARG, "the backward needs the forward's LSE and its strides");
+  fa_problem_t pb{};
+  pb.B = B;
+  pb.H = H;
+  pb.N_q = N_q;
+  pb.N_k = N_k;
+  pb.d = d;
+  pb.Q = *Q;
+  pb.K = *K;
+  pb.V = *V;
+  pb.O = *O;
+  pb.LSE = const_cast<float*>(LSE);
+  for (int i = 0; i < 3; ++i) pb.lse_stride[i] = lse_stride[i];
+  pb.scale = scale;
+  pb.is_causal = is_causal;
+  Path path;
+  fa_status_t st = validate(dtype, pb, 0, &path);
+  if (st != FA_OK) return st;
+  if (dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "the backward supports bf16 inputs only");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "the backward supports head dims 64 and 128");
+  if ((st = check_bwd_tensor(dO, "dO")) != FA_OK || (st = check_bwd_tensor(dQ, "dQ")) != FA_OK ||
+      (st = check_bwd_tensor(dK, "dK")) != FA_OK || (st = check_bwd_tensor(dV, "dV")) != FA_OK)
+    return st;
+  const long long n_kt = (N_k + 127) / 128, n_qt = (N_q + 127) / 128;
+  if (B * H * n_kt >= (1ll << 31) || B * H * n_qt * 128 >= (1ll << 40))
+    return fail(FA_ERR_UNSUPPORTED, "too many backward work units");
+  if (!workspace) return fail(FA_ERR_INVALID_ARG, "the backward needs a workspace");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(FA_ERR_INVALID_ARG, "the backward workspace must be 256-byte aligned");
+  const size_t need = bwd_ws_bytes(B, H, N_q, d);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "backward workspace too small: " + std::to_string(workspace_bytes) + " < " +
+                                        std::to_string(need) + " bytes");
+  DevState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  const BwdWs ws = bwd_ws_layout(workspace, B, H, N_q, d);
+  BwdLaunch L{};
+  if ((st = make_map(&L.tmQ, *Q, false, B, H, N_q, (int)d, 128, "Q")) != FA_OK) return st;
+  if ((st = make_map(&L.tmdO, *dO, false, B, H, N_q, (int)d, 128, "dO")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, *K, false, B, H, N_k, (int)d, 128, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, *V, false, B, H, N_k, (int)d, 128, "V")) != FA_OK) return st;
+  const int N_qp = (int)(n_qt * 128);
+  BwdParams& p = L.p;
+  p.B = (int)B;
+  p.H = (int)H;
+  p.N_q = (int)N_q;
+  p.N_k = (int)N_k;
+  p.causal = is_causal;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.n_qt = (int)n_qt;
+  p.n_kt = (int)n_kt;
+  p.N_qp = N_qp;
+  p.n_units = (int)(B * H * n_kt);
+  p.lse2 = ws.lse2;
+  p.delta = ws.delta;
+  p.dq_acc = ws.dq_acc;
+  p.dK = dK->ptr;
+  p.dV = dV->ptr;
+  for (int i = 0; i < 3; ++i) {
+    p.dk_stride[i] = dK->stride[i];
+    p.dv_stride[i] = dV->stride[i];
+  }
+  p.err = ds->err;
+  p.timeout_ns = g_timeout_ns.load();
+  BwdPreParams& pre = L.pre;
+  pre.B = (int)B;
+  pre.H = (int)H;
+  pre.N_q = (int)N_q;
+  pre.N_qp = N_qp;
+  pre.O = O->ptr;
+  pre.dO = dO->ptr;
+  pre.LSE = LSE;
+  for (int i = 0; i < 3; ++i) {
+    pre.o_stride[i] = O->stride[i];
+    pre.do_stride[i] = dO->stride[i];
+    pre.lse_stride[i] = lse_stride[i];
+  }
+  pre.lse2 = ws.lse2;
+  pre.delta = ws.delta;
+  pre.dq_acc = ws.dq_acc;
+  BwdPostParams& post = L.post;
+  post.B = (int)B;
+  post.H = (int)H;
+  post.N_q = (int)N_q;
+  post.N_qp = N_qp;
+  post.scale = scale;
+  post.dq_acc = ws.dq_acc;
+  post.dQ = dQ->ptr;
+  for (int i = 0; i < 3; ++i) post.dq_stride[i] = dQ->stride[i];
+  L.d = (int)d;
+  L.grid = p.n_units < ds->sm_count ? p.n_units : ds->sm_count;
+  L.device = ds->device;
+  L.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_bf16(L);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("backward launch", e));
+  return FA_OK;
 }
 
 fa_status_t fa_check(void* stream_ptr) {

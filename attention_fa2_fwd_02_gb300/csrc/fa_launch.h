@@ -8,6 +8,7 @@
 #include <string>
 
 #include "fa.h"
+#include "fa_bwd.cuh"
 #include "fa_tc.cuh"
 
 namespace fa {
@@ -34,6 +35,20 @@ cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d64_split(const TcLaunch& L);
+
+// Backward pass (fa_bwd.cu): preprocess, tensor-core kernel and dQ
+// conversion on one stream.  bf16 only; d = 64 or 128.
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmdO;
+  BwdParams p;
+  BwdPreParams pre;
+  BwdPostParams post;
+  int d;
+  int grid;
+  int device;
+  cudaStream_t stream;
+};
+cudaError_t launch_bwd_bf16(const BwdLaunch& L);
 
 // Records `msg` as the calling thread's fa_last_error() text and returns st
 // (for entry points defined outside fa_api.cu).

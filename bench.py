@@ -207,12 +207,51 @@ def workload_desc(w) -> dict:
 
 
 def get_workload(name):
+    """The workload; names ending in ``_bwd`` time the backward pass of the
+    named forward workload (bf16, d = 64 or 128)."""
     from attention_fa2_fwd_02_gb300.inputs import AXIAL, WORKLOADS
     if name == "axial":
         return AXIAL
-    if name not in WORKLOADS:
-        raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)} or axial")
-    return WORKLOADS[name]
+    base = name[:-4] if name.endswith("_bwd") else name
+    if base not in WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)}, axial, "
+                         f"or <bf16 workload>_bwd")
+    w = WORKLOADS[base]
+    if name.endswith("_bwd") and (w.dtype != torch.bfloat16 or w.d not in (64, 128)):
+        raise SystemExit(f"{name}: the backward runs on bf16 workloads with d = 64 or 128")
+    return w
+
+
+def bwd_flops(w) -> float:
+    """Backward FLOPs: five products of 2*N_q*N_k*d each per (b, h) (S, dP, dV,
+    dK, dQ), i.e. 2.5x the forward's two; halved when causal."""
+    return 2.5 * w.flops
+
+
+def bwd_oracle_sample(w, Q, K, V, G, budget_s: float):
+    """The backward oracle (as it stands) on the leading n x n block of random
+    (b, h) slices, n grown until one call takes ~budget_s / 4; returns
+    (algorithmic flops, seconds, description)."""
+    import oracle
+    oracle.build()
+    g = np.random.default_rng(0)
+    n = 128
+    flops, calls, t0 = 0.0, 0, time.perf_counter()
+    while True:
+        b, h = int(g.integers(w.B)), int(g.integers(w.H))
+        nq, nk = min(n, w.N_q), min(n, w.N_k)
+        t1 = time.perf_counter()
+        oracle.attention_bwd(Q[b, h, :nq], K[b, h, :nk], V[b, h, :nk], G[b, h, :nq], w.scale, w.causal)
+        one = time.perf_counter() - t1
+        flops += 10.0 * nq * nk * w.d * (0.5 if w.causal else 1.0)
+        calls += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+        if one < budget_s / 8 and n < min(w.N_q, w.N_k):
+            n *= 2
+    dt = time.perf_counter() - t0
+    return flops, dt, (f"{calls} backward calls on leading blocks (up to {n}x{n}) of random (b,h) slices "
+                       f"of the same inputs; flops counted as 10*n_q*n_k*d (halved causal)")
 
 
 # ------------------------------------------------------------ CPU oracle leg
@@ -266,6 +305,31 @@ def run_reference(args, w):
     oracle.build()
     Q, K, V = w.make()
     steps, warm = args.steps, max(3, args.warmup)
+    if args.workload.endswith("_bwd"):
+        from attention_fa2_fwd_02_gb300.inputs import normal
+        G = normal(Q.shape, 4242, torch.bfloat16)
+        budget = max(0.05, 120.0 / (steps + warm))
+        for _ in range(warm):
+            bwd_oracle_sample(w, Q, K, V, G, budget)
+        tot_f, tot_t, desc = 0.0, 0.0, ""
+        for _ in range(steps):
+            f, dt, desc = bwd_oracle_sample(w, Q, K, V, G, budget)
+            tot_f += f
+            tot_t += dt
+        val = tot_f / tot_t / 1e12
+        cfg = workload_desc(w)
+        cfg["pass"] = "backward"
+        line = {
+            "impl": "reference", "metric": "attention bwd TFLOP/s", "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": tot_t / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     # size one step so that the whole run takes about two minutes
     f, dt, _ = oracle_sample(w, Q, K, V, budget_s=0.5)
     rate = f / dt
@@ -321,18 +385,34 @@ def main():
     warm = max(3, args.warmup)
     steps = max(1, args.steps)
     axial = isinstance(w, AxialWorkload)
+    bwd = args.workload.endswith("_bwd")
     Qh, Kh, Vh = w.make()
     Qd, Kd, Vd = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+    if bwd:
+        from attention_fa2_fwd_02_gb300.inputs import normal
+        Gh = normal(Qh.shape, 4242, torch.bfloat16)
+        Gd = Gh.to(dev)
     stream = torch.cuda.current_stream(dev)
     props = torch.cuda.get_device_properties(dev)
     l2_bytes = getattr(props, "L2_cache_size", 0) or 129 * 2**20
     in_bytes = sum(x.numel() * x.element_size() for x in (Qd, Kd, Vd))
+    if bwd:  # the backward also reads O, LSE and dO
+        in_bytes = 2 * in_bytes + Gd.numel() * 2
     flush = None
     if in_bytes <= l2_bytes:
         flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
 
     n_split = 1  # key-range splits the library picks for this problem
-    if axial:
+    if bwd:
+        # forward outputs (not timed), then the backward as the step
+        Od, Ld = fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, split_kv=1)
+        dQd, dKd, dVd = torch.empty_like(Qd), torch.empty_like(Kd), torch.empty_like(Vd)
+        ws = torch.empty(fa.lib().fa_bwd_workspace_bytes(w.B, w.H, w.N_q, w.d), dtype=torch.uint8, device=dev)
+
+        def step():
+            return fa.bwd(Qd, Kd, Vd, Od, Ld, Gd, scale=w.scale, is_causal=w.causal, dQ=dQd, dK=dKd, dV=dVd,
+                          workspace=ws)
+    elif axial:
         def step():
             return fa.axial(Qd, Kd, Vd, scale=w.scale, with_lse=True)
     else:
@@ -403,7 +483,7 @@ def main():
     # with an L2 flush between steps the step time is the kernel time only
     step_ms = kernel_ms if flush is not None else wall_ms / steps
     step_ms = max_over_ranks(step_ms, dist)
-    flops = w.flops
+    flops = bwd_flops(w) if bwd else w.flops
     value = whole_job_value(flops, world, step_ms)
 
     # --------------------------------------------------------- roofline
@@ -428,11 +508,46 @@ def main():
                 "frac": achieved / peak, "traffic": traffic, "peak_source": note}
         if n_split > 1:  # the events bracket both launches of a split step
             roof["timed"] = f"split-KV attention kernel (n_split={n_split}) + merge kernel"
+        if bwd:  # the events bracket the three launches of a backward step
+            roof["timed"] = "backward preprocess + tensor-core backward kernel + dQ conversion"
 
 
     # ------------------------------------------------------ end to end
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and bwd:
+        # through the public API from host buffers: Q, K, V, O, LSE, dO in,
+        # dQ, dK, dV out, every step
+        hp = [x.pin_memory() for x in (Qh, Kh, Vh)]
+        Op, Lp, Gp = Od.cpu().pin_memory(), Ld.cpu().pin_memory(), Gh.pin_memory()
+        outs = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (Qh, Kh, Vh)]
+
+        def e2e_step():
+            for dst, src in zip((Qd, Kd, Vd, Od, Ld, Gd), (*hp, Op, Lp, Gp)):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(outs, (dQd, dKd, dVd)):
+                dst.copy_(src, non_blocking=True)
+
+        e_steps = max(3, min(steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, dist)
+        h2d = sum(x.numel() * x.element_size() for x in (*hp, Op, Lp, Gp))
+        d2h = sum(x.numel() * x.element_size() for x in outs)
+        e2e = {"value": whole_job_value(flops, world, e_ms), "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        fa.check()
+    elif not args.no_e2e:
         Qp, Kp, Vp = (x.pin_memory() for x in (Qh, Kh, Vh))
         Op = torch.empty(Qh.shape, dtype=Qh.dtype).pin_memory()
         Lp = torch.empty(Qh.shape[:-1], dtype=torch.float32).pin_memory()
@@ -481,7 +596,10 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        f, dt, desc = oracle_sample(w, Qh, Kh, Vh, budget_s=args.cpu_seconds)
+        if bwd:
+            f, dt, desc = bwd_oracle_sample(w, Qh, Kh, Vh, Gh, budget_s=args.cpu_seconds)
+        else:
+            f, dt, desc = oracle_sample(w, Qh, Kh, Vh, budget_s=args.cpu_seconds)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                "kind": "oracle", "sample": f"{desc}; {dt:.1f} s of fp64 CPU work"}
 
@@ -492,15 +610,18 @@ def main():
         cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
         cfg["cuda_graph"] = use_graph
         cfg["split_kv"] = n_split
+        if bwd:
+            cfg["pass"] = "backward (dQ, dK, dV from Q, K, V, O, LSE, dO); FLOPs = 2.5x the forward's"
         line = {
-            "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+            "metric": "attention bwd TFLOP/s" if bwd else "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if (not axial and w.dtype == torch.bfloat16) else ("f32" if axial else "tf32"),
             "data": "synthetic (seeded i.i.d. N(0,1))", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             # one kernel per step, plus the merge kernel when the keys are split
-            "gpu_launches": steps * (2 if n_split > 1 else 1), "kernel_ms": kernel_ms,
+            # (a backward step is three launches: preprocess, kernel, dQ conversion)
+            "gpu_launches": steps * (3 if bwd else (2 if n_split > 1 else 1)), "kernel_ms": kernel_ms,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -194,6 +194,38 @@ fa_status_t fa_fwd_splitkv_noalloc(fa_dtype_t dtype, int64_t B, int64_t H, int64
                                    int n_split, void* stream);
 
 /*
+ * fa_bwd -- backward of fa_fwd: dQ, dK, dV of sum(dO * O) ("Blackwell
+ * Attention Example", section "Backward Kernel Implementation": the row-sum
+ * preprocess delta = rowsum(dO * O) and the products dV = P^T dO,
+ * dS = P * (dO V^T - delta), dQ = scale * dS K, dK = scale * dS^T Q, with
+ * P recomputed from Q, K and the forward's LSE).
+ *
+ *   dtype          FA_BF16 (FA_ERR_UNSUPPORTED for FA_FP32); every tensor bf16.
+ *   d              64 or 128.
+ *   Q, K, V        the forward's inputs; O and LSE / lse_stride its outputs
+ *                  (LSE natural log, as fa_fwd writes it).  Same views and
+ *                  rules as fa_fwd (16-byte aligned bases and strides).
+ *   dO             incoming gradient, [B, H, N_q, d] like O.
+ *   dQ, dK, dV     outputs, shaped like Q, K, V (any strides meeting the same
+ *                  alignment rules); every element is written.  Keys that no
+ *                  query sees (causal, N_k > N_q) get zero gradients.
+ *   scale, is_causal  as in the forward call.
+ *   workspace      device memory of at least fa_bwd_workspace_bytes(B, H,
+ *                  N_q, d) bytes, 256-byte aligned, caller-owned scratch (an
+ *                  fp32 dQ accumulator and two per-row vectors).  Concurrent
+ *                  calls need separate workspaces.
+ * Asynchronous on `stream` (three kernels).  Argument errors are reported on
+ * the host before any launch.
+ */
+size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d);
+
+fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
+                   const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, const fa_tensor_t* O,
+                   const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale, int is_causal,
+                   const fa_tensor_t* dQ, const fa_tensor_t* dK, const fa_tensor_t* dV, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
  * fa_check -- synchronise `stream`, then read and clear the device error word
  * raised by kernels launched from this library on the current device.
  * Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait expired in some launch since

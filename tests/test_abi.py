@@ -148,3 +148,33 @@ def test_splitkv_workspace_size(L):
     want = ((2 * rows * 64 * 4 + 255) // 256) * 256 + ((2 * rows * 4 + 255) // 256) * 256
     assert L.fa_fwd_splitkv_workspace_bytes(2, 3, 100, 64, 2) == want
     assert L.fa_fwd_splitkv_workspace_bytes(2, 3, 100, 64, 1) == 0
+
+
+def _bwd(L, dtype=fa.FA_BF16, d=128, ws=0x100000, ws_bytes=1 << 30, lse=0x50000, N=256):
+    s = (N * d, N * d, d, 1)
+    t = [_t(a, s) for a in (0x10000, 0x20000, 0x30000, 0x40000, 0x60000, 0x70000, 0x80000, 0x90000)]
+    ls = (ctypes.c_int64 * 3)(N, N, 1)
+    return L.fa_bwd(dtype, 1, 1, N, N, d, *(ctypes.byref(x) for x in t[:5]), lse, ls, 0.1, 0,
+                    *(ctypes.byref(x) for x in t[5:]), ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),  # bf16 only
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),             # the forward's LSE is required
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0x100080), fa.FA_ERR_INVALID_ARG),       # not 256-byte aligned
+    (dict(ws_bytes=4096), fa.FA_ERR_INVALID_ARG),     # too small
+])
+def test_bwd_host_validation(L, kw, status):
+    assert _bwd(L, **kw) == status
+    assert L.fa_last_error() != b""
+
+
+def test_bwd_workspace_size(L):
+    # fp32 dQ accumulator + LSE*log2(e) + delta over N_q rounded up to 128, parts 256-aligned
+    rows = 2 * 3 * 256
+    want = ((rows * 64 * 4 + 255) // 256) * 256 + 2 * (((rows * 4) + 255) // 256) * 256
+    assert L.fa_bwd_workspace_bytes(2, 3, 200, 64) == want
+    assert L.fa_bwd_workspace_bytes(0, 3, 200, 64) == 0

@@ -402,11 +402,11 @@ fa_status_t run_problems(fa_dtype_t dtype, int n, const fa_problem_t* problems, 
 }
 
 // Backward workspace (caller-owned): fp32 dQ accumulator [B*H][N_qp][d], then
-// LSE * log2(e) and delta, [B*H][N_qp] each; every part 256-byte aligned.
+// -LSE * log2(e) and delta, [B*H][N_qp] each; every part 256-byte aligned.
 // N_qp = N_q rounded up to the 128-row query tile.
 struct BwdWs {
   float* dq_acc = nullptr;
-  float* lse2 = nullptr;
+  float* nlse2 = nullptr;
   float* delta = nullptr;
 };
 size_t bwd_part(size_t bytes) { return (bytes + 255) & ~size_t(255); }
@@ -419,7 +419,7 @@ BwdWs bwd_ws_layout(void* ws, long long B, long long H, long long N_q, long long
   BwdWs w;
   char* c = static_cast<char*>(ws);
   w.dq_acc = reinterpret_cast<float*>(c);
-  w.lse2 = reinterpret_cast<float*>(c + bwd_part(rows * d * 4));
+  w.nlse2 = reinterpret_cast<float*>(c + bwd_part(rows * d * 4));
   w.delta = reinterpret_cast<float*>(c + bwd_part(rows * d * 4) + bwd_part(rows * 4));
   return w;
 }
@@ -562,7 +562,8 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   if ((st = check_bwd_tensor(dO, "dO")) != FA_OK || (st = check_bwd_tensor(dQ, "dQ")) != FA_OK ||
       (st = check_bwd_tensor(dK, "dK")) != FA_OK || (st = check_bwd_tensor(dV, "dV")) != FA_OK)
     return st;
-  const long long n_kt = (N_k + 127) / 128, n_qt = (N_q + 127) / 128;
+  const long long bm = d == 128 ? 64 : 128;  // query rows per step of the backward kernel
+  const long long n_kt = (N_k + 127) / 128, n_qt = (N_q + bm - 1) / bm;
   if (B * H * n_kt >= (1ll << 31) || B * H * n_qt * 128 >= (1ll << 40))
     return fail(FA_ERR_UNSUPPORTED, "too many backward work units");
   if (!workspace) return fail(FA_ERR_INVALID_ARG, "the backward needs a workspace");
@@ -576,11 +577,11 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   if ((st = device_state(&ds)) != FA_OK) return st;
   const BwdWs ws = bwd_ws_layout(workspace, B, H, N_q, d);
   BwdLaunch L{};
-  if ((st = make_map(&L.tmQ, *Q, false, B, H, N_q, (int)d, 128, "Q")) != FA_OK) return st;
-  if ((st = make_map(&L.tmdO, *dO, false, B, H, N_q, (int)d, 128, "dO")) != FA_OK) return st;
+  if ((st = make_map(&L.tmQ, *Q, false, B, H, N_q, (int)d, (int)bm, "Q")) != FA_OK) return st;
+  if ((st = make_map(&L.tmdO, *dO, false, B, H, N_q, (int)d, (int)bm, "dO")) != FA_OK) return st;
   if ((st = make_map(&L.tmK, *K, false, B, H, N_k, (int)d, 128, "K")) != FA_OK) return st;
   if ((st = make_map(&L.tmV, *V, false, B, H, N_k, (int)d, 128, "V")) != FA_OK) return st;
-  const int N_qp = (int)(n_qt * 128);
+  const int N_qp = (int)((N_q + 127) / 128 * 128);  // workspace row pitch
   BwdParams& p = L.p;
   p.B = (int)B;
   p.H = (int)H;
@@ -593,7 +594,7 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   p.n_kt = (int)n_kt;
   p.N_qp = N_qp;
   p.n_units = (int)(B * H * n_kt);
-  p.lse2 = ws.lse2;
+  p.nlse2 = ws.nlse2;
   p.delta = ws.delta;
   p.dq_acc = ws.dq_acc;
   p.dK = dK->ptr;
@@ -617,7 +618,7 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
     pre.do_stride[i] = dO->stride[i];
     pre.lse_stride[i] = lse_stride[i];
   }
-  pre.lse2 = ws.lse2;
+  pre.nlse2 = ws.nlse2;
   pre.delta = ws.delta;
   pre.dq_acc = ws.dq_acc;
   BwdPostParams& post = L.post;

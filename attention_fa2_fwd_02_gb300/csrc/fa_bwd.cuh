@@ -9,24 +9,30 @@
 //     dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Three launches:
-//  * fa_bwd_pre_kernel: delta and LSE * log2(e) per query row into the
-//    workspace (padded rows: delta = 0, LSE = +inf, so their P is exactly 0),
+//  * fa_bwd_pre_kernel: delta and -LSE * log2(e) per query row into the
+//    workspace (padded rows: delta = 0, -LSE = -inf, so their P is exactly 0),
 //    and the fp32 dQ accumulator zeroed;
-//  * fa_bwd_kernel: one work unit = one 128-key tile of one (b, h).  It keeps
-//    K_j, V_j in shared memory and dK_j, dV_j in tensor memory, and walks the
-//    128-row query tiles that see it: S^T = K_j Q_i^T and dP^T = V_j dO_i^T
-//    (lanes = keys), P^T and dS^T by the compute warpgroup, then
-//    dV += P^T dO_i and dK += dS^T Q_i with the A operand in tensor memory,
-//    and dQ_i = dS K_j with dS^T staged in shared memory (the A operand must
-//    have the query rows in lanes, which only the transposed copy provides);
-//    dQ_i is added into the fp32 accumulator with vector reductions;
+//  * fa_bwd_kernel: one work unit = one 128-key tile j of one (b, h).  K_j, V_j
+//    stay in shared memory and dK_j, dV_j accumulate in tensor memory while
+//    the unit walks the query tiles that see it (BM rows per step):
+//    S^T = K_j Q_i^T and dP^T = V_j dO_i^T (lanes = keys), P^T and dS^T by two
+//    compute warpgroups (each a half of the query columns), then
+//    dV += P^T dO_i and dK += dS^T Q_i (A in tensor memory) and the step's dQ
+//    contribution from dS^T staged in shared memory; dQ goes to one of two
+//    tensor-memory buffers, so that its read-out (fp32 reductions into the
+//    accumulator) overlaps the following steps;
 //  * fa_bwd_post_kernel: dQ = scale * accumulator in the output dtype.
 //
-// Warp roles of fa_bwd_kernel (384 threads): warpgroup 0 = compute (P^T,
-// dS^T; thread = key row = tensor-memory lane), warpgroup 1 = epilogue (dQ
-// reductions; dK, dV stores at the end of a unit), warp 8 = TMA loads, warp 9
-// = MMA issue.  Tensor memory: S^T (then P^T, then dQ) | dP^T (then dS^T) |
-// dV | dK.  Every wait is bounded (Watchdog).
+// The dQ product: d = 128 uses 64-row query steps and computes dQ_i^T =
+// K_j^T dS_i^T (M = head dim = 128 lanes, N = 64 queries), d = 64 uses
+// 128-row steps and computes dQ_i = dS_i K_j (M = 128 queries, N = 64): either
+// way one 64-column buffer, with M = 128 for the tensor core.
+//
+// Warp roles (512 threads): warpgroups 0 and 1 = compute (thread = key row =
+// tensor-memory lane), warpgroup 2 = epilogue (dQ reductions; dK, dV stores
+// at the end of a unit), warp 12 = TMA loads, warp 13 = MMA issue.  Tensor
+// memory: S^T (then P^T) | dP^T (then dS^T) | dV | dK | dQ x 2.  Every wait
+// is bounded (Watchdog).
 #pragma once
 
 #include "fa_ptx.cuh"
@@ -38,12 +44,12 @@ struct BwdParams {
   int causal;
   float scale;            // softmax scale
   float scale_log2;       // scale * log2(e)
-  int n_qt, n_kt;         // query / key tiles
-  int N_qp;               // N_q rounded up to the query tile
+  int n_qt, n_kt;         // query tiles (BM rows) / key tiles (128)
+  int N_qp;               // row pitch of the workspace vectors (N_q rounded up to 128)
   int n_units;            // B * H * n_kt
-  const float* lse2;      // workspace: LSE * log2(e) [B*H][N_qp] (+inf on padding)
-  const float* delta;     // workspace: dO . O        [B*H][N_qp] (0 on padding)
-  float* dq_acc;          // workspace: fp32 dQ / scale [B*H][N_qp][D]
+  const float* nlse2;     // workspace: -LSE * log2(e) [B*H][N_qp] (-inf on padding)
+  const float* delta;     // workspace: dO . O          [B*H][N_qp] (0 on padding)
+  float* dq_acc;          // workspace: fp32 dQ / scale  [B*H][N_qp][D]
   void* dK;
   void* dV;
   long long dk_stride[3], dv_stride[3];  // elements: b, h, n
@@ -54,51 +60,56 @@ struct BwdParams {
 template <int D_>
 struct BwdCfg {
   static constexpr int D = D_;
-  static constexpr int BM = 128;  // query rows per step
-  static constexpr int BN = 128;  // keys per work unit (tensor-memory lanes)
-  static constexpr int NST = D == 128 ? 1 : 2;  // Q/dO ring depth (shared-memory budget)
-  static constexpr int kPanels = D / 64;        // 128-byte swizzle panels of 64 bf16
-  static constexpr uint32_t kRowTileBytes = 128 * D * 2;  // one 128-row bf16 tile
-  static constexpr uint32_t kPanelBytes = 128 * 128;      // one panel of a 128-row tile
+  static constexpr int BN = 128;             // keys per work unit (tensor-memory lanes)
+  static constexpr int BM = D == 128 ? 64 : 128;  // query rows per step
+  static constexpr bool kDqT = D == 128;     // dQ computed transposed (lanes = head dim)
+  static constexpr int NST = 2;              // Q/dO ring depth
+  static constexpr int kPanels = D / 64;     // 128-byte swizzle panels of 64 bf16 (head dim)
+  static constexpr int kQPanels = BM / 64;   // panels of the dS^T tile (queries)
+  static constexpr uint32_t kKVTileBytes = BN * D * 2;
+  static constexpr uint32_t kKVPanelBytes = BN * 128;
+  static constexpr uint32_t kQTileBytes = BM * D * 2;
+  static constexpr uint32_t kQPanelBytes = BM * 128;
   static constexpr uint32_t kOffK = 0;
-  static constexpr uint32_t kOffV = kOffK + kRowTileBytes;
-  static constexpr uint32_t kOffQ = kOffV + kRowTileBytes;           // [NST]
-  static constexpr uint32_t kOffdO = kOffQ + NST * kRowTileBytes;    // [NST]
-  static constexpr uint32_t kOffdS = kOffdO + NST * kRowTileBytes;   // dS^T [keys][queries], 2 panels
-  static constexpr uint32_t kOffVec = kOffdS + BN * BM * 2;          // [NST] lse2[BM], delta[BM]
+  static constexpr uint32_t kOffV = kOffK + kKVTileBytes;
+  static constexpr uint32_t kOffQ = kOffV + kKVTileBytes;          // [NST]
+  static constexpr uint32_t kOffdO = kOffQ + NST * kQTileBytes;    // [NST]
+  static constexpr uint32_t kOffdS = kOffdO + NST * kQTileBytes;   // dS^T [keys][queries]
+  static constexpr uint32_t kOffVec = kOffdS + BN * BM * 2;        // [NST] -lse2[BM], delta[BM]
   static constexpr uint32_t kOffBar = kOffVec + NST * 2 * BM * 4;
-  static constexpr int kNumBars = 9 + 2 * NST;  // + teardown
+  static constexpr int kNumBars = 11 + 2 * NST;  // + teardown
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
-  static constexpr uint32_t kThreads = 384;
+  static constexpr uint32_t kThreads = 512;
   // tensor memory columns
-  static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + D;
+  static constexpr uint32_t kColS = 0, kColdP = BM, kColdV = 2 * BM, kColdK = 2 * BM + D;
+  static constexpr uint32_t kColdQ = 2 * BM + 2 * D;  // two 64-column buffers
   static constexpr uint32_t kTmemCols = 512;
   // instruction descriptors (bf16 inputs, fp32 accumulators)
-  static constexpr uint32_t kIdescS = make_idesc(1u, 128, BM, 0, 0);     // K-major A and B
-  static constexpr uint32_t kIdescAcc = make_idesc(1u, 128, D, 0, 1);    // A in TMEM, B MN-major
-  static constexpr uint32_t kIdescdQ = make_idesc(1u, 128, D, 1, 1);     // A and B MN-major
-  static constexpr uint32_t kKVBytes = 2 * kRowTileBytes;
-  static constexpr uint32_t kStepBytes = 2 * kRowTileBytes + 2 * BM * 4;
+  static constexpr uint32_t kIdescS = make_idesc(1u, 128, BM, 0, 0);    // K-major A and B
+  static constexpr uint32_t kIdescAcc = make_idesc(1u, 128, D, 0, 1);   // A in TMEM, B MN-major
+  static constexpr uint32_t kIdescdQ = make_idesc(1u, 128, 64, 1, 1);   // A and B MN-major
+  static constexpr uint32_t kKVBytes = 2 * kKVTileBytes;
+  static constexpr uint32_t kStepBytes = 2 * kQTileBytes + 2 * BM * 4;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert(2 * 128 + 2 * D <= 512, "tensor memory budget");
+  static_assert(kColdQ + 128 == 512, "tensor memory layout");
 };
 
 struct BwdBars {
   uint64_t* kv_full;    // [1] K_j, V_j landed
   uint64_t* kv_empty;   // [1] unit's MMAs done with K_j, V_j
   uint64_t* s_full;     // [1] S^T, dP^T ready
-  uint64_t* p_full;     // [1] P^T, dS^T written (128 arrivals)
-  uint64_t* dq_full;    // [1] dQ_i ready in tensor memory
-  uint64_t* dq_empty;   // [1] dQ_i read out (128 arrivals)
+  uint64_t* p_full;     // [1] P^T, dS^T written (256 arrivals)
   uint64_t* dkv_full;   // [1] unit's dK, dV complete
   uint64_t* dkv_empty;  // [1] dK, dV read out (128 arrivals)
-  uint64_t* q_full;     // [NST] Q_i, dO_i, lse2_i, delta_i landed
+  uint64_t* dq_full;    // [2] dQ buffer ready
+  uint64_t* dq_empty;   // [2] dQ buffer read out (128 arrivals)
+  uint64_t* q_full;     // [NST] Q_i, dO_i, -lse2_i, delta_i landed
   uint64_t* q_empty;    // [NST]
 };
 
 // Work unit u -> (b*H + h, key tile j).  Causal units are taken in ascending j
-// (the longest first: key tile j is seen by query tiles j .. n_qt-1).
+// (the longest first: key tile j is seen by the query tiles from its diagonal on).
 struct BwdUnit {
   int bh, b, h, j, i0, n_steps;
 };
@@ -115,8 +126,8 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   }
   w.b = w.bh / p.H;
   w.h = w.bh - w.b * p.H;
-  // first query tile holding a row >= the tile's first key (BM == BN)
-  w.i0 = p.causal ? w.j : 0;
+  // first query tile holding a row >= the tile's first key
+  w.i0 = p.causal ? (w.j * C::BN) / C::BM : 0;
   w.n_steps = w.i0 < p.n_qt ? p.n_qt - w.i0 : 0;
   return w;
 }
@@ -134,8 +145,8 @@ __device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, u
 }
 
 // ------------------------------------------------------------- pre / post
-// One warp per padded query row: delta = dO . O (fp32), lse2 = LSE * log2(e),
-// dQ accumulator row zeroed.  Rows past N_q get delta 0 and lse2 +inf.
+// One warp per padded query row: delta = dO . O (fp32), nlse2 = -LSE * log2(e),
+// dQ accumulator row zeroed.  Rows past N_q get delta 0 and nlse2 -inf.
 struct BwdPreParams {
   int B, H, N_q, N_qp;
   const void* O;
@@ -144,7 +155,7 @@ struct BwdPreParams {
   long long do_stride[3];
   const float* LSE;
   long long lse_stride[3];
-  float* lse2;
+  float* nlse2;
   float* delta;
   float* dq_acc;
 };
@@ -174,9 +185,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__
   for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
   if (lane == 0) {
     p.delta[row] = dl;
-    p.lse2[row] = q < p.N_q ? p.LSE[b * p.lse_stride[0] + h * p.lse_stride[1] +
-                                    static_cast<long long>(q) * p.lse_stride[2]] * 1.4426950408889634f
-                            : INFINITY;
+    p.nlse2[row] = q < p.N_q ? -p.LSE[b * p.lse_stride[0] + h * p.lse_stride[1] +
+                                      static_cast<long long>(q) * p.lse_stride[2]] * 1.4426950408889634f
+                             : -INFINITY;
   }
 }
 
@@ -210,6 +221,21 @@ __device__ __forceinline__ bool bwd_warp_wait(uint64_t* bar, uint32_t parity, co
   bool ok = mbar_wait(bar, parity, wd, where);
   return __all_sync(0xffffffffu, ok);
 }
+__device__ __forceinline__ void bwd_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ void red_add_f32(float* dst, uint32_t v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(__uint_as_float(v)) : "memory");
+}
 
 template <class C>
 __device__ void bwd_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
@@ -227,9 +253,9 @@ __device__ void bwd_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, co
     mbar_arrive_expect_tx(&bars.kv_full[0], C::kKVBytes);
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn) {
-      tma_load_4d(tmK, &bars.kv_full[0], smem + C::kOffK + pn * C::kPanelBytes, pn * 64, w.j * C::BN, w.h, w.b,
+      tma_load_4d(tmK, &bars.kv_full[0], smem + C::kOffK + pn * C::kKVPanelBytes, pn * 64, w.j * C::BN, w.h, w.b,
                   pol_kv);
-      tma_load_4d(tmV, &bars.kv_full[0], smem + C::kOffV + pn * C::kPanelBytes, pn * 64, w.j * C::BN, w.h, w.b,
+      tma_load_4d(tmV, &bars.kv_full[0], smem + C::kOffV + pn * C::kKVPanelBytes, pn * 64, w.j * C::BN, w.h, w.b,
                   pol_kv);
     }
     ++kv_armed;
@@ -241,14 +267,14 @@ __device__ void bwd_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, co
       mbar_arrive_expect_tx(&bars.q_full[st], C::kStepBytes);
 #pragma unroll
       for (int pn = 0; pn < C::kPanels; ++pn) {
-        tma_load_4d(tmQ, &bars.q_full[st], smem + C::kOffQ + st * C::kRowTileBytes + pn * C::kPanelBytes, pn * 64,
+        tma_load_4d(tmQ, &bars.q_full[st], smem + C::kOffQ + st * C::kQTileBytes + pn * C::kQPanelBytes, pn * 64,
                     i * C::BM, w.h, w.b, pol_q);
-        tma_load_4d(tmdO, &bars.q_full[st], smem + C::kOffdO + st * C::kRowTileBytes + pn * C::kPanelBytes,
+        tma_load_4d(tmdO, &bars.q_full[st], smem + C::kOffdO + st * C::kQTileBytes + pn * C::kQPanelBytes,
                     pn * 64, i * C::BM, w.h, w.b, pol_q);
       }
       const long long vrow = static_cast<long long>(w.bh) * p.N_qp + i * C::BM;
       uint8_t* vec = smem + C::kOffVec + st * 2 * C::BM * 4;
-      bulk_load(vec, p.lse2 + vrow, C::BM * 4, &bars.q_full[st]);
+      bulk_load(vec, p.nlse2 + vrow, C::BM * 4, &bars.q_full[st]);
       bulk_load(vec + C::BM * 4, p.delta + vrow, C::BM * 4, &bars.q_full[st]);
       ++q_armed[st];
     }
@@ -262,11 +288,21 @@ __device__ void bwd_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, co
   }
 }
 
-// K-major operand (a 128-row bf16 tile, K = head dim): k-step kk of 16.
-template <class C>
+// k-step kk (16 elements of K) of a K-major operand: a bf16 tile whose rows are
+// M or N, K along the 128-byte swizzle panels.
+template <uint32_t kPanelBytes>
 __device__ __forceinline__ uint32_t kmajor_off(int kk) {
   const uint32_t byte = kk * 32;
-  return ((byte / 128) * C::kPanelBytes + byte % 128) >> 4;
+  return ((byte / 128) * kPanelBytes + byte % 128) >> 4;
+}
+
+// Column (within the S^T or dP^T region) of the bf16 pairs of queries
+// 16 kk .. 16 kk + 15: the compute warpgroup owning them stores them in the
+// first half of its own columns.
+template <class C>
+__device__ __forceinline__ uint32_t pcol(int kk) {
+  constexpr int kCols = C::BM / 2;
+  return (16 * kk / kCols) * kCols + (16 * kk % kCols) / 2;
 }
 
 template <class C>
@@ -282,23 +318,25 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, c
     if (w.n_steps == 0) continue;
     if (!(ok = bwd_warp_wait(&bars.kv_full[0], ku & 1u, wd, 0x62))) break;
     for (int s = 0; ok && s < w.n_steps; ++s, ++gs) {
-      const uint32_t st = gs % C::NST;
+      const uint32_t st = gs % C::NST, qb = gs & 1u;
       const bool first = (s == 0), last = (s == w.n_steps - 1);
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ + st * C::kRowTileBytes);
-      const uint32_t do_addr = smem_u32(smem + C::kOffdO + st * C::kRowTileBytes);
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ + st * C::kQTileBytes);
+      const uint32_t do_addr = smem_u32(smem + C::kOffdO + st * C::kQTileBytes);
       if (!(ok = bwd_warp_wait(&bars.q_full[st], (gs / C::NST) & 1u, wd, 0x63))) break;
-      // S^T lands where the previous step's dQ was: wait until it is read out
-      if (gs > 0 && !(ok = bwd_warp_wait(&bars.dq_empty[0], (gs - 1) & 1u, wd, 0x64))) break;
       tc_fence_after();
+      // S^T and dP^T overwrite P^T and dS^T of the previous step, whose dV
+      // and dK MMAs were issued before (in-order execution).
       if (elect_one()) {
         const uint64_t ak = sdesc_sw128<16, 1024>(k_addr), av = sdesc_sw128<16, 1024>(v_addr);
         const uint64_t bq = sdesc_sw128<16, 1024>(q_addr), bdo = sdesc_sw128<16, 1024>(do_addr);
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk)
-          mma_ss<false>(tmem + C::kColS, ak + kmajor_off<C>(kk), bq + kmajor_off<C>(kk), C::kIdescS, kk > 0);
+          mma_ss<false>(tmem + C::kColS, ak + kmajor_off<C::kKVPanelBytes>(kk), bq + kmajor_off<C::kQPanelBytes>(kk),
+                        C::kIdescS, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk)
-          mma_ss<false>(tmem + C::kColdP, av + kmajor_off<C>(kk), bdo + kmajor_off<C>(kk), C::kIdescS, kk > 0);
+          mma_ss<false>(tmem + C::kColdP, av + kmajor_off<C::kKVPanelBytes>(kk),
+                        bdo + kmajor_off<C::kQPanelBytes>(kk), C::kIdescS, kk > 0);
         tc_commit(&bars.s_full[0]);
       }
       __syncwarp();
@@ -306,31 +344,34 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, c
       // the first accumulation of a unit overwrites dK, dV: the previous
       // unit's must have been read out
       if (first && ku > 0 && !(ok = bwd_warp_wait(&bars.dkv_empty[0], (ku - 1) & 1u, wd, 0x66))) break;
+      // the dQ buffer of two steps ago must have been read out
+      if (gs >= 2 && !(ok = bwd_warp_wait(&bars.dq_empty[qb], ((gs >> 1) - 1) & 1u, wd, 0x64))) break;
       tc_fence_after();
       if (elect_one()) {
-        // dV += P^T dO_i, dK += dS^T Q_i: A in tensor memory (bf16 pairs),
+        // dV += P^T dO_i and dK += dS^T Q_i: A in tensor memory (bf16 pairs),
         // B MN-major (head dim contiguous, k = query rows in 16-row steps)
-        const uint64_t bdo = sdesc_sw128<C::kPanelBytes, 1024>(do_addr);
-        const uint64_t bq = sdesc_sw128<C::kPanelBytes, 1024>(q_addr);
+        const uint64_t bdo = sdesc_sw128<C::kQPanelBytes, 1024>(do_addr);
+        const uint64_t bq = sdesc_sw128<C::kQPanelBytes, 1024>(q_addr);
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ts<false>(tmem + C::kColdV, tmem + C::kColS + kk * 8, bdo + ((kk * 16 * 128) >> 4), C::kIdescAcc,
+          mma_ts<false>(tmem + C::kColdV, tmem + C::kColS + pcol<C>(kk), bdo + ((kk * 16 * 128) >> 4), C::kIdescAcc,
                         (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ts<false>(tmem + C::kColdK, tmem + C::kColdP + kk * 8, bq + ((kk * 16 * 128) >> 4), C::kIdescAcc,
+          mma_ts<false>(tmem + C::kColdK, tmem + C::kColdP + pcol<C>(kk), bq + ((kk * 16 * 128) >> 4), C::kIdescAcc,
                         (!first || kk > 0) ? 1u : 0u);
-        // dQ_i = dS K_j: A = dS^T in shared memory read MN-major (queries
-        // contiguous), B = K_j MN-major (head dim contiguous); k = keys.
-        // It overwrites the P^T columns, which the dV MMAs above (issued
-        // first, executed in order) have read.
-        const uint64_t ads = sdesc_sw128<C::BN * 128, 1024>(ds_addr);
-        const uint64_t bk = sdesc_sw128<C::kPanelBytes, 1024>(k_addr);
+        // dQ over the keys (k = 16-key steps of 16 rows x 128 bytes):
+        //  d = 128: dQ_i^T = K_j^T dS_i^T, A = K_j MN-major (head dim
+        //           contiguous), B = dS^T MN-major (queries contiguous);
+        //  d = 64:  dQ_i = dS_i K_j, A = dS^T MN-major, B = K_j MN-major.
+        const uint64_t dsd = sdesc_sw128<C::BN * 128, 1024>(ds_addr);
+        const uint64_t kd = sdesc_sw128<C::kKVPanelBytes, 1024>(k_addr);
+        const uint64_t a0 = C::kDqT ? kd : dsd, b0 = C::kDqT ? dsd : kd;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ss<false>(tmem + C::kColS, ads + ((kk * 16 * 128) >> 4), bk + ((kk * 16 * 128) >> 4), C::kIdescdQ,
-                        kk > 0 ? 1u : 0u);
-        tc_commit(&bars.dq_full[0]);
+          mma_ss<false>(tmem + C::kColdQ + qb * 64, a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * 128) >> 4),
+                        C::kIdescdQ, kk > 0 ? 1u : 0u);
+        tc_commit(&bars.dq_full[qb]);
         tc_commit(&bars.q_empty[st]);
         if (last) {
           tc_commit(&bars.dkv_full[0]);
@@ -348,9 +389,12 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, c
   }
 }
 
+// Two warpgroups (cg = 0, 1), each a half of the step's query columns; the
+// bf16 P^T / dS^T of warpgroup cg sit at columns cg*kCols + (query % kCols)/2.
 template <class C>
 __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, const BwdBars& bars,
-                                 const Watchdog& wd) {
+                                 const Watchdog& wd, int cg) {
+  constexpr int kCols = C::BM / 2;  // query columns per warpgroup: 32 or 64
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int r = wq * 32 + lane;  // key row of the tile = tensor-memory lane
@@ -366,53 +410,57 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
     const int key = w.j * C::BN + r;
     const bool key_ok = key < p.N_k;
     for (int s = 0; s < w.n_steps; ++s, ++gs) {
-      const int i = w.i0 + s;
+      const int q0 = (w.i0 + s) * C::BM + cg * kCols;  // first query of this warpgroup's columns
       const uint32_t st = gs % C::NST;
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * C::BM * 4);
-      const float* dlt = lse2 + C::BM;
+      const float* nl2 = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * C::BM * 4) + cg * kCols;
+      const float* dlt = nl2 + C::BM;
       if (!bwd_warp_wait(&bars.s_full[0], gs & 1u, wd, 0x67)) return;
       tc_fence_after();
-      // per-element masking only where needed: the key tail, and the
-      // diagonal tile of a causal unit (query tails have lse2 = +inf)
-      const int q0 = i * C::BM;
-      const bool diag = p.causal && q0 < w.j * C::BN + C::BN;
-      const bool need_mask = __any_sync(0xffffffffu, !key_ok) || diag;
+      // per-element masking only where needed: the key tail and tiles that
+      // reach above the diagonal (query tails have -lse2 = -inf)
+      const bool need_mask = __any_sync(0xffffffffu, !key_ok || (p.causal && key > q0));
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::BM; c0 += 32) {
+      for (int c0 = 0; c0 < kCols; c0 += 32) {
         uint32_t sv[32], dpv[32];
-        tmem_ld32(tS + c0, sv);
-        tmem_ld32(tdP + c0, dpv);
+        tmem_ld32(tS + cg * kCols + c0, sv);
+        tmem_ld32(tdP + cg * kCols + c0, dpv);
         tmem_ld_wait32(sv);
         reg_fence32(dpv);
         uint32_t pw[16], dw[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int c = c0 + k;
-          const float2 l2 = *reinterpret_cast<const float2*>(lse2 + c);
-          const float2 dl = *reinterpret_cast<const float2*>(dlt + c);
-          const float2 x = ffma2(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sc2,
-                                 make_float2(-l2.x, -l2.y));
-          float p0 = ex2(x.x), p1 = ex2(x.y);
-          if (need_mask) {
-            const int q = q0 + c;
-            if (!key_ok || (p.causal && key > q)) p0 = 0.f;
-            if (!key_ok || (p.causal && key > q + 1)) p1 = 0.f;
+        for (int k = 0; k < 32; k += 4) {
+          const float4 l2 = *reinterpret_cast<const float4*>(nl2 + c0 + k);
+          const float4 dl = *reinterpret_cast<const float4*>(dlt + c0 + k);
+#pragma unroll
+          for (int h = 0; h < 4; h += 2) {
+            const int c = c0 + k + h;
+            const float2 x = ffma2(make_float2(__uint_as_float(sv[k + h]), __uint_as_float(sv[k + h + 1])), sc2,
+                                   h ? make_float2(l2.z, l2.w) : make_float2(l2.x, l2.y));
+            float p0 = ex2(x.x), p1 = ex2(x.y);
+            if (need_mask) {
+              if (!key_ok || (p.causal && key > q0 + c)) p0 = 0.f;
+              if (!key_ok || (p.causal && key > q0 + c + 1)) p1 = 0.f;
+            }
+            const float2 g = fadd2(make_float2(__uint_as_float(dpv[k + h]), __uint_as_float(dpv[k + h + 1])),
+                                   h ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y));
+            const float2 ds = fmul2(make_float2(p0, p1), g);
+            pw[(k + h) / 2] = pack_bf16x2(p0, p1);
+            dw[(k + h) / 2] = pack_bf16x2(ds.x, ds.y);
           }
-          const float ds0 = p0 * (__uint_as_float(dpv[k]) - dl.x);
-          const float ds1 = p1 * (__uint_as_float(dpv[k + 1]) - dl.y);
-          pw[k / 2] = pack_bf16x2(p0, p1);
-          dw[k / 2] = pack_bf16x2(ds0, ds1);
         }
-        // P^T and dS^T overwrite S^T and dP^T in place (bf16 pairs: column
-        // c/2 < c, whose fp32 values were read above)
-        tmem_st16(tS + c0 / 2, pw);
-        tmem_st16(tdP + c0 / 2, dw);
-        // dS^T row r, queries c0..c0+31, into the 128-byte-swizzled panel
+        // P^T and dS^T (bf16 pairs) go into the first half of this
+        // warpgroup's own S^T / dP^T columns: column c0/2 + k < c0 + 32, all
+        // read by this thread already (the MMA warp addresses each 16-query
+        // k-step there)
+        tmem_st16(tS + cg * kCols + c0 / 2, pw);
+        tmem_st16(tdP + cg * kCols + c0 / 2, dw);
+        // dS^T row r, queries of this chunk, into the 128-byte-swizzled panel
         // layout (64 queries per panel, 8-row groups of 1024 bytes)
-        uint8_t* panel = ds_row + (c0 / 64) * (C::BN * 128);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const int chunk = ((c0 % 64) / 8 + t) ^ (r & 7);
+          const int qc = cg * kCols + c0 + 8 * t;  // first query (of the step) of the 16-byte chunk
+          uint8_t* panel = ds_row + (qc / 64) * (C::BN * 128);
+          const int chunk = ((qc % 64) / 8) ^ (r & 7);
           *reinterpret_cast<uint4*>(panel + chunk * 16) =
               make_uint4(dw[4 * t], dw[4 * t + 1], dw[4 * t + 2], dw[4 * t + 3]);
         }
@@ -447,21 +495,30 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
         }
       continue;
     }
+    float* acc = p.dq_acc + static_cast<long long>(w.bh) * p.N_qp * C::D;
     for (int s = 0; s < w.n_steps; ++s, ++gs) {
-      const int q = (w.i0 + s) * C::BM + r;
-      float* dst = p.dq_acc + (static_cast<long long>(w.bh) * p.N_qp + q) * C::D;
-      if (!bwd_warp_wait(&bars.dq_full[0], gs & 1u, wd, 0x68)) return;
+      const uint32_t qb = gs & 1u;
+      const int q0 = (w.i0 + s) * C::BM;
+      if (!bwd_warp_wait(&bars.dq_full[qb], (gs >> 1) & 1u, wd, 0x68)) return;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < C::D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::kColS + c, v);
-        tmem_ld_wait32(v);
-#pragma unroll
-        for (int k = 0; k < 32; k += 4) red_add_v4(dst + c + k, v[k], v[k + 1], v[k + 2], v[k + 3]);
-      }
+      uint32_t v[64];
+      tmem_ld32(tmem + lane_base + C::kColdQ + qb * 64, v);
+      tmem_ld32(tmem + lane_base + C::kColdQ + qb * 64 + 32, v + 32);
+      tmem_ld_wait32(v);
+      reg_fence32(v + 32);
       tc_fence_before();
-      mbar_arrive(&bars.dq_empty[0]);
+      mbar_arrive(&bars.dq_empty[qb]);  // the values are in registers now
+      if constexpr (C::kDqT) {
+        // lane r = head-dim index, columns = the step's 64 queries: a warp's
+        // reductions hit 32 consecutive floats of one query row
+#pragma unroll
+        for (int c = 0; c < 64; ++c) red_add_f32(acc + static_cast<long long>(q0 + c) * C::D + r, v[c]);
+      } else {
+        // lane r = query row of the step, columns = the 64 head-dim values
+        float* dst = acc + static_cast<long long>(q0 + r) * C::D;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) red_add_v4(dst + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
+      }
     }
     if (!bwd_warp_wait(&bars.dkv_full[0], ku & 1u, wd, 0x69)) return;
     tc_fence_after();
@@ -496,7 +553,7 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
 }
 
 template <class C>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const __grid_constant__ BwdParams p) {
@@ -508,13 +565,13 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   bars.kv_empty = bar + 1;
   bars.s_full = bar + 2;
   bars.p_full = bar + 3;
-  bars.dq_full = bar + 4;
-  bars.dq_empty = bar + 5;
-  bars.dkv_full = bar + 6;
-  bars.dkv_empty = bar + 7;
-  bars.q_full = bar + 8;
-  bars.q_empty = bar + 8 + C::NST;
-  uint64_t* teardown = bar + 8 + 2 * C::NST;
+  bars.dkv_full = bar + 4;
+  bars.dkv_empty = bar + 5;
+  bars.dq_full = bar + 6;
+  bars.dq_empty = bar + 8;
+  bars.q_full = bar + 10;
+  bars.q_empty = bar + 10 + C::NST;
+  uint64_t* teardown = bar + 10 + 2 * C::NST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int warp = threadIdx.x / 32;
@@ -523,11 +580,13 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&bars.kv_full[0], 1);
     mbar_init(&bars.kv_empty[0], 1);
     mbar_init(&bars.s_full[0], 1);
-    mbar_init(&bars.p_full[0], 128);
-    mbar_init(&bars.dq_full[0], 1);
-    mbar_init(&bars.dq_empty[0], 128);
+    mbar_init(&bars.p_full[0], 256);
     mbar_init(&bars.dkv_full[0], 1);
     mbar_init(&bars.dkv_empty[0], 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.dq_full[b], 1);
+      mbar_init(&bars.dq_empty[b], 128);
+    }
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
@@ -536,13 +595,13 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmdO);
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -551,18 +610,27 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{abort_flag, p.err, p.timeout_ns};
-  if (warp < 4) {
-    bwd_compute_role<C>(p, smem, tmem, bars, wd);
-  } else if (warp < 8) {
+  // register split (setmaxnreg, per warpgroup): the shares must add up to
+  // the 4 x 128 registers per thread the block was launched with
+  constexpr uint32_t kRegCompute = 144, kRegEpilogue = 112, kRegProducer = 112;
+  static_assert(2 * kRegCompute + kRegEpilogue + kRegProducer == 4 * 128, "register split");
+  if (warp < 8) {
+    setmaxnreg_inc<kRegCompute>();
+    bwd_compute_role<C>(p, smem, tmem, bars, wd, warp / 4);
+  } else if (warp < 12) {
+    setmaxnreg_dec<kRegEpilogue>();
     bwd_epilogue_role<C>(p, tmem, bars, wd);
-  } else if (warp == 8) {
-    if (lane == 0) bwd_load_role<C>(&tmQ, &tmK, &tmV, &tmdO, p, smem, bars, wd);
-  } else if (warp == 9) {
-    bwd_mma_role<C>(p, smem, tmem, bars, wd, teardown);
+  } else {
+    setmaxnreg_dec<kRegProducer>();
+    if (warp == 12) {
+      if (lane == 0) bwd_load_role<C>(&tmQ, &tmK, &tmV, &tmdO, p, smem, bars, wd);
+    } else if (warp == 13) {
+      bwd_mma_role<C>(p, smem, tmem, bars, wd, teardown);
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -594,6 +594,13 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   p.n_kt = (int)n_kt;
   p.N_qp = N_qp;
   p.n_units = (int)(B * H * n_kt);
+  {  // heads per schedule group: their fp32 dQ rows, Q and dO within ~48 MB of L2
+    const long long per_head = N_qp * d * 4 + 2 * N_q * d * 2;
+    long long g = (48ll << 20) / (per_head > 0 ? per_head : 1);
+    if (g < 1) g = 1;
+    if (g > B * H) g = B * H;
+    p.head_group = (int)g;
+  }
   p.nlse2 = ws.nlse2;
   p.delta = ws.delta;
   p.dq_acc = ws.dq_acc;

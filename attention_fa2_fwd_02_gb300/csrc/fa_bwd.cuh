@@ -47,6 +47,7 @@ struct BwdParams {
   int n_qt, n_kt;         // query tiles (BM rows) / key tiles (128)
   int N_qp;               // row pitch of the workspace vectors (N_q rounded up to 128)
   int n_units;            // B * H * n_kt
+  int head_group;         // heads per schedule group (their dQ accumulator and Q, dO in L2)
   const float* nlse2;     // workspace: -LSE * log2(e) [B*H][N_qp] (-inf on padding)
   const float* delta;     // workspace: dO . O          [B*H][N_qp] (0 on padding)
   float* dq_acc;          // workspace: fp32 dQ / scale  [B*H][N_qp][D]
@@ -108,8 +109,11 @@ struct BwdBars {
   uint64_t* q_empty;    // [NST]
 };
 
-// Work unit u -> (b*H + h, key tile j).  Causal units are taken in ascending j
-// (the longest first: key tile j is seen by the query tiles from its diagonal on).
+// Work unit u -> (b*H + h, key tile j).  Heads are taken in groups of
+// head_group; inside a group the key tiles go in ascending j with the group's
+// heads interleaved, so that concurrently running CTAs reduce into (and read
+// Q, dO of) a few heads whose data stays in L2, and causal units come longest
+// first (key tile j is seen by the query tiles from its diagonal on).
 struct BwdUnit {
   int bh, b, h, j, i0, n_steps;
 };
@@ -117,13 +121,13 @@ template <class C>
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   BwdUnit w;
   const int BH = p.B * p.H;
-  if (p.causal) {
-    w.j = u / BH;
-    w.bh = u - w.j * BH;
-  } else {
-    w.bh = u / p.n_kt;
-    w.j = u - w.bh * p.n_kt;
-  }
+  const int per_group = p.head_group * p.n_kt;
+  const int g = u / per_group;
+  const int rem = u - g * per_group;
+  const int g0 = g * p.head_group;
+  const int gh = min(p.head_group, BH - g0);  // the last group may be smaller
+  w.j = rem / gh;
+  w.bh = g0 + (rem - w.j * gh);
   w.b = w.bh / p.H;
   w.h = w.bh - w.b * p.H;
   // first query tile holding a row >= the tile's first key

@@ -43,7 +43,7 @@ class FaProblem(ctypes.Structure):
                 ("N_k", ctypes.c_int64), ("d", ctypes.c_int64),
                 ("Q", FaTensor), ("K", FaTensor), ("V", FaTensor), ("O", FaTensor),
                 ("LSE", ctypes.c_void_p), ("lse_stride", ctypes.c_int64 * 3),
-                ("scale", ctypes.c_float), ("is_causal", ctypes.c_int)]
+                ("scale", ctypes.c_float), ("is_causal", ctypes.c_int), ("H_kv", ctypes.c_int64)]
 
 
 class FaError(RuntimeError):
@@ -107,6 +107,13 @@ def lib() -> ctypes.CDLL:
                                                  P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
                                                  ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int,
                                                  ctypes.c_void_p]
+            L.fa_fwd_gqa.restype = ctypes.c_int
+            L.fa_fwd_gqa.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 6 + [P(FaTensor)] * 3 + \
+                [ctypes.c_float, ctypes.c_int, P(FaTensor), ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p]
+            L.fa_bwd_gqa.restype = ctypes.c_int
+            L.fa_bwd_gqa.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 6 + [P(FaTensor)] * 5 +
+                                     [ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_float, ctypes.c_int] +
+                                     [P(FaTensor)] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
             L.fa_bwd.restype = ctypes.c_int
@@ -162,8 +169,9 @@ def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
         raise ValueError("Q, K, V must be on one device")
     q4, k4, v4 = _as4(Q), _as4(K), _as4(V)
     B, H, N_q, d = q4.shape
-    if k4.shape != v4.shape or k4.shape[0] != B or k4.shape[1] != H or k4.shape[3] != d:
-        raise ValueError(f"shape mismatch: Q{tuple(Q.shape)} K{tuple(K.shape)} V{tuple(V.shape)}")
+    if k4.shape != v4.shape or k4.shape[0] != B or k4.shape[3] != d or H % k4.shape[1] != 0:
+        raise ValueError(f"shape mismatch: Q{tuple(Q.shape)} K{tuple(K.shape)} V{tuple(V.shape)} "
+                         "(K/V heads must divide the query heads)")
     N_k = k4.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -176,6 +184,7 @@ def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
         lse = torch.empty(Q.shape[:-1], dtype=torch.float32, device=Q.device)
     pb = FaProblem()
     pb.B, pb.H, pb.N_q, pb.N_k, pb.d = B, H, N_q, N_k, d
+    pb.H_kv = k4.shape[1]
     pb.Q, pb.K, pb.V, pb.O = _ft(q4), _ft(k4), _ft(v4), _ft(o4)
     if lse is not None:
         if lse.dtype != torch.float32 or lse.device != Q.device or lse.shape != Q.shape[:-1]:
@@ -212,11 +221,11 @@ def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None =
     with torch.cuda.device(Q.device):
         lse_stride = (ctypes.c_int64 * 3)(*pb.lse_stride)
         n_split = 1
-        if pb.d in (64, 128):
+        if pb.d in (64, 128) and pb.H_kv == pb.H:  # (split-KV takes K/V with the query heads)
             n_split = (L.fa_fwd_splitkv_choose(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.is_causal)
                        if split_kv is None else int(split_kv))
         if n_split == 1:
-            st = L.fa_fwd(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
+            st = L.fa_fwd_gqa(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
                           ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
                           pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
                           _stream_ptr(Q.device, stream))
@@ -255,6 +264,13 @@ def fwd_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: torch.Te
     L = lib()
     code = _dtype_code(Q)
     with torch.cuda.device(Q.device):
+        if pb.H_kv != pb.H:  # grouped K/V heads: the unsplit kernel, which needs no scratch
+            st = L.fa_fwd_gqa(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
+                              ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                              pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE,
+                              (ctypes.c_int64 * 3)(*pb.lse_stride), _stream_ptr(Q.device, stream))
+            _raise_on(st)
+            return out, lse
         n_split = 1
         if pb.d in (64, 128):
             n_split = (L.fa_fwd_splitkv_choose(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.is_causal)
@@ -285,8 +301,9 @@ def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE:
     B, H, N_q, d = q4.shape
     N_k = k4.shape[2]
     if o4.shape != q4.shape or g4.shape != q4.shape or v4.shape != k4.shape or k4.shape[0] != B or \
-            k4.shape[1] != H or k4.shape[3] != d:
-        raise ValueError("shape mismatch between Q, K, V, O and dO")
+            H % k4.shape[1] != 0 or k4.shape[3] != d:
+        raise ValueError("shape mismatch between Q, K, V, O and dO (K/V heads must divide the query heads)")
+    H_kv = k4.shape[1]
     if LSE.dtype != torch.float32 or LSE.shape != Q.shape[:-1]:
         raise ValueError("LSE must be fp32 with Q's leading shape")
     if scale is None:
@@ -307,7 +324,7 @@ def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE:
     while l3.dim() < 3:
         l3 = l3.unsqueeze(0)
     with torch.cuda.device(Q.device):
-        st = L.fa_bwd(_dtype_code(Q), B, H, N_q, N_k, d,
+        st = L.fa_bwd_gqa(_dtype_code(Q), B, H, H_kv, N_q, N_k, d,
                       ctypes.byref(_ft(q4)), ctypes.byref(_ft(k4)), ctypes.byref(_ft(v4)), ctypes.byref(_ft(o4)),
                       ctypes.byref(_ft(g4)), ctypes.c_void_p(l3.data_ptr()), (ctypes.c_int64 * 3)(*l3.stride()),
                       float(scale), 1 if is_causal else 0,

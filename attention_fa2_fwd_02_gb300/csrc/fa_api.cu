@@ -102,6 +102,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 enum class Path { kTensorCore, kSmall };
 
 bool tensor_ok(const fa_tensor_t& t) { return t.ptr != nullptr && t.stride[3] == 1; }
+long long kv_heads(const fa_problem_t& pb) { return pb.H_kv > 0 ? pb.H_kv : pb.H; }
 
 // Validate one problem and choose its kernel.
 fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* path) {
@@ -112,6 +113,8 @@ fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* pa
   if (!tensor_ok(pb.Q) || !tensor_ok(pb.K) || !tensor_ok(pb.V) || !tensor_ok(pb.O))
     return fail(FA_ERR_INVALID_ARG, at + "Q, K, V, O need a non-null pointer and stride[3] == 1");
   if (!std::isfinite(pb.scale)) return fail(FA_ERR_INVALID_ARG, at + "scale must be finite");
+  if (pb.H_kv < 0 || (pb.H_kv > 0 && pb.H % pb.H_kv != 0))
+    return fail(FA_ERR_INVALID_ARG, at + "H_kv must divide H (0 = H)");
   if (pb.is_causal != 0 && pb.is_causal != 1) return fail(FA_ERR_INVALID_ARG, at + "is_causal must be 0 or 1");
   if (pb.LSE && (pb.lse_stride[0] < 0 || pb.lse_stride[1] < 0 || pb.lse_stride[2] < 0))
     return fail(FA_ERR_UNSUPPORTED, at + "negative LSE strides are not supported");
@@ -191,8 +194,8 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   TcLaunch L;
   fa_status_t st;
   if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, d, 128, "Q")) != FA_OK) return st;
-  if ((st = make_map(&L.tmK, pb.K, fp32, pb.B, pb.H, pb.N_k, d, bn, "K")) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, pb.H, pb.N_k, d, bn, "V")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, pb.K, fp32, pb.B, kv_heads(pb), pb.N_k, d, bn, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, kv_heads(pb), pb.N_k, d, bn, "V")) != FA_OK) return st;
   TcParams& p = L.p;
   p.B = (int)pb.B;
   p.H = (int)pb.H;
@@ -212,6 +215,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   if (g < 1) g = 1;
   if (g > pb.B * pb.H) g = pb.B * pb.H;
   p.head_group = (int)g;
+  p.kv_group = (int)(pb.H / kv_heads(pb));
   p.O = pb.O.ptr;
   for (int i = 0; i < 3; ++i) {
     p.o_stride[i] = pb.O.stride[i];
@@ -349,6 +353,7 @@ fa_status_t launch_small(fa_dtype_t dtype, int d, const std::vector<const fa_pro
     }
     s.B = (int)pb.B;
     s.H = (int)pb.H;
+    s.kv_group = (int)(pb.H / kv_heads(pb));
     s.N_q = (int)pb.N_q;
     s.N_k = (int)pb.N_k;
     s.causal = pb.is_causal;
@@ -449,11 +454,19 @@ extern "C" {
 fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
                    const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale, int is_causal,
                    const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* stream) {
+  return fa_fwd_gqa(dtype, B, H, H, N_q, N_k, d, Q, K, V, scale, is_causal, O, LSE, lse_stride, stream);
+}
+
+fa_status_t fa_fwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                       const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale, int is_causal,
+                       const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* stream) {
   if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
   if (LSE && !lse_stride) return fail(FA_ERR_INVALID_ARG, "lse_stride must not be NULL when LSE is given");
+  if (H_kv <= 0) return fail(FA_ERR_INVALID_ARG, "problem 0: H_kv must divide H");
   fa_problem_t pb{};
   pb.B = B;
   pb.H = H;
+  pb.H_kv = H_kv;
   pb.N_q = N_q;
   pb.N_k = N_k;
   pb.d = d;
@@ -538,7 +551,17 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
                    const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale, int is_causal,
                    const fa_tensor_t* dQ, const fa_tensor_t* dK, const fa_tensor_t* dV, void* workspace,
                    size_t workspace_bytes, void* stream) {
+  return fa_bwd_gqa(dtype, B, H, H, N_q, N_k, d, Q, K, V, O, dO, LSE, lse_stride, scale, is_causal, dQ, dK, dV,
+                    workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                       const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, const fa_tensor_t* O,
+                       const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale,
+                       int is_causal, const fa_tensor_t* dQ, const fa_tensor_t* dK, const fa_tensor_t* dV,
+                       void* workspace, size_t workspace_bytes, void* stream) {
   if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
+  if (H_kv <= 0) return fail(FA_ERR_INVALID_ARG, "H_kv must divide H");
   if (!LSE || !lse_stride) return fail(FA_ERR_INVALID_ARG, "the backward needs the forward's LSE and its strides");
   fa_problem_t pb{};
   pb.B = B;
@@ -554,6 +577,7 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   for (int i = 0; i < 3; ++i) pb.lse_stride[i] = lse_stride[i];
   pb.scale = scale;
   pb.is_causal = is_causal;
+  pb.H_kv = H_kv;
   Path path;
   fa_status_t st = validate(dtype, pb, 0, &path);
   if (st != FA_OK) return st;
@@ -564,7 +588,7 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
     return st;
   const long long bm = d == 128 ? 64 : 128;  // query rows per step of the backward kernel
   const long long n_kt = (N_k + 127) / 128, n_qt = (N_q + bm - 1) / bm;
-  if (B * H * n_kt >= (1ll << 31) || B * H * n_qt * 128 >= (1ll << 40))
+  if (B * H_kv * n_kt >= (1ll << 31) || B * H * n_qt * 128 >= (1ll << 40) || (H / H_kv) * n_qt >= (1ll << 31))
     return fail(FA_ERR_UNSUPPORTED, "too many backward work units");
   if (!workspace) return fail(FA_ERR_INVALID_ARG, "the backward needs a workspace");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
@@ -579,8 +603,8 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   BwdLaunch L{};
   if ((st = make_map(&L.tmQ, *Q, false, B, H, N_q, (int)d, (int)bm, "Q")) != FA_OK) return st;
   if ((st = make_map(&L.tmdO, *dO, false, B, H, N_q, (int)d, (int)bm, "dO")) != FA_OK) return st;
-  if ((st = make_map(&L.tmK, *K, false, B, H, N_k, (int)d, 128, "K")) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, *V, false, B, H, N_k, (int)d, 128, "V")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, *K, false, B, H_kv, N_k, (int)d, 128, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, *V, false, B, H_kv, N_k, (int)d, 128, "V")) != FA_OK) return st;
   const int N_qp = (int)((N_q + 127) / 128 * 128);  // workspace row pitch
   BwdParams& p = L.p;
   p.B = (int)B;
@@ -593,12 +617,14 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
   p.n_qt = (int)n_qt;
   p.n_kt = (int)n_kt;
   p.N_qp = N_qp;
-  p.n_units = (int)(B * H * n_kt);
-  {  // heads per schedule group: their fp32 dQ rows, Q and dO within ~48 MB of L2
-    const long long per_head = N_qp * d * 4 + 2 * N_q * d * 2;
+  p.H_kv = (int)H_kv;
+  p.kv_group = (int)(H / H_kv);
+  p.n_units = (int)(B * H_kv * n_kt);
+  {  // K/V heads per schedule group: their query heads' fp32 dQ rows, Q and dO within ~48 MB of L2
+    const long long per_head = (N_qp * d * 4 + 2 * N_q * d * 2) * (H / H_kv);
     long long g = (48ll << 20) / (per_head > 0 ? per_head : 1);
     if (g < 1) g = 1;
-    if (g > B * H) g = B * H;
+    if (g > B * H_kv) g = B * H_kv;
     p.head_group = (int)g;
   }
   p.nlse2 = ws.nlse2;
@@ -684,6 +710,6 @@ void fa_debug_set(uint64_t timeout_ns, int debug_flags) {
   g_debug_flags.store(debug_flags);
 }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 }  // extern "C"

@@ -41,13 +41,14 @@ namespace fa {
 
 struct BwdParams {
   int B, H, N_q, N_k;
+  int H_kv, kv_group;     // K/V heads, query heads per K/V head (grouped-query attention)
   int causal;
   float scale;            // softmax scale
   float scale_log2;       // scale * log2(e)
   int n_qt, n_kt;         // query tiles (BM rows) / key tiles (128)
   int N_qp;               // row pitch of the workspace vectors (N_q rounded up to 128)
-  int n_units;            // B * H * n_kt
-  int head_group;         // heads per schedule group (their dQ accumulator and Q, dO in L2)
+  int n_units;            // B * H_kv * n_kt
+  int head_group;         // K/V heads per schedule group (their dQ accumulator and Q, dO in L2)
   const float* nlse2;     // workspace: -LSE * log2(e) [B*H][N_qp] (-inf on padding)
   const float* delta;     // workspace: dO . O          [B*H][N_qp] (0 on padding)
   float* dq_acc;          // workspace: fp32 dQ / scale  [B*H][N_qp][D]
@@ -109,31 +110,47 @@ struct BwdBars {
   uint64_t* q_empty;    // [NST]
 };
 
-// Work unit u -> (b*H + h, key tile j).  Heads are taken in groups of
+// Work unit u -> (b*H_kv + hk, key tile j).  K/V heads are taken in groups of
 // head_group; inside a group the key tiles go in ascending j with the group's
 // heads interleaved, so that concurrently running CTAs reduce into (and read
 // Q, dO of) a few heads whose data stays in L2, and causal units come longest
-// first (key tile j is seen by the query tiles from its diagonal on).
+// first (key tile j is seen by the query tiles from its diagonal on).  A unit
+// walks, for each of the kv_group query heads that read K/V head hk, the
+// query tiles i0 .. n_qt-1: step s is query head hk*kv_group + s / n_q, tile
+// i0 + s % n_q.
 struct BwdUnit {
-  int bh, b, h, j, i0, n_steps;
+  int b, hk, j, i0, n_q, n_steps;
+};
+struct BwdStep {
+  int h, i;
+  long long bh;  // b * H + h: the query head's rows of the workspace
 };
 template <class C>
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   BwdUnit w;
-  const int BH = p.B * p.H;
+  const int BHk = p.B * p.H_kv;
   const int per_group = p.head_group * p.n_kt;
   const int g = u / per_group;
   const int rem = u - g * per_group;
   const int g0 = g * p.head_group;
-  const int gh = min(p.head_group, BH - g0);  // the last group may be smaller
+  const int gh = min(p.head_group, BHk - g0);  // the last group may be smaller
   w.j = rem / gh;
-  w.bh = g0 + (rem - w.j * gh);
-  w.b = w.bh / p.H;
-  w.h = w.bh - w.b * p.H;
+  const int bhk = g0 + (rem - w.j * gh);
+  w.b = bhk / p.H_kv;
+  w.hk = bhk - w.b * p.H_kv;
   // first query tile holding a row >= the tile's first key
   w.i0 = p.causal ? (w.j * C::BN) / C::BM : 0;
-  w.n_steps = w.i0 < p.n_qt ? p.n_qt - w.i0 : 0;
+  w.n_q = w.i0 < p.n_qt ? p.n_qt - w.i0 : 0;
+  w.n_steps = w.n_q * p.kv_group;
   return w;
+}
+__device__ __forceinline__ BwdStep bwd_step(const BwdParams& p, const BwdUnit& w, int s) {
+  BwdStep t;
+  const int g = s / w.n_q;
+  t.i = w.i0 + (s - g * w.n_q);
+  t.h = w.hk * p.kv_group + g;
+  t.bh = static_cast<long long>(w.b) * p.H + t.h;
+  return t;
 }
 
 // 1-D bulk copy global -> shared, completing on `bar` (16-byte aligned, size
@@ -257,26 +274,27 @@ __device__ void bwd_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, co
     mbar_arrive_expect_tx(&bars.kv_full[0], C::kKVBytes);
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn) {
-      tma_load_4d(tmK, &bars.kv_full[0], smem + C::kOffK + pn * C::kKVPanelBytes, pn * 64, w.j * C::BN, w.h, w.b,
+      tma_load_4d(tmK, &bars.kv_full[0], smem + C::kOffK + pn * C::kKVPanelBytes, pn * 64, w.j * C::BN, w.hk, w.b,
                   pol_kv);
-      tma_load_4d(tmV, &bars.kv_full[0], smem + C::kOffV + pn * C::kKVPanelBytes, pn * 64, w.j * C::BN, w.h, w.b,
+      tma_load_4d(tmV, &bars.kv_full[0], smem + C::kOffV + pn * C::kKVPanelBytes, pn * 64, w.j * C::BN, w.hk, w.b,
                   pol_kv);
     }
     ++kv_armed;
     ++ku;
     for (int s = 0; ok && s < w.n_steps; ++s, ++gs) {
-      const int i = w.i0 + s;
+      const BwdStep t = bwd_step(p, w, s);
+      const int i = t.i;
       const uint32_t st = gs % C::NST;
       if (!(ok = mbar_wait(&bars.q_empty[st], ((gs / C::NST) & 1u) ^ 1u, wd, 0x61))) break;
       mbar_arrive_expect_tx(&bars.q_full[st], C::kStepBytes);
 #pragma unroll
       for (int pn = 0; pn < C::kPanels; ++pn) {
         tma_load_4d(tmQ, &bars.q_full[st], smem + C::kOffQ + st * C::kQTileBytes + pn * C::kQPanelBytes, pn * 64,
-                    i * C::BM, w.h, w.b, pol_q);
+                    i * C::BM, t.h, w.b, pol_q);
         tma_load_4d(tmdO, &bars.q_full[st], smem + C::kOffdO + st * C::kQTileBytes + pn * C::kQPanelBytes,
-                    pn * 64, i * C::BM, w.h, w.b, pol_q);
+                    pn * 64, i * C::BM, t.h, w.b, pol_q);
       }
-      const long long vrow = static_cast<long long>(w.bh) * p.N_qp + i * C::BM;
+      const long long vrow = t.bh * p.N_qp + i * C::BM;
       uint8_t* vec = smem + C::kOffVec + st * 2 * C::BM * 4;
       bulk_load(vec, p.nlse2 + vrow, C::BM * 4, &bars.q_full[st]);
       bulk_load(vec + C::BM * 4, p.delta + vrow, C::BM * 4, &bars.q_full[st]);
@@ -414,7 +432,7 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
     const int key = w.j * C::BN + r;
     const bool key_ok = key < p.N_k;
     for (int s = 0; s < w.n_steps; ++s, ++gs) {
-      const int q0 = (w.i0 + s) * C::BM + cg * kCols;  // first query of this warpgroup's columns
+      const int q0 = bwd_step(p, w, s).i * C::BM + cg * kCols;  // first query of this warpgroup's columns
       const uint32_t st = gs % C::NST;
       const float* nl2 = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * C::BM * 4) + cg * kCols;
       const float* dlt = nl2 + C::BM;
@@ -488,9 +506,9 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
     const BwdUnit w = bwd_unit<C>(p, u);
     const int key = w.j * C::BN + r;
     __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dK) + w.b * p.dk_stride[0] +
-                            w.h * p.dk_stride[1] + static_cast<long long>(key) * p.dk_stride[2];
+                            w.hk * p.dk_stride[1] + static_cast<long long>(key) * p.dk_stride[2];
     __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dV) + w.b * p.dv_stride[0] +
-                            w.h * p.dv_stride[1] + static_cast<long long>(key) * p.dv_stride[2];
+                            w.hk * p.dv_stride[1] + static_cast<long long>(key) * p.dv_stride[2];
     if (w.n_steps == 0) {  // keys no query sees: zero gradients
       if (key < p.N_k)
         for (int c = 0; c < C::D; c += 8) {
@@ -499,10 +517,11 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
         }
       continue;
     }
-    float* acc = p.dq_acc + static_cast<long long>(w.bh) * p.N_qp * C::D;
     for (int s = 0; s < w.n_steps; ++s, ++gs) {
+      const BwdStep t = bwd_step(p, w, s);
+      float* acc = p.dq_acc + t.bh * p.N_qp * C::D;
       const uint32_t qb = gs & 1u;
-      const int q0 = (w.i0 + s) * C::BM;
+      const int q0 = t.i * C::BM;
       if (!bwd_warp_wait(&bars.dq_full[qb], (gs >> 1) & 1u, wd, 0x68)) return;
       tc_fence_after();
       uint32_t v[64];

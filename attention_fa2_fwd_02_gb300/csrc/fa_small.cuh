@@ -34,6 +34,7 @@ struct SmallProblem {
   float* LSE;
   long long qs[3], ks[3], vs[3], os[3], ls[3];  // element strides b, h, n
   int B, H, N_q, N_k;
+  int kv_group;        // query heads per K/V head (grouped-query attention; 1 = none)
   int causal;
   float scale_log2;
   int n_qblk;          // ceil(N_q / 32)
@@ -120,8 +121,9 @@ fa_small_fwd_kernel(const __grid_constant__ SmallParams P) {
   const bool vec = pr.vec_ok != 0;
 
   const T* Qb = reinterpret_cast<const T*>(pr.Q) + b * pr.qs[0] + h * pr.qs[1];
-  const T* Kb = reinterpret_cast<const T*>(pr.K) + b * pr.ks[0] + h * pr.ks[1];
-  const T* Vb = reinterpret_cast<const T*>(pr.V) + b * pr.vs[0] + h * pr.vs[1];
+  const int hk = h / pr.kv_group;  // the K/V head of query head h
+  const T* Kb = reinterpret_cast<const T*>(pr.K) + b * pr.ks[0] + hk * pr.ks[1];
+  const T* Vb = reinterpret_cast<const T*>(pr.V) + b * pr.vs[0] + hk * pr.vs[1];
 
   stage_rows<T, D>(sQ, Qb, pr.qs[2], r0, pr.N_q, vec, lane);
   __syncwarp();

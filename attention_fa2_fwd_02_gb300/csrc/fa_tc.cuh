@@ -45,6 +45,7 @@ struct TcParams {
   float* ws_o;            // split-KV partial outputs, fp32 [n_split][B*H*N_q][D]
   float* ws_lse;          // split-KV partial LSE (natural log), [n_split][B*H*N_q]
   int head_group;         // heads per schedule group (K/V L2 locality)
+  int kv_group;           // query heads per K/V head (grouped-query attention; 1 = none)
   void* O;
   long long o_stride[3];  // elements: b, h, n
   float* LSE;
@@ -132,7 +133,7 @@ struct Bars {
 };
 
 struct TileInfo {
-  int b, h, q0;
+  int b, h, hk, q0;      // hk: the K/V head of query head h
   int split;   // key-range split of this work unit
   int j0;      // first key tile of the unit
   int n_kv;    // key tiles of the unit (0: nothing to do)
@@ -160,6 +161,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   TileInfo ti;
   ti.b = bh / p.H;
   ti.h = bh - ti.b * p.H;
+  ti.hk = ti.h / p.kv_group;
   ti.q0 = qb * 256;
   ti.split = split;
   int kv_end = p.N_k;
@@ -224,7 +226,7 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(map, &bars.kv_full[slot], dst + pn * C::kKVPanelBytes, pn * C::kPanelElems,
-                  (ti.j0 + j) * C::BN, ti.h, ti.b, pol_kv);
+                  (ti.j0 + j) * C::BN, ti.hk, ti.b, pol_kv);
     return true;
   };
 

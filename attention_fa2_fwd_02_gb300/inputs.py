@@ -47,6 +47,11 @@ class Workload:
     causal: bool
     scale: float
     seed: int
+    H_kv: int = 0  # K/V heads (grouped-query attention); 0 = H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def flops(self) -> float:
@@ -63,19 +68,19 @@ class Workload:
         """Q, K, V read once; O written once (input dtype); LSE written (fp32)."""
         e = self.elem_bytes
         q = self.B * self.H * self.N_q * self.d * e
-        kv = 2 * self.B * self.H * self.N_k * self.d * e
+        kv = 2 * self.B * self.kv_heads * self.N_k * self.d * e
         o = q
         lse = self.B * self.H * self.N_q * 4
         return float(q + kv + o + lse)
 
     def make(self):
         return qkv((self.B, self.H, self.N_q, self.d),
-                   (self.B, self.H, self.N_k, self.d), self.seed, self.dtype)
+                   (self.B, self.kv_heads, self.N_k, self.d), self.seed, self.dtype)
 
 
-def _w(name, B, H, Nq, Nk, d, dtype, causal, scale=None, seed=0):
+def _w(name, B, H, Nq, Nk, d, dtype, causal, scale=None, seed=0, H_kv=0):
     return Workload(name, B, H, Nq, Nk, d, dtype, causal,
-                    1.0 / math.sqrt(d) if scale is None else scale, seed)
+                    1.0 / math.sqrt(d) if scale is None else scale, seed, H_kv)
 
 
 # The five configurations (non-causal and causal variants where both are run).
@@ -88,6 +93,9 @@ WORKLOADS = {
     "large_causal": _w("large_causal", 4, 32, 8192, 8192, 128, torch.bfloat16, True, seed=4),
     "cross_long_nc": _w("cross_long_nc", 2, 16, 4096, 32768, 64, torch.bfloat16, False, seed=5),
     "long_causal": _w("long_causal", 1, 16, 32768, 32768, 128, torch.bfloat16, True, seed=6),
+    # grouped-query attention: the large self-attention shape with 8 K/V heads
+    "large_gqa_nc": _w("large_gqa_nc", 4, 32, 8192, 8192, 128, torch.bfloat16, False, seed=9, H_kv=8),
+    "large_gqa_causal": _w("large_gqa_causal", 4, 32, 8192, 8192, 128, torch.bfloat16, True, seed=9, H_kv=8),
     # profiling-size cases of the same kernels: inputs still larger than the
     # 129 MB L2, but small enough for a many-pass ncu capture
     "prof_nc": _w("prof_nc", 1, 32, 8192, 8192, 128, torch.bfloat16, False, seed=7),

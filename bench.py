@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="large_nc")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--api", choices=["fa", "sdpa"], default="fa",
+                    help="forward through fa.fwd (default) or through torch.nn.functional."
+                         "scaled_dot_product_attention routed to this library")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -200,9 +203,10 @@ def workload_desc(w) -> dict:
                 "shape": list(w.shape), "scale": w.scale, "causal": False}
     kind = "causal" if w.causal else "non-causal"
     dt = "bf16" if w.dtype == torch.bfloat16 else "fp32"
-    return {"workload": f"{w.name}: B={w.B} H={w.H} N_q={w.N_q} N_k={w.N_k} d={w.d} {dt} {kind}, "
+    gqa = f" H_kv={w.kv_heads}" if w.kv_heads != w.H else ""
+    return {"workload": f"{w.name}: B={w.B} H={w.H}{gqa} N_q={w.N_q} N_k={w.N_k} d={w.d} {dt} {kind}, "
                         f"scale={w.scale:.6g}",
-            "B": w.B, "H": w.H, "N_q": w.N_q, "N_k": w.N_k, "d": w.d, "dtype": dt,
+            "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N_q": w.N_q, "N_k": w.N_k, "d": w.d, "dtype": dt,
             "causal": w.causal, "scale": w.scale}
 
 
@@ -241,7 +245,8 @@ def bwd_oracle_sample(w, Q, K, V, G, budget_s: float):
         b, h = int(g.integers(w.B)), int(g.integers(w.H))
         nq, nk = min(n, w.N_q), min(n, w.N_k)
         t1 = time.perf_counter()
-        oracle.attention_bwd(Q[b, h, :nq], K[b, h, :nk], V[b, h, :nk], G[b, h, :nq], w.scale, w.causal)
+        hk = h // (w.H // w.kv_heads)
+        oracle.attention_bwd(Q[b, h, :nq], K[b, hk, :nk], V[b, hk, :nk], G[b, h, :nq], w.scale, w.causal)
         one = time.perf_counter() - t1
         flops += 10.0 * nq * nk * w.d * (0.5 if w.causal else 1.0)
         calls += 1
@@ -286,7 +291,8 @@ def oracle_sample(w, Q, K, V, budget_s: float, rows_per_call: int = 512):
         b, h = int(g.integers(w.B)), int(g.integers(w.H))
         r0 = int(g.integers(0, max(1, w.N_q - rows_per_call + 1)))
         rows = np.arange(r0, min(w.N_q, r0 + rows_per_call))
-        oracle.attention(Q[b, h], K[b, h], V[b, h], w.scale, w.causal, rows=rows)
+        hk = h // (w.H // w.kv_heads)  # the K/V head of query head h
+        oracle.attention(Q[b, h], K[b, hk], V[b, hk], w.scale, w.causal, rows=rows)
         nvis = np.minimum(rows + 1, w.N_k) if w.causal else np.full(rows.size, w.N_k)
         flops += float(4.0 * w.d * nvis.sum())
         n_rows += rows.size
@@ -346,7 +352,8 @@ def run_reference(args, w):
         sample_desc = f"{rows} query rows of one random (b,h) slice per step"
         def step():
             b, h = int(g.integers(w.B)), int(g.integers(w.H))
-            oracle.attention(Q[b, h], K[b, h], V[b, h], w.scale, w.causal, rows=np.arange(rows))
+            hk = h // (w.H // w.kv_heads)
+            oracle.attention(Q[b, h], K[b, hk], V[b, hk], w.scale, w.causal, rows=np.arange(rows))
         nvis = np.minimum(np.arange(rows) + 1, w.N_k) if w.causal else np.full(rows, w.N_k)
         step_flops = float(4.0 * w.d * nvis.sum())
     for _ in range(warm):
@@ -419,7 +426,7 @@ def main():
         Od = torch.empty_like(Qd)
         Ld = torch.empty(Qd.shape[:-1], dtype=torch.float32, device=dev)
         code = fa.FA_BF16 if w.dtype == torch.bfloat16 else fa.FA_FP32
-        if w.d in (64, 128):
+        if w.d in (64, 128) and w.kv_heads == w.H:  # (split-KV takes K/V with the query heads)
             n_split = fa.lib().fa_fwd_splitkv_choose(code, w.B, w.H, w.N_q, w.N_k, w.d, int(w.causal))
         ws = None
         if n_split > 1:  # the split path's scratch, allocated once outside the timed region
@@ -429,6 +436,17 @@ def main():
         def step():
             return fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, out=Od, lse=Ld,
                           split_kv=n_split, workspace=ws)
+
+        if args.api == "sdpa":  # the same forward, reached through PyTorch's SDPA entry point
+            import torch.nn.functional as F
+            from attention_fa2_fwd_02_gb300 import sdpa
+            n_split = fa.lib().fa_fwd_splitkv_choose(code, w.B, w.H, w.N_q, w.N_k, w.d, int(w.causal)) \
+                if (w.d in (64, 128) and w.kv_heads == w.H) else 1
+
+            def step():
+                with sdpa.routed():
+                    return F.scaled_dot_product_attention(Qd, Kd, Vd, is_causal=w.causal, scale=w.scale,
+                                                          enable_gqa=w.kv_heads != w.H)
 
     for _ in range(warm):
         if flush is not None:
@@ -565,6 +583,8 @@ def main():
                 Op2.copy_(o2, non_blocking=True)
                 Lp.copy_(l1, non_blocking=True)
                 Lp2.copy_(l2, non_blocking=True)
+            elif args.api == "sdpa":  # the routed SDPA returns O only
+                Op.copy_(step(), non_blocking=True)
             else:
                 step()
                 Op.copy_(Od, non_blocking=True)
@@ -585,7 +605,7 @@ def main():
         torch.cuda.synchronize(dev)
         e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, dist)
         h2d = in_bytes
-        d2h = Op.numel() * Op.element_size() + Lp.numel() * 4
+        d2h = Op.numel() * Op.element_size() + (0 if args.api == "sdpa" else Lp.numel() * 4)
         if axial:
             d2h *= 2
         e2e = {"value": whole_job_value(flops, world, e_ms), "unit": "TFLOP/s",
@@ -610,6 +630,8 @@ def main():
         cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
         cfg["cuda_graph"] = use_graph
         cfg["split_kv"] = n_split
+        if args.api == "sdpa":
+            cfg["api"] = "torch.nn.functional.scaled_dot_product_attention routed to this library"
         if bwd:
             cfg["pass"] = "backward (dQ, dK, dV from Q, K, V, O, LSE, dO); FLOPs = 2.5x the forward's"
         line = {

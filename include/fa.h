@@ -91,7 +91,18 @@ fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
                    const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
                    void* stream);
 
-/* One problem of a grouped call: the arguments of fa_fwd, by value. */
+/*
+ * fa_fwd_gqa -- fa_fwd with grouped K/V heads (grouped-query attention): K and
+ * V are [B, H_kv, N_k, d] and query head h attends to K/V head h / (H / H_kv).
+ * H_kv must divide H (FA_ERR_INVALID_ARG otherwise); H_kv = H is fa_fwd.
+ * Other arguments and rules as fa_fwd.
+ */
+fa_status_t fa_fwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k,
+                       int64_t d, const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                       int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* stream);
+
+/* One problem of a grouped call: the arguments of fa_fwd_gqa, by value.
+ * H_kv = 0 means H_kv = H (K and V have the query heads). */
 typedef struct {
   int64_t B, H, N_q, N_k, d;
   fa_tensor_t Q, K, V, O;
@@ -99,6 +110,7 @@ typedef struct {
   int64_t lse_stride[3];
   float scale;
   int is_causal;
+  int64_t H_kv;
 } fa_problem_t;
 
 /*
@@ -218,6 +230,19 @@ fa_status_t fa_fwd_splitkv_noalloc(fa_dtype_t dtype, int64_t B, int64_t H, int64
  * the host before any launch.
  */
 size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d);
+
+/*
+ * fa_bwd_gqa -- fa_bwd with grouped K/V heads: K, V, dK and dV are
+ * [B, H_kv, N_k, d], H_kv divides H, and dK, dV of a K/V head sum the
+ * gradients of the H / H_kv query heads that read it.  The workspace size is
+ * fa_bwd_workspace_bytes(B, H, N_q, d) (query heads).  Other arguments as
+ * fa_bwd.
+ */
+fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                       const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, const fa_tensor_t* O,
+                       const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale,
+                       int is_causal, const fa_tensor_t* dQ, const fa_tensor_t* dK, const fa_tensor_t* dV,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
                    const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, const fa_tensor_t* O,

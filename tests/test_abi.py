@@ -47,7 +47,7 @@ def test_library_is_built_for_sm103a():
 def test_status_strings(L):
     assert L.fa_status_string(0) == b"ok"
     assert L.fa_status_string(4) == b"device wait timed out"
-    assert L.fa_version() == 100
+    assert L.fa_version() == 101
 
 
 def _t(ptr, strides):
@@ -178,3 +178,15 @@ def test_bwd_workspace_size(L):
     want = ((rows * 64 * 4 + 255) // 256) * 256 + 2 * (((rows * 4) + 255) // 256) * 256
     assert L.fa_bwd_workspace_bytes(2, 3, 200, 64) == want
     assert L.fa_bwd_workspace_bytes(0, 3, 200, 64) == 0
+
+
+def test_gqa_heads_must_divide(L):
+    s = (256 * 64, 256 * 64, 64, 1)
+    t = [_t(a, s) for a in (0x10000, 0x20000, 0x30000, 0x40000)]
+    ls = (ctypes.c_int64 * 3)(256, 256, 1)
+    st = L.fa_fwd_gqa(fa.FA_BF16, 1, 6, 4, 256, 256, 64, ctypes.byref(t[0]), ctypes.byref(t[1]),
+                      ctypes.byref(t[2]), 0.1, 0, ctypes.byref(t[3]), None, ls, None)
+    assert st == fa.FA_ERR_INVALID_ARG and b"H_kv" in L.fa_last_error()
+    st = L.fa_fwd_gqa(fa.FA_BF16, 1, 6, 0, 256, 256, 64, ctypes.byref(t[0]), ctypes.byref(t[1]),
+                      ctypes.byref(t[2]), 0.1, 0, ctypes.byref(t[3]), None, ls, None)
+    assert st == fa.FA_ERR_INVALID_ARG

@@ -14,7 +14,9 @@ flash_attention_reference; "Blackwell Attention Example", kernel docstring):
 
 * O = softmax(scale * Q K^T) V per (batch, head) slice, SDPA layout [..., N, d];
 * LSE = log sum_j exp(s_ij), natural log of the scaled scores;
-* causal: key j visible to query row i iff j <= i (top-left alignment);
+* causal: key j visible to query row i iff j <= i (top-left alignment,
+  is_causal = True or 1); bottom-right alignment (is_causal = 2): j <= i +
+  N_k - N_q, a row that sees no key has O = 0 and LSE = -inf;
 * backward ("Blackwell Attention Example", section "Backward Kernel
   Implementation"): the gradients of sum(dO * O) with respect to Q, K and V,
   with delta_i = dO_i . O_i and dS = P (dP - delta).
@@ -98,6 +100,15 @@ def _as_f32(x) -> np.ndarray:
     return x
 
 
+def _causal_code(is_causal) -> int:
+    """False/0 none, True/1 top-left, 2 or "bottom_right" bottom-right."""
+    if is_causal == "bottom_right":
+        return 2
+    if is_causal in (2,) and not isinstance(is_causal, bool):
+        return 2
+    return 1 if is_causal else 0
+
+
 def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
     """fp64 attention of every (batch..., head) slice.
 
@@ -128,7 +139,7 @@ def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
     for s in range(Qs.shape[0]):
         rc = lib.oracle_attention_slice(
             Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d,
-            N_q, N_k, d, float(scale), int(bool(is_causal)),
+            N_q, N_k, d, float(scale), _causal_code(is_causal),
             rows_ptr, n_rows, O[s].ctypes.data, L[s].ctypes.data)
         if rc != 0:
             raise RuntimeError(f"oracle_attention_slice failed with {rc}")
@@ -168,7 +179,7 @@ def attention_bwd(Q, K, V, dO, scale: float, is_causal: bool = False, q_rows=Non
     for s in range(Qs.shape[0]):
         rc = lib.oracle_attention_bwd_slice(
             Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d, Gs[s].ctypes.data, d,
-            N_q, N_k, d, float(scale), int(bool(is_causal)),
+            N_q, N_k, d, float(scale), _causal_code(is_causal),
             None if qr is None else qr.ctypes.data, nq, None if kr is None else kr.ctypes.data, nk,
             dQ[s].ctypes.data, dK[s].ctypes.data, dV[s].ctypes.data)
         if rc != 0:

@@ -42,6 +42,22 @@
 #include <omp.h>
 #endif
 
+/*
+ * Visible keys of query row i: all N_k keys; with is_causal = 1 (top-left
+ * alignment) keys j <= i; with is_causal = 2 (bottom-right alignment, the
+ * last query row sees the last key) keys j <= i + N_k - N_q.  The result is a
+ * prefix 0 .. n_vis-1 of the keys, possibly empty (bottom-right with
+ * N_q > N_k): a row that sees no key has O = 0 and LSE = -inf (an empty sum).
+ */
+static int64_t visible_keys(int64_t i, int64_t N_q, int64_t N_k, int is_causal) {
+  int64_t n = N_k;
+  if (is_causal == 1) n = i + 1;
+  if (is_causal == 2) n = i + 1 + N_k - N_q;
+  if (n > N_k) n = N_k;
+  if (n < 0) n = 0;
+  return n;
+}
+
 /* Number of threads the parallel loop below uses (1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
@@ -66,7 +82,8 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
                            double scale, int is_causal,
                            const int64_t* rows, int64_t n_rows,
                            double* O, double* LSE) {
-  if (!Q || !K || !V || !O || !LSE || N_q < 0 || N_k <= 0 || d <= 0 || n_rows < 0)
+  if (!Q || !K || !V || !O || !LSE || N_q < 0 || N_k <= 0 || d <= 0 || n_rows < 0 ||
+      is_causal < 0 || is_causal > 2)
     return -1;
   if (!rows && n_rows != N_q) return -1;
   int failed = 0;
@@ -88,9 +105,12 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
         failed = 1;
         continue;
       }
-      /* visible keys: all of them, or j <= i under the causal mask */
-      int64_t n_vis = N_k;
-      if (is_causal && i + 1 < N_k) n_vis = i + 1;
+      const int64_t n_vis = visible_keys(i, N_q, N_k, is_causal);
+      if (n_vis == 0) { /* no visible key: empty sum */
+        for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+        LSE[r] = -INFINITY;
+        continue;
+      }
 
       const float* q = Q + i * q_row_stride;
       double m = -INFINITY;
@@ -149,7 +169,8 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
                                const int64_t* q_rows, int64_t n_q_rows,
                                const int64_t* k_rows, int64_t n_k_rows,
                                double* dQ, double* dK, double* dV) {
-  if (!Q || !K || !V || !dO || N_q <= 0 || N_k <= 0 || d <= 0 || n_q_rows < 0 || n_k_rows < 0)
+  if (!Q || !K || !V || !dO || N_q <= 0 || N_k <= 0 || d <= 0 || n_q_rows < 0 || n_k_rows < 0 ||
+      is_causal < 0 || is_causal > 2)
     return -1;
   if ((!q_rows && n_q_rows != N_q) || (!k_rows && n_k_rows != N_k)) return -1;
   if ((n_q_rows > 0 && !dQ) || (n_k_rows > 0 && (!dK || !dV))) return -1;
@@ -179,7 +200,12 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
 #pragma omp for schedule(dynamic, 4)
     for (int64_t i = 0; i < N_q; ++i) {
       if (!s || !o) continue;
-      const int64_t n_vis = (is_causal && i + 1 < N_k) ? i + 1 : N_k;
+      const int64_t n_vis = visible_keys(i, N_q, N_k, is_causal);
+      if (n_vis == 0) { /* no visible key: O = 0, so delta = 0; P = 0 in every product */
+        lse[i] = -INFINITY;
+        delta[i] = 0.0;
+        continue;
+      }
       const float* q = Q + i * q_row_stride;
       double m = -INFINITY;
       for (int64_t j = 0; j < n_vis; ++j) {
@@ -212,7 +238,7 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
   for (int64_t r = 0; r < n_q_rows; ++r) {
     if (failed) continue;
     const int64_t i = q_rows ? q_rows[r] : r;
-    const int64_t n_vis = (is_causal && i + 1 < N_k) ? i + 1 : N_k;
+    const int64_t n_vis = visible_keys(i, N_q, N_k, is_causal);
     const float* q = Q + i * q_row_stride;
     const float* g = dO + i * do_row_stride;
     double* out = dQ + r * d;
@@ -241,7 +267,8 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
     double* gk = dK + r * d;
     double* gv = dV + r * d;
     for (int64_t c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
-    for (int64_t i = is_causal ? j : 0; i < N_q; ++i) {
+    for (int64_t i = 0; i < N_q; ++i) {
+      if (j >= visible_keys(i, N_q, N_k, is_causal)) continue; /* query i does not see key j */
       const float* q = Q + i * q_row_stride;
       const float* g = dO + i * do_row_stride;
       double dot = 0.0, dp = 0.0;

@@ -19,7 +19,7 @@ import torch
 
 
 def _grid(shape, seed, step=2.0 ** -8, lim=4.0):
-    """Values on a 2^-8 grid in [-4, 4]: x +- 2^-12 stays exact in fp32."""
+    """Values on a 2^-8 grid in [-4, 4]: x +- 2^-12 and x +- 2^-13 stay exact in fp32."""
     r = np.random.default_rng(seed)
     return (np.round(r.uniform(-lim, lim, shape) / step) * step).astype(np.float32)
 
@@ -31,29 +31,33 @@ def _loss(fwd, Q, K, V, dO, scale, causal):
 
 def pin_finite_differences(bwd, fwd):
     eps = 2.0 ** -12
-    for causal in (False, True):
+    for causal in (False, True, 2):
         Q, K, V, dO = _grid((9, 8), 1), _grid((11, 8), 2), _grid((11, 8), 3), _grid((9, 8), 4)
         scale = 0.375
         dQ, dK, dV = bwd(Q, K, V, dO, scale, causal)
         r = np.random.default_rng(5)
         for which, g in ((0, dQ), (1, dK), (2, dV)):
             E = r.choice([-1.0, 1.0], size=[Q, K, V][which].shape).astype(np.float32)
-            args_p = [Q, K, V]
-            args_m = [Q, K, V]
-            args_p = [a + eps * E if i == which else a for i, a in enumerate(args_p)]
-            args_m = [a - eps * E if i == which else a for i, a in enumerate(args_m)]
-            num = (_loss(fwd, *args_p, dO, scale, causal) - _loss(fwd, *args_m, dO, scale, causal)) / (2 * eps)
+            def central(h):
+                args_p = [a + h * E if i == which else a for i, a in enumerate((Q, K, V))]
+                args_m = [a - h * E if i == which else a for i, a in enumerate((Q, K, V))]
+                return (_loss(fwd, *args_p, dO, scale, causal) - _loss(fwd, *args_m, dO, scale, causal)) / (2 * h)
+            # Richardson extrapolation of two exact steps (the eps^2 term cancels)
+            num = (4.0 * central(eps / 2) - central(eps)) / 3.0
             ana = float(np.sum(g * E))
             assert abs(num - ana) <= 1e-6 * (1.0 + abs(ana)), (which, causal, num, ana)
 
 
 def pin_torch_autograd(bwd, fwd):
     r = np.random.default_rng(7)
-    for causal, (nq, nk) in ((False, (13, 10)), (True, (13, 10)), (True, (8, 15))):
+    for causal, (nq, nk) in ((False, (13, 10)), (True, (13, 10)), (True, (8, 15)), (2, (8, 15)), (2, (10, 10))):
         Q, K, V, dO = (r.standard_normal(s).astype(np.float32) for s in ((nq, 16), (nk, 16), (nk, 16), (nq, 16)))
         dQ, dK, dV = bwd(Q, K, V, dO, 0.21, causal)
         q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
-        mask = torch.ones(nq, nk, dtype=torch.bool).tril() if causal else None
+        if causal is not True and causal == 2:
+            mask = torch.ones(nq, nk, dtype=torch.bool).tril(diagonal=nk - nq)
+        else:
+            mask = torch.ones(nq, nk, dtype=torch.bool).tril() if causal else None
         o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], attn_mask=mask, scale=0.21)[0]
         (o * torch.tensor(dO, dtype=torch.float64)).sum().backward()
         for got, want in ((dQ, q.grad), (dK, k.grad), (dV, v.grad)):
@@ -138,7 +142,8 @@ def _numpy_bwd(kind):
         Qd, Kd, Vd, Gd = (x.astype(np.float64) for x in (Q, K, V, dO))
         S = scale * Qd @ Kd.T
         if causal:
-            S = np.where(np.tri(*S.shape, dtype=bool), S, -np.inf)
+            k = S.shape[1] - S.shape[0] if (causal is not True and causal == 2) else 0
+            S = np.where(np.tri(*S.shape, k=k, dtype=bool), S, -np.inf)
         P = np.exp(S - S.max(1, keepdims=True))
         P /= P.sum(1, keepdims=True)
         O = P @ Vd
@@ -169,7 +174,8 @@ def _numpy_fwd(Q, K, V, scale, causal):
     Qd, Kd, Vd = (x.astype(np.float64) for x in (Q, K, V))
     S = scale * Qd @ Kd.T
     if causal:
-        S = np.where(np.tri(*S.shape, dtype=bool), S, -np.inf)
+        k = S.shape[1] - S.shape[0] if (causal is not True and causal == 2) else 0
+        S = np.where(np.tri(*S.shape, k=k, dtype=bool), S, -np.inf)
     m = S.max(1, keepdims=True)
     P = np.exp(S - m)
     l = P.sum(1, keepdims=True)

@@ -213,9 +213,31 @@ def pin_worked_examples(attn):
         np.testing.assert_allclose(L, L_want, rtol=0, atol=1e-12, err_msg=case["name"])
 
 
+def pin_bottom_right_causal(attn):
+    """is_causal = 2 (bottom-right alignment: key j visible to row i iff
+    j <= i + N_k - N_q): PyTorch SDPA (CPU, float64) with that explicit mask
+    on every row that sees a key; rows that see none (N_q > N_k) give O = 0 and
+    LSE = -inf; with N_q == N_k it is the top-left mask."""
+    for (Nq, Nk, seed) in [(9, 21, 60), (21, 9, 61), (13, 13, 62)]:
+        Q, K, V = _rand((Nq, 8), seed), _rand((Nk, 8), seed + 1), _rand((Nk, 8), seed + 2)
+        O, L = attn(Q, K, V, 0.3, 2)
+        mask = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+        tq, tk, tv = (torch.from_numpy(x.astype(np.float64)) for x in (Q, K, V))
+        seen = mask.any(1).numpy()
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            tq[None, seen], tk[None], tv[None], attn_mask=mask[seen], scale=0.3)[0]
+        S = (0.3 * tq @ tk.T).masked_fill(~mask, float("-inf"))
+        np.testing.assert_allclose(O[seen], ref.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L[seen], torch.logsumexp(S[seen], -1).numpy(), rtol=0, atol=1e-12)
+        assert np.all(O[~seen] == 0.0) and np.all(np.isneginf(L[~seen]))
+        if Nq == Nk:
+            O1, L1 = attn(Q, K, V, 0.3, True)
+            np.testing.assert_allclose(O, O1, rtol=0, atol=1e-12)
+
+
 PINS = [pin_q_zero, pin_scale_zero, pin_single_key, pin_first_causal_row,
         pin_permutation, pin_large_scores, pin_online_softmax_recompute,
-        pin_torch_sdpa, pin_invariants, pin_worked_examples]
+        pin_torch_sdpa, pin_invariants, pin_worked_examples, pin_bottom_right_causal]
 
 
 # ----------------------------------------------------------------------------
@@ -283,7 +305,13 @@ def _mutant(kind):
             S = -S
         i = np.arange(Nq)[:, None]
         j = np.arange(Nk)[None, :]
-        if causal:
+        if causal is not True and causal == 2:  # bottom-right alignment
+            off = Nk - Nq
+            if kind == "bottom_right_sign":
+                off = Nq - Nk
+            vis = j <= i + off
+            S = np.where(vis, S, -np.inf)
+        elif causal:
             if kind == "causal_strict":
                 vis = j < i
             elif kind == "causal_bottom_right":
@@ -291,6 +319,8 @@ def _mutant(kind):
             else:
                 vis = j <= i
             S = np.where(vis, S, -np.inf)
+        empty = np.all(np.isneginf(S), axis=1)  # rows that see no key: O = 0, LSE = -inf
+        S = np.where(empty[:, None], 0.0, S)
         if kind == "no_max_shift":
             with np.errstate(over="ignore", invalid="ignore"):
                 P = np.exp(S)
@@ -305,13 +335,16 @@ def _mutant(kind):
             L = np.log(l)
         if kind == "v_is_k":
             O = (P @ K) / l[:, None]
+        if kind != "bottom_right_empty_rows_mean":
+            O = np.where(empty[:, None], 0.0, O)
+            L = np.where(empty, -np.inf, L)
         return O, L
     return attn
 
 
 MUTANTS = ["no_scale", "transposed_scores", "negated_scores", "causal_strict",
            "causal_bottom_right", "no_max_shift", "no_normalise", "lse_log2",
-           "lse_missing_max", "v_is_k"]
+           "lse_missing_max", "v_is_k", "bottom_right_sign", "bottom_right_empty_rows_mean"]
 
 
 def test_correct_reference_passes_all_pins():

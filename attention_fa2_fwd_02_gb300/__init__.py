@@ -160,6 +160,17 @@ def _stream_ptr(device: torch.device, stream=None) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def causal_code(is_causal) -> int:
+    """The C ABI's is_causal: False -> 0 (no mask), True or "top_left" -> 1,
+    "bottom_right" -> 2 (key j visible to query row i iff j <= i + N_k - N_q)."""
+    if isinstance(is_causal, str):
+        codes = {"top_left": 1, "bottom_right": 2, "none": 0}
+        if is_causal not in codes:
+            raise ValueError(f"is_causal must be a bool, 'top_left' or 'bottom_right', not {is_causal!r}")
+        return codes[is_causal]
+    return 1 if is_causal else 0
+
+
 def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
     if not (Q.is_cuda and K.is_cuda and V.is_cuda):
         raise ValueError("Q, K, V must be CUDA tensors (this library has no CPU path)")
@@ -198,7 +209,7 @@ def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
         pb.LSE = None
         pb.lse_stride = (ctypes.c_int64 * 3)(0, 0, 0)
     pb.scale = float(scale)
-    pb.is_causal = 1 if is_causal else 0
+    pb.is_causal = causal_code(is_causal)
     return pb, out, lse
 
 
@@ -327,7 +338,7 @@ def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE:
         st = L.fa_bwd_gqa(_dtype_code(Q), B, H, H_kv, N_q, N_k, d,
                       ctypes.byref(_ft(q4)), ctypes.byref(_ft(k4)), ctypes.byref(_ft(v4)), ctypes.byref(_ft(o4)),
                       ctypes.byref(_ft(g4)), ctypes.c_void_p(l3.data_ptr()), (ctypes.c_int64 * 3)(*l3.stride()),
-                      float(scale), 1 if is_causal else 0,
+                      float(scale), causal_code(is_causal),
                       ctypes.byref(_ft(_as4(dQ))), ctypes.byref(_ft(_as4(dK))), ctypes.byref(_ft(_as4(dV))),
                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
                       _stream_ptr(Q.device, stream))
@@ -353,11 +364,12 @@ class _Attention(torch.autograd.Function):
 
 
 def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None = None,
-              is_causal: bool = False) -> torch.Tensor:
-    """softmax(scale * Q K^T) V with autograd: forward and backward on the GPU."""
+              is_causal: bool | str = False) -> torch.Tensor:
+    """softmax(scale * Q K^T) V with autograd: forward and backward on the GPU.
+    is_causal: False, True / "top_left", or "bottom_right"."""
     if scale is None:
         scale = 1.0 / math.sqrt(Q.shape[-1])
-    return _Attention.apply(Q, K, V, float(scale), bool(is_causal))
+    return _Attention.apply(Q, K, V, float(scale), is_causal if isinstance(is_causal, str) else bool(is_causal))
 
 
 def fwd_grouped(problems, stream=None):

@@ -115,7 +115,8 @@ fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* pa
   if (!std::isfinite(pb.scale)) return fail(FA_ERR_INVALID_ARG, at + "scale must be finite");
   if (pb.H_kv < 0 || (pb.H_kv > 0 && pb.H % pb.H_kv != 0))
     return fail(FA_ERR_INVALID_ARG, at + "H_kv must divide H (0 = H)");
-  if (pb.is_causal != 0 && pb.is_causal != 1) return fail(FA_ERR_INVALID_ARG, at + "is_causal must be 0 or 1");
+  if (pb.is_causal < 0 || pb.is_causal > 2)
+    return fail(FA_ERR_INVALID_ARG, at + "is_causal must be 0, 1 (top-left) or 2 (bottom-right)");
   if (pb.LSE && (pb.lse_stride[0] < 0 || pb.lse_stride[1] < 0 || pb.lse_stride[2] < 0))
     return fail(FA_ERR_UNSUPPORTED, at + "negative LSE strides are not supported");
   const fa_tensor_t* ts[4] = {&pb.Q, &pb.K, &pb.V, &pb.O};
@@ -201,7 +202,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   p.H = (int)pb.H;
   p.N_q = (int)pb.N_q;
   p.N_k = (int)pb.N_k;
-  p.causal = pb.is_causal;
+  p.causal = pb.is_causal == 0 ? kNoCausal : (pb.is_causal == 2 ? (int)(pb.N_k - pb.N_q) : 0);
   p.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
   p.n_qblk = (int)((pb.N_q + 255) / 256);
   p.n_tiles = (int)(pb.B * pb.H * p.n_qblk);
@@ -246,7 +247,8 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
     c.H = (int)pb.H;
     c.N_q = (int)pb.N_q;
     c.N_k = (int)pb.N_k;
-    c.causal = pb.is_causal;
+    c.causal = pb.is_causal != 0;
+    c.causal_off = pb.is_causal == 2 ? (int)(pb.N_k - pb.N_q) : 0;
     c.n_split = n_split;
     c.bn = bn;
     c.rows = pb.B * pb.H * pb.N_q;
@@ -356,7 +358,8 @@ fa_status_t launch_small(fa_dtype_t dtype, int d, const std::vector<const fa_pro
     s.kv_group = (int)(pb.H / kv_heads(pb));
     s.N_q = (int)pb.N_q;
     s.N_k = (int)pb.N_k;
-    s.causal = pb.is_causal;
+    s.causal = pb.is_causal != 0;
+    s.causal_off = pb.is_causal == 2 ? (int)(pb.N_k - pb.N_q) : 0;
     s.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
     s.n_qblk = (int)((pb.N_q + 31) / 32);
     s.vec_ok = row_aligned16(pb.Q, E) && row_aligned16(pb.K, E) && row_aligned16(pb.V, E) &&
@@ -611,7 +614,8 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   p.H = (int)H;
   p.N_q = (int)N_q;
   p.N_k = (int)N_k;
-  p.causal = is_causal;
+  p.causal = is_causal != 0;
+  p.causal_off = is_causal == 2 ? (int)(N_k - N_q) : 0;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.n_qt = (int)n_qt;

@@ -43,6 +43,7 @@ struct BwdParams {
   int B, H, N_q, N_k;
   int H_kv, kv_group;     // K/V heads, query heads per K/V head (grouped-query attention)
   int causal;
+  int causal_off;         // causal: key j visible to row i iff j <= i + causal_off
   float scale;            // softmax scale
   float scale_log2;       // scale * log2(e)
   int n_qt, n_kt;         // query tiles (BM rows) / key tiles (128)
@@ -138,8 +139,9 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   const int bhk = g0 + (rem - w.j * gh);
   w.b = bhk / p.H_kv;
   w.hk = bhk - w.b * p.H_kv;
-  // first query tile holding a row >= the tile's first key
-  w.i0 = p.causal ? (w.j * C::BN) / C::BM : 0;
+  // first query tile holding a row that sees the tile's first key
+  const int first_q = w.j * C::BN - p.causal_off;
+  w.i0 = (p.causal && first_q > 0) ? first_q / C::BM : 0;
   w.n_q = w.i0 < p.n_qt ? p.n_qt - w.i0 : 0;
   w.n_steps = w.n_q * p.kv_group;
   return w;
@@ -206,9 +208,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__
   for (int s = 16; s > 0; s >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, s);
   if (lane == 0) {
     p.delta[row] = dl;
-    p.nlse2[row] = q < p.N_q ? -p.LSE[b * p.lse_stride[0] + h * p.lse_stride[1] +
-                                      static_cast<long long>(q) * p.lse_stride[2]] * 1.4426950408889634f
-                             : -INFINITY;
+    // rows past N_q and rows that saw no key (LSE = -inf): -inf, so their P is 0
+    const float lse = q < p.N_q ? p.LSE[b * p.lse_stride[0] + h * p.lse_stride[1] +
+                                        static_cast<long long>(q) * p.lse_stride[2]]
+                                : -INFINITY;
+    p.nlse2[row] = lse == -INFINITY ? -INFINITY : -lse * 1.4426950408889634f;
   }
 }
 
@@ -440,7 +444,7 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
       tc_fence_after();
       // per-element masking only where needed: the key tail and tiles that
       // reach above the diagonal (query tails have -lse2 = -inf)
-      const bool need_mask = __any_sync(0xffffffffu, !key_ok || (p.causal && key > q0));
+      const bool need_mask = __any_sync(0xffffffffu, !key_ok || (p.causal && key > q0 + p.causal_off));
 #pragma unroll 1
       for (int c0 = 0; c0 < kCols; c0 += 32) {
         uint32_t sv[32], dpv[32];
@@ -460,8 +464,8 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
                                    h ? make_float2(l2.z, l2.w) : make_float2(l2.x, l2.y));
             float p0 = ex2(x.x), p1 = ex2(x.y);
             if (need_mask) {
-              if (!key_ok || (p.causal && key > q0 + c)) p0 = 0.f;
-              if (!key_ok || (p.causal && key > q0 + c + 1)) p1 = 0.f;
+              if (!key_ok || (p.causal && key > q0 + c + p.causal_off)) p0 = 0.f;
+              if (!key_ok || (p.causal && key > q0 + c + 1 + p.causal_off)) p1 = 0.f;
             }
             const float2 g = fadd2(make_float2(__uint_as_float(dpv[k + h]), __uint_as_float(dpv[k + h + 1])),
                                    h ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y));

@@ -8,7 +8,7 @@
 // the log-sum-exps):
 //     L = log sum_s e^{L_s},   O = sum_s e^{L_s - L} O_s.
 // A split none of whose keys a row sees (causal) has O_s = 0, L_s = -inf and
-// weight 0.  One warp per row; each lane owns D/32 consecutive columns.
+// weight 0; a row that sees no key at all gets O = 0, L = -inf.  One warp per row; each lane owns D/32 consecutive columns.
 #pragma once
 
 #include "fa_ptx.cuh"
@@ -19,6 +19,7 @@ constexpr int kMaxSplit = 8;
 
 struct CombineParams {
   int B, H, N_q, N_k, causal, n_split, bn;  // bn: key-tile width used by the split kernel
+  int causal_off;                           // as TcParams::causal_off
   long long rows;                           // B * H * N_q
   const float* ws_o;                        // [n_split][rows][D]
   const float* ws_lse;                      // [n_split][rows]
@@ -40,8 +41,8 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const __grid_constant__
   // splits that exist for this row's 256-row tile (same rule as the split kernel)
   const int q0 = (q / 256) * 256;
   int kv_end = p.N_k;
-  if (p.causal) kv_end = min(kv_end, min(q0 + 256, p.N_q));
-  const int n_tot = (kv_end + p.bn - 1) / p.bn;
+  if (p.causal) kv_end = min(kv_end, min(q0 + 256, p.N_q) + p.causal_off);
+  const int n_tot = kv_end > 0 ? (kv_end + p.bn - 1) / p.bn : 0;
   const int s_eff = min(p.n_split, n_tot);
 
   float lse_s[kMaxSplit];
@@ -54,8 +55,10 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const __grid_constant__
   float l = 0.f;
 #pragma unroll
   for (int s = 0; s < kMaxSplit; ++s)
-    if (s < s_eff) l += expf(lse_s[s] - m);
-  const float lse = m + logf(l);
+    if (s < s_eff && m != -INFINITY) l += expf(lse_s[s] - m);
+  // a row that sees no key in any split (bottom-right causal, N_q > N_k):
+  // l = 0, so LSE = -inf and every weight below is 0
+  const float lse = m == -INFINITY ? -INFINITY : m + logf(l);
 
   float acc[PER];
 #pragma unroll
@@ -63,7 +66,7 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const __grid_constant__
 #pragma unroll
   for (int s = 0; s < kMaxSplit; ++s) {
     if (s >= s_eff) break;
-    const float w = expf(lse_s[s] - lse);
+    const float w = lse == -INFINITY ? 0.f : expf(lse_s[s] - lse);
     const float* src = p.ws_o + (s * p.rows + row) * D + lane * PER;
     if constexpr (PER == 4) {
       const float4 v = *reinterpret_cast<const float4*>(src);

@@ -36,6 +36,7 @@ struct SmallProblem {
   int B, H, N_q, N_k;
   int kv_group;        // query heads per K/V head (grouped-query attention; 1 = none)
   int causal;
+  int causal_off;      // causal: key j visible to row i iff j <= i + causal_off
   float scale_log2;
   int n_qblk;          // ceil(N_q / 32)
   int vec_ok;          // every row starts on a 16-byte boundary
@@ -140,8 +141,8 @@ fa_small_fwd_kernel(const __grid_constant__ SmallParams P) {
 #pragma unroll
   for (int c = 0; c < D; ++c) acc[c] = 0.f;
   float m = -INFINITY, l = 0.f;
-  const int vis_end = pr.causal ? min(pr.N_k, q + 1) : pr.N_k;        // this lane's keys
-  const int kv_end = pr.causal ? min(pr.N_k, r0 + 32) : pr.N_k;       // the warp's keys
+  const int vis_end = pr.causal ? min(pr.N_k, q + 1 + pr.causal_off) : pr.N_k;   // this lane's keys
+  const int kv_end = pr.causal ? min(pr.N_k, r0 + 32 + pr.causal_off) : pr.N_k;  // the warp's keys
 
 #pragma unroll 1
   for (int kc = 0; kc < kv_end; kc += 32) {
@@ -166,7 +167,8 @@ fa_small_fwd_kernel(const __grid_constant__ SmallParams P) {
       mloc = fmaxf(mloc, s[jj]);
     }
     const float m_new = fmaxf(m, mloc);
-    const float alpha = ex2(m - m_new);  // m = -inf on the first chunk -> 0
+    // m = -inf on the first chunk -> 0; a row that has seen no key keeps 1
+    const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
     l *= alpha;
 #pragma unroll
     for (int c = 0; c < D; ++c) acc[c] *= alpha;
@@ -187,7 +189,7 @@ fa_small_fwd_kernel(const __grid_constant__ SmallParams P) {
   }
 
   // epilogue: O = acc / l through shared memory, LSE = (m + log2 l) ln 2
-  const float inv = 1.f / l;
+  const float inv = l > 0.f ? 1.f / l : 0.f;  // a row that sees no key: O = 0, LSE = -inf
   __syncwarp();
 #pragma unroll
   for (int c = 0; c < D; c += 4)

@@ -33,10 +33,14 @@ namespace fa {
 
 constexpr float kTau = 8.0f;              // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994531f;
+// TcParams::causal value for "no causal mask" (the field is the mask's offset
+// otherwise; one int keeps the kernel's parameter block at its size)
+constexpr int kNoCausal = 0x7fffffff;
 
 struct TcParams {
   int B, H, N_q, N_k;
-  int causal;
+  int causal;             // kNoCausal: no mask; else key j is visible to row i iff j <= i + causal
+                          // (0: top-left alignment, N_k - N_q: bottom-right)
   float scale_log2;       // scale * log2(e)
   int n_qblk;             // ceil(N_q / 256)
   int n_tiles;            // B * H * n_qblk
@@ -157,7 +161,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   const int heads = min(p.head_group, BH - g * p.head_group);
   const int qi = r / heads;
   const int bh = g * p.head_group + (r - qi * heads);
-  const int qb = p.causal ? (p.n_qblk - 1 - qi) : qi;
+  const int qb = p.causal != kNoCausal ? (p.n_qblk - 1 - qi) : qi;
   TileInfo ti;
   ti.b = bh / p.H;
   ti.h = bh - ti.b * p.H;
@@ -165,11 +169,15 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   ti.q0 = qb * 256;
   ti.split = split;
   int kv_end = p.N_k;
-  if (p.causal) kv_end = min(kv_end, min(ti.q0 + 256, p.N_q));
-  const int n_tot = (kv_end + BN - 1) / BN;
+  if (p.causal != kNoCausal) kv_end = min(kv_end, min(ti.q0 + 256, p.N_q) + p.causal);
+  // (bottom-right alignment with N_q > N_k: a tile may see no key at all)
+  const int n_tot = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
   if constexpr (!C::kSplit) {
+    // A tile that sees no key (bottom-right causal, N_q > N_k) still takes
+    // one fully masked key tile: its rows get l = 0, hence O = 0 and
+    // LSE = -inf, and no role needs a skip test.
     ti.j0 = 0;
-    ti.n_kv = n_tot;
+    ti.n_kv = n_tot > 0 ? n_tot : 1;
     return ti;
   }
   const int s_eff = min(p.n_split, n_tot);
@@ -407,7 +415,7 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
     counted = C::kSplit ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
     const int q = ti.q0 + stage * C::BM + row;
-    const int vis_end = p.causal ? min(p.N_k, q + 1) : p.N_k;  // keys < vis_end are visible
+    const int vis_end = p.causal != kNoCausal ? min(p.N_k, q + 1 + p.causal) : p.N_k;  // keys < vis_end are visible
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < ti.n_kv; ++j) {
       if (!warp_wait(&bars.s_full[stage], s_par, wd, 0x30 + stage)) return;
@@ -532,9 +540,9 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
     }
     // hand the row statistics to the epilogue: 1/l and LSE (natural log)
     if (!warp_wait(&bars.st_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x32 + stage)) return;
-    // (l_run = 0 only in a split-KV unit none of whose keys this row sees:
-    // then O = 0 and LSE = -inf, which the combine step weighs by zero)
-    const float inv_l = C::kSplit ? (l_run > 0.f ? 1.f / l_run : 0.f) : 1.f / l_run;
+    // (l_run = 0 only for a row that sees no key of the unit -- a split-KV
+    // unit, or bottom-right causal with N_q > N_k: then O = 0 and LSE = -inf)
+    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     stats[stage * C::BM + row] = make_float2(inv_l, (m_run + __log2f(l_run)) * kLn2);
     mbar_arrive(&bars.st_full[stage]);
   }

@@ -72,7 +72,10 @@ typedef struct {
  *   Q              [B, H, N_q, d] device view.
  *   K, V           [B, H, N_k, d] device views.
  *   scale          multiplier of Q.K (finite; 1/sqrt(d) is the usual choice).
- *   is_causal      0 or 1; top-left causal mask (key j visible iff j <= i).
+ *   is_causal      0: no mask; 1: top-left causal mask (key j visible to
+ *                  query row i iff j <= i); 2: bottom-right alignment (j <=
+ *                  i + N_k - N_q; with N_q > N_k the first rows see no key and
+ *                  get O = 0, LSE = -inf).
  *   O              [B, H, N_q, d] device view, written.  Must not overlap the inputs.
  *   LSE            fp32 [B, H, N_q] device array written at
  *                  LSE + b*lse_stride[0] + h*lse_stride[1] + i*lse_stride[2],

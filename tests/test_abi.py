@@ -75,7 +75,7 @@ def _call(L, dtype=fa.FA_BF16, B=1, H=1, Nq=256, Nk=256, d=128, qptr=0x10000, st
     (dict(strides=(256 * 128, 256 * 128, 128, 2)), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
-    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),   # 0, 1 (top-left), 2 (bottom-right)
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),

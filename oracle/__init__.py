@@ -24,6 +24,7 @@ flash_attention_reference; "Blackwell Attention Example", kernel docstring):
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -185,3 +186,44 @@ def attention_bwd(Q, K, V, dO, scale: float, is_causal: bool = False, q_rows=Non
         if rc != 0:
             raise RuntimeError(f"oracle_attention_bwd_slice failed with {rc}")
     return dQ.reshape(*lead, nq, d), dK.reshape(*lead, nk, d), dV.reshape(*lead, nk, d)
+
+
+def layer_norm(x, weight, bias, eps: float = 1e-5):
+    """fp64 LayerNorm over the last dim: (x - mean) / sqrt(var + eps) * w + b,
+    var the biased (population) variance, as torch.nn.LayerNorm."""
+    x = np.asarray(x, dtype=np.float64)
+    mean = x.mean(-1, keepdims=True)
+    var = ((x - mean) ** 2).mean(-1, keepdims=True)
+    return (x - mean) / np.sqrt(var + eps) * np.asarray(weight, np.float64) + np.asarray(bias, np.float64)
+
+
+def _axial_pass(seqs, p, heads: int):
+    """One pass of the axial block on sequences [S, L, D] (fp64): the axial
+    transcript's _attn_ref (LayerNorm, bias-free QKV projection, per-head
+    softmax(q k^T / sqrt(d)) v, output projection with bias) plus the
+    residual of its forward."""
+    S, L, D = seqs.shape
+    d = D // heads
+    xn = layer_norm(seqs, p["norm_w"], p["norm_b"])
+    qkv = xn @ np.asarray(p["qkv_w"], np.float64).T            # [S, L, 3D]
+    qkv = qkv.reshape(S, L, 3, heads, d)
+    q, k, v = (qkv[:, :, i].transpose(0, 2, 1, 3) for i in range(3))   # [S, heads, L, d]
+    # softmax(q k^T / sqrt(d)) v per (sequence, head), fp64, written out
+    sc = (q @ k.transpose(0, 1, 3, 2)) / math.sqrt(d)                  # [S, heads, L, L]
+    pr = np.exp(sc - sc.max(-1, keepdims=True))
+    pr /= pr.sum(-1, keepdims=True)
+    o = (pr @ v).transpose(0, 2, 1, 3).reshape(S, L, D)
+    return seqs + o @ np.asarray(p["out_w"], np.float64).T + np.asarray(p["out_b"], np.float64)
+
+
+def axial_block(x, row, col, heads: int):
+    """fp64 forward of the axial attention block on x [B, H, W, D]: the row
+    pass over the W-long rows, then the column pass over the H-long columns of
+    the updated grid ("axial attention" transcript, the module's forward).
+    row / col: dicts of norm_w, norm_b [D], qkv_w [3D, D], out_w [D, D],
+    out_b [D].  Returns float64 [B, H, W, D]."""
+    x = np.asarray(x, dtype=np.float64)
+    B, H, W, D = x.shape
+    y = _axial_pass(x.reshape(B * H, W, D), row, heads).reshape(B, H, W, D)
+    yc = y.transpose(0, 2, 1, 3).reshape(B * W, H, D)
+    return _axial_pass(yc, col, heads).reshape(B, W, H, D).transpose(0, 2, 1, 3)

@@ -22,7 +22,7 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["fwd", "fwd_noalloc", "bwd", "attention", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
+__all__ = ["fwd", "fwd_noalloc", "bwd", "attention", "axial_block", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
            "LIB_PATH", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT"]
 
@@ -44,6 +44,11 @@ class FaProblem(ctypes.Structure):
                 ("Q", FaTensor), ("K", FaTensor), ("V", FaTensor), ("O", FaTensor),
                 ("LSE", ctypes.c_void_p), ("lse_stride", ctypes.c_int64 * 3),
                 ("scale", ctypes.c_float), ("is_causal", ctypes.c_int), ("H_kv", ctypes.c_int64)]
+
+
+class AxialWeights(ctypes.Structure):
+    _fields_ = [("norm_w", ctypes.c_void_p), ("norm_b", ctypes.c_void_p), ("qkv_w", ctypes.c_void_p),
+                ("out_w", ctypes.c_void_p), ("out_b", ctypes.c_void_p)]
 
 
 class FaError(RuntimeError):
@@ -107,6 +112,9 @@ def lib() -> ctypes.CDLL:
                                                  P(FaTensor), ctypes.c_float, ctypes.c_int, P(FaTensor),
                                                  ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int,
                                                  ctypes.c_void_p]
+            L.fa_axial_block_fwd.restype = ctypes.c_int
+            L.fa_axial_block_fwd.argtypes = [ctypes.c_int64] * 5 + [ctypes.c_void_p, P(AxialWeights),
+                                                                   P(AxialWeights), ctypes.c_void_p, ctypes.c_void_p]
             L.fa_fwd_gqa.restype = ctypes.c_int
             L.fa_fwd_gqa.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 6 + [P(FaTensor)] * 3 + \
                 [ctypes.c_float, ctypes.c_int, P(FaTensor), ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p]
@@ -370,6 +378,38 @@ def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | 
     if scale is None:
         scale = 1.0 / math.sqrt(Q.shape[-1])
     return _Attention.apply(Q, K, V, float(scale), is_causal if isinstance(is_causal, str) else bool(is_causal))
+
+
+def axial_block(x: torch.Tensor, row: dict, col: dict, heads: int = 4, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """The axial attention block (row pass, then column pass), fused per sequence.
+
+    x: contiguous fp32 CUDA tensor [B, H, W, D] (D = 64, heads = 4, H, W <= 32).
+    row / col: dicts of CUDA fp32 tensors norm_w, norm_b [D], qkv_w [3D, D],
+    out_w [D, D], out_b [D] (nn.LayerNorm / nn.Linear parameter layouts).
+    Returns out (allocated if not given; may be x for an in-place update).
+    """
+    if not x.is_cuda or x.dtype != torch.float32 or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 CUDA tensor [B, H, W, D]")
+    out = torch.empty_like(x) if out is None else out
+    if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like x")
+    keep = []
+
+    def pack(p):
+        ts = [p[k].contiguous() for k in ("norm_w", "norm_b", "qkv_w", "out_w", "out_b")]
+        for t in ts:
+            if not t.is_cuda or t.dtype != torch.float32:
+                raise ValueError("axial block weights must be fp32 CUDA tensors")
+        keep.extend(ts)
+        return AxialWeights(*(ctypes.c_void_p(t.data_ptr()) for t in ts))
+    rw, cw = pack(row), pack(col)
+    B, H, W, D = x.shape
+    with torch.cuda.device(x.device):
+        st = lib().fa_axial_block_fwd(B, H, W, D, heads, ctypes.c_void_p(x.data_ptr()), ctypes.byref(rw),
+                                      ctypes.byref(cw), ctypes.c_void_p(out.data_ptr()), _stream_ptr(x.device, stream))
+    _raise_on(st)
+    return out
 
 
 def fwd_grouped(problems, stream=None):

@@ -18,6 +18,7 @@
 #include "fa.h"
 #include "fa_combine.cuh"
 #include "fa_launch.h"
+#include "fa_axial_block.cuh"
 #include "fa_small.cuh"
 
 namespace fa {
@@ -49,6 +50,7 @@ struct DevState {
   int sm_count = 0;
   unsigned int* err = nullptr;
   bool small_attr[2][2] = {{false, false}, {false, false}};  // [bf16/fp32][d16/d32] opt-in set
+  bool axial_attr = false;                                   // fused axial block opt-in set
 };
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
@@ -673,6 +675,66 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   L.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_bf16(L);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("backward launch", e));
+  return FA_OK;
+}
+
+fa_status_t fa_axial_block_fwd(int64_t B, int64_t H, int64_t W, int64_t D, int64_t heads, const float* x,
+                               const fa_axial_weights_t* row, const fa_axial_weights_t* col, float* out,
+                               void* stream) {
+  if (!x || !out || !row || !col) return fail(FA_ERR_INVALID_ARG, "x, out and the weights must not be NULL");
+  if (B <= 0 || H <= 0 || W <= 0) return fail(FA_ERR_INVALID_ARG, "B, H, W must be >= 1");
+  if (D != kAxD || heads != kAxHeads)
+    return fail(FA_ERR_UNSUPPORTED, "the fused axial block takes D = 64 with 4 heads");
+  if (H > kAxMaxL || W > kAxMaxL) return fail(FA_ERR_UNSUPPORTED, "the fused axial block takes H, W <= 32");
+  if (B * H * W * D >= (1ll << 40)) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  const void* ptrs[] = {x, out, row->norm_w, row->norm_b, row->qkv_w, row->out_w, row->out_b,
+                        col->norm_w, col->norm_b, col->qkv_w, col->out_w, col->out_b};
+  for (const void* q : ptrs) {
+    if (!q) return fail(FA_ERR_INVALID_ARG, "a weight pointer is NULL");
+    if (reinterpret_cast<uintptr_t>(q) % 16 != 0)
+      return fail(FA_ERR_UNSUPPORTED, "x, out and the weights must be 16-byte aligned");
+  }
+  DevState* ds = nullptr;
+  fa_status_t st = device_state(&ds);
+  if (st != FA_OK) return st;
+  const int smem = static_cast<int>(sizeof(AxialSmem));
+  {  // once per device (so that a captured launch makes no attribute call)
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!ds->axial_attr) {
+      cudaError_t e = cudaFuncSetAttribute(fa_axial_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("cudaFuncSetAttribute (axial block)", e));
+      ds->axial_attr = true;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int pass = 0; pass < 2; ++pass) {
+    const fa_axial_weights_t* wgt = pass == 0 ? row : col;
+    AxialPassParams p{};
+    p.x = pass == 0 ? x : out;  // the column pass reads the row pass's output
+    p.out = out;
+    p.outer_stride = H * W * D;
+    if (pass == 0) {  // rows: sequence (b, h), tokens w
+      p.n_seq = (int)(B * H);
+      p.L = (int)W;
+      p.seq_div = (int)H;
+      p.inner_stride = W * D;
+      p.tok_stride = D;
+    } else {          // columns: sequence (b, w), tokens h
+      p.n_seq = (int)(B * W);
+      p.L = (int)H;
+      p.seq_div = (int)W;
+      p.inner_stride = D;
+      p.tok_stride = W * D;
+    }
+    p.norm_w = wgt->norm_w;
+    p.norm_b = wgt->norm_b;
+    p.qkv_w = wgt->qkv_w;
+    p.out_w = wgt->out_w;
+    p.out_b = wgt->out_b;
+    fa_axial_pass_kernel<<<p.n_seq, 256, smem, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("axial block launch", e));
+  }
   return FA_OK;
 }
 

@@ -145,3 +145,50 @@ class AxialWorkload:
 
 
 AXIAL = AxialWorkload()
+
+
+@dataclass(frozen=True)
+class AxialBlockWorkload:
+    """The whole axial attention block (row pass then column pass) on a grid
+    x [B, H, W, D] fp32 with random weights: LayerNorm, QKV projection,
+    4-head attention, output projection with bias, residual, per pass."""
+    name: str = "axial_block"
+    B: int = 4
+    H: int = 32
+    W: int = 32
+    D: int = 64
+    heads: int = 4
+    seed: int = 11
+
+    @property
+    def shape(self):
+        return (self.B, self.H, self.W, self.D)
+
+    @property
+    def flops(self) -> float:
+        """Per pass and sequence of L tokens: QKV 2*L*D*3D, attention
+        4*L^2*D, output projection 2*L*D*D (LayerNorm, softmax and the
+        residual not counted)."""
+        def per_seq(L):
+            return 2.0 * L * self.D * 3 * self.D + 4.0 * L * L * self.D + 2.0 * L * self.D * self.D
+        return self.B * self.H * per_seq(self.W) + self.B * self.W * per_seq(self.H)
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """The grid read and written once per pass, both passes' weights read once."""
+        grid = self.B * self.H * self.W * self.D * 4
+        weights = 2 * (3 * self.D * self.D + self.D * self.D + 3 * self.D) * 4
+        return 4.0 * grid + weights
+
+    def weights(self, seed):
+        D = self.D
+        return dict(norm_w=1.0 + 0.1 * normal((D,), seed), norm_b=0.1 * normal((D,), seed + 1),
+                    qkv_w=normal((3 * D, D), seed + 2) / 8.0, out_w=normal((D, D), seed + 3) / 8.0,
+                    out_b=0.1 * normal((D,), seed + 4))
+
+    def make(self):
+        """x, row weights, column weights (CPU fp32; weights ~ nn.Linear scale 1/sqrt(D))."""
+        return normal(self.shape, 3 * self.seed), self.weights(10 * self.seed), self.weights(10 * self.seed + 5)
+
+
+AXIAL_BLOCK = AxialBlockWorkload()

@@ -196,7 +196,12 @@ def whole_job_value(flops_per_step: float, world: int, slowest_ms_per_step: floa
 
 
 def workload_desc(w) -> dict:
-    from attention_fa2_fwd_02_gb300.inputs import AxialWorkload
+    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload, AxialWorkload
+    if isinstance(w, AxialBlockWorkload):
+        return {"workload": f"axial attention block x[{w.B},{w.H},{w.W},{w.D}] fp32, {w.heads} heads: LayerNorm + "
+                            f"QKV + attention + out-projection + residual, row pass then column pass, "
+                            f"random weights",
+                "shape": list(w.shape), "heads": w.heads}
     if isinstance(w, AxialWorkload):
         return {"workload": f"axial attention core x[{w.B},{w.Hg},{w.Wg},{w.heads},{w.hd}] fp32, "
                             f"row + column, scale {w.scale}",
@@ -213,9 +218,11 @@ def workload_desc(w) -> dict:
 def get_workload(name):
     """The workload; names ending in ``_bwd`` time the backward pass of the
     named forward workload (bf16, d = 64 or 128)."""
-    from attention_fa2_fwd_02_gb300.inputs import AXIAL, WORKLOADS
+    from attention_fa2_fwd_02_gb300.inputs import AXIAL, AXIAL_BLOCK, WORKLOADS
     if name == "axial":
         return AXIAL
+    if name == "axial_block":
+        return AXIAL_BLOCK
     base = name[:-4] if name.endswith("_bwd") else name
     if base not in WORKLOADS:
         raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)}, axial, "
@@ -302,6 +309,11 @@ def oracle_sample(w, Q, K, V, budget_s: float, rows_per_call: int = 512):
     return flops, dt, f"{n_rows} query rows ({rows_per_call}-row blocks of random (b,h) slices)"
 
 
+def axial_block_oracle_step(w, x, row, col):
+    import oracle
+    return oracle.axial_block(x, row, col, w.heads)
+
+
 def run_reference(args, w):
     """--impl reference: the oracle on the host cores, each step a bounded sample."""
     rank = int(os.environ.get("RANK", "0"))
@@ -309,6 +321,28 @@ def run_reference(args, w):
         return
     import oracle
     oracle.build()
+    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload
+    if isinstance(w, AxialBlockWorkload):  # the whole block per step (it is small)
+        x, row, col = w.make()
+        xn, rn, cn = x.numpy(), {k: v.numpy() for k, v in row.items()}, {k: v.numpy() for k, v in col.items()}
+        steps, warm = args.steps, max(3, args.warmup)
+        for _ in range(warm):
+            axial_block_oracle_step(w, xn, rn, cn)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            axial_block_oracle_step(w, xn, rn, cn)
+        el = time.perf_counter() - t0
+        val = w.flops * steps / el / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": "axial block TFLOP/s", "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(w),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "the full block (row + column pass) per step, numpy fp64"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     Q, K, V = w.make()
     steps, warm = args.steps, max(3, args.warmup)
     if args.workload.endswith("_bwd"):
@@ -376,11 +410,119 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ GPU leg
+def run_axial_block(args, w):
+    """The fused axial block: two launches per step (row pass, column pass),
+    HBM roofline, end to end with the grid copied in and out every step."""
+    import attention_fa2_fwd_02_gb300 as fa
+    world, rank, local, dist = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.build()
+    warm, steps = max(3, args.warmup), max(1, args.steps)
+    xh, row, col = w.make()
+    xd = xh.to(dev)
+    rowd, cold = ({k: v.to(dev) for k, v in p.items()} for p in (row, col))
+    outd = torch.empty_like(xd)
+    stream = torch.cuda.current_stream(dev)
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2**20
+    flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)  # the grid fits in L2: flush
+
+    def step():
+        return fa.axial_block(xd, rowd, cold, heads=w.heads, out=outd)
+    for _ in range(warm):
+        flush.zero_()
+        step()
+    fa.check()
+    graph = torch.cuda.CUDAGraph()  # microsecond launches: timed from a graph replay
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for k in range(steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        graph.replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    fa.check()
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    step_ms = max_over_ranks(kernel_ms, dist)
+    value = whole_job_value(w.flops, world, step_ms)
+    peaks, peak_src = load_peaks()
+    achieved = w.algorithmic_bytes / (kernel_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+            "frac": achieved / float(peaks["hbm_gbs"]), "traffic": recorded_traffic(args.workload),
+            "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
+            "timed": "row-pass + column-pass launches of fa_axial_pass_kernel"}
+    e2e = None
+    if not args.no_e2e:
+        xp, op = xh.pin_memory(), torch.empty_like(xh).pin_memory()
+
+        def e2e_step():
+            xd.copy_(xp, non_blocking=True)
+            step()
+            op.copy_(outd, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(3, min(steps, 50))
+        a.record(stream)
+        for _ in range(n):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(a.elapsed_time(b) / n, dist)
+        nb = xh.numel() * 4
+        e2e = {"value": whole_job_value(w.flops, world, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
+        fa.check()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xn, rn, cn = xh.numpy(), {k: v.numpy() for k, v in row.items()}, {k: v.numpy() for k, v in col.items()}
+        t0, reps = time.perf_counter(), 0
+        while True:
+            axial_block_oracle_step(w, xn, rn, cn)
+            reps += 1
+            if time.perf_counter() - t0 >= min(args.cpu_seconds, 5.0):
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": w.flops * reps / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} full blocks (row + column pass), numpy fp64; {dt:.1f} s"}
+    if rank == 0:
+        cfg = workload_desc(w)
+        cfg["l2"] = "L2 flushed (%.0f MB write) between steps" % (flush.numel() * 4 / 2**20)
+        cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
+        cfg["cuda_graph"] = True
+        print(json.dumps({
+            "metric": "axial block TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded i.i.d. N(0,1) grid and weights)",
+            "config": cfg, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": 2 * steps, "kernel_ms": kernel_ms}), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     w = get_workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload
+    if isinstance(w, AxialBlockWorkload):
+        run_axial_block(args, w)
         return
     import attention_fa2_fwd_02_gb300 as fa
     from attention_fa2_fwd_02_gb300.inputs import AxialWorkload

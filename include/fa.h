@@ -254,6 +254,34 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
                    size_t workspace_bytes, void* stream);
 
 /*
+ * fa_axial_block_fwd -- the axial attention block of the axial-attention
+ * transcript (its module's forward), fused per sequence, fp32: on x
+ * [B, H, W, D] (contiguous), a row pass over the W-long rows and then a
+ * column pass over the H-long columns of the updated grid, each
+ *     x += out_proj(attention(qkv_proj(LayerNorm(x))))
+ * with LayerNorm (biased variance, eps 1e-5, weight and bias), a bias-free
+ * QKV projection (qkv_w [3D, D], rows q | k | v, as nn.Linear's weight),
+ * softmax(q k^T / sqrt(D / heads)) v per head and an output projection
+ * (out_w [D, D], out_b [D]).
+ *
+ *   Supported: D = 64, heads = 4, 1 <= H, W <= 32 (FA_ERR_UNSUPPORTED
+ *   otherwise); x, out and every weight 16-byte aligned.
+ *   out            [B, H, W, D], written; may be x (in place).
+ * Asynchronous on `stream` (two launches).
+ */
+typedef struct {
+  const float* norm_w; /* [D] */
+  const float* norm_b; /* [D] */
+  const float* qkv_w;  /* [3D, D] */
+  const float* out_w;  /* [D, D] */
+  const float* out_b;  /* [D] */
+} fa_axial_weights_t;
+
+fa_status_t fa_axial_block_fwd(int64_t B, int64_t H, int64_t W, int64_t D, int64_t heads, const float* x,
+                               const fa_axial_weights_t* row, const fa_axial_weights_t* col, float* out,
+                               void* stream);
+
+/*
  * fa_check -- synchronise `stream`, then read and clear the device error word
  * raised by kernels launched from this library on the current device.
  * Returns FA_OK, FA_ERR_TIMEOUT (a bounded wait expired in some launch since

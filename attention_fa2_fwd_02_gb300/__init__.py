@@ -22,7 +22,7 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["fwd", "fwd_noalloc", "bwd", "attention", "axial_block", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
+__all__ = ["fwd", "fwd_noalloc", "fwd_varlen", "bwd", "attention", "axial_block", "fwd_grouped", "axial", "check", "debug_set", "FaError", "lib", "build",
            "LIB_PATH", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT"]
 
@@ -122,6 +122,10 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_gqa.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 6 + [P(FaTensor)] * 5 +
                                      [ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_float, ctypes.c_int] +
                                      [P(FaTensor)] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
+            L.fa_fwd_varlen.restype = ctypes.c_int
+            L.fa_fwd_varlen.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 7 + [ctypes.c_void_p] * 2 +
+                                        [P(FaTensor)] * 3 + [ctypes.c_float, ctypes.c_int, P(FaTensor),
+                                                             ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p])
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
             L.fa_bwd.restype = ctypes.c_int
@@ -299,6 +303,62 @@ def fwd_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: torch.Te
                                       pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE,
                                       (ctypes.c_int64 * 3)(*pb.lse_stride), n_split,
                                       _stream_ptr(Q.device, stream))
+    _raise_on(st)
+    return out, lse
+
+
+def fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+               cu_seqlens_k: torch.Tensor, max_seqlen_q: int, scale: float | None = None,
+               is_causal=False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+               with_lse: bool = True, stream=None):
+    """Attention over a packed batch of sequences of different lengths.
+
+    q: [total_q, H, d], k and v: [total_k, H_kv, d] (H_kv divides H), bf16,
+    d = 64 or 128, rows of sequence b at cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+    (and likewise for the keys); the offsets are int32 CUDA tensors of B + 1
+    entries from 0 to total.  Each sequence attends only to itself;
+    ``is_causal`` (False, True / "top_left", "bottom_right") applies per
+    sequence.  ``max_seqlen_q`` bounds the query lengths (it sizes the grid).
+    Returns (out [total_q, H, d], lse [H, total_q] fp32 or None).
+    """
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and cu_seqlens_q.is_cuda and cu_seqlens_k.is_cuda):
+        raise ValueError("q, k, v and the offsets must be CUDA tensors (this library has no CPU path)")
+    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or k.shape[2] != q.shape[2]:
+        raise ValueError(f"expected q [total_q, H, d], k/v [total_k, H_kv, d]: "
+                         f"{tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for name, cu in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_contiguous() or cu.device != q.device:
+            raise ValueError(f"{name} must be a contiguous 1-D int32 tensor on q's device")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 >= 2 offsets")
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or out.device != q.device:
+        raise ValueError("out must match q's shape, dtype and device")
+    if with_lse and lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (H, total_q) or lse.dtype != torch.float32 or lse.device != q.device):
+        raise ValueError("lse must be fp32 [H, total_q] on q's device")
+
+    def view(t):  # [total, heads, d] -> [1, heads, total, d]
+        return _ft(t.permute(1, 0, 2).unsqueeze(0))
+    tq, tk, tv, to = view(q), view(k), view(v), view(out)
+    lse_stride = (ctypes.c_int64 * 3)(0, *(lse.stride() if lse is not None else (0, 0)))
+    L = lib()
+    with torch.cuda.device(q.device):
+        st = L.fa_fwd_varlen(_dtype_code(q), B, H, H_kv, total_q, total_k, int(max_seqlen_q), d,
+                             ctypes.c_void_p(cu_seqlens_q.data_ptr()), ctypes.c_void_p(cu_seqlens_k.data_ptr()),
+                             ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), float(scale),
+                             causal_code(is_causal), ctypes.byref(to),
+                             ctypes.c_void_p(lse.data_ptr()) if lse is not None else None, lse_stride,
+                             _stream_ptr(q.device, stream))
     _raise_on(st)
     return out, lse
 

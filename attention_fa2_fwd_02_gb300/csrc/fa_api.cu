@@ -678,6 +678,77 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   return FA_OK;
 }
 
+fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
+                          int64_t max_len_q, int64_t d, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                          int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                          void* stream) {
+  if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
+  if (!cu_seqlens_q || !cu_seqlens_k) return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k are required");
+  if (LSE && !lse_stride) return fail(FA_ERR_INVALID_ARG, "lse_stride must not be NULL when LSE is given");
+  if (B <= 0 || max_len_q <= 0 || max_len_q > total_q || H_kv <= 0)
+    return fail(FA_ERR_INVALID_ARG, "need B >= 1, H_kv >= 1 and 1 <= max_len_q <= total_q");
+  // the packed tensors as [1, H, total, d] views: validate them like one problem
+  fa_problem_t pb{};
+  pb.B = 1;
+  pb.H = H;
+  pb.H_kv = H_kv;
+  pb.N_q = total_q;
+  pb.N_k = total_k;
+  pb.d = d;
+  pb.Q = *Q;
+  pb.K = *K;
+  pb.V = *V;
+  pb.O = *O;
+  pb.LSE = LSE;
+  for (int i = 0; i < 3; ++i) pb.lse_stride[i] = LSE ? lse_stride[i] : 0;
+  pb.scale = scale;
+  pb.is_causal = is_causal;
+  Path path;
+  fa_status_t st = validate(dtype, pb, 0, &path);
+  if (st != FA_OK) return st;
+  if (dtype != FA_BF16 || path != Path::kTensorCore)
+    return fail(FA_ERR_UNSUPPORTED, "packed variable-length batches take bf16 with d = 64 or 128");
+  const long long n_qblk = (max_len_q + 255) / 256;
+  if (B * H * n_qblk >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query tiles");
+  DevState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  TcLaunch L;
+  if ((st = make_map(&L.tmQ, pb.Q, false, 1, H, total_q, (int)d, 128, "Q")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, pb.K, false, 1, H_kv, total_k, (int)d, 128, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, pb.V, false, 1, H_kv, total_k, (int)d, 128, "V")) != FA_OK) return st;
+  TcParams& p = L.p;
+  p.B = (int)B;
+  p.H = (int)H;
+  p.N_q = (int)total_q;
+  p.N_k = (int)total_k;
+  p.causal = is_causal == 0 ? kNoCausal : (is_causal == 2 ? kVarlenBottomRight : 0);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.n_qblk = (int)n_qblk;
+  p.n_tiles = (int)(B * H * n_qblk);
+  p.n_split = 1;
+  p.n_units = p.n_tiles;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.head_group = 1;
+  p.kv_group = (int)(H / H_kv);
+  p.O = O->ptr;
+  for (int i = 0; i < 3; ++i) {
+    p.o_stride[i] = O->stride[i];
+    p.lse_stride[i] = LSE ? lse_stride[i] : 0;
+  }
+  p.LSE = LSE;
+  p.err = ds->err;
+  p.timeout_ns = g_timeout_ns.load();
+  p.debug_flags = g_debug_flags.load();
+  L.grid = p.n_units < ds->sm_count ? p.n_units : ds->sm_count;
+  L.device = ds->device;
+  L.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = d == 128 ? launch_tc_bf16_d128_varlen(L) : launch_tc_bf16_d64_varlen(L);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("varlen kernel launch", e));
+  return FA_OK;
+}
+
 fa_status_t fa_axial_block_fwd(int64_t B, int64_t H, int64_t W, int64_t D, int64_t heads, const float* x,
                                const fa_axial_weights_t* row, const fa_axial_weights_t* col, float* out,
                                void* stream) {
@@ -776,6 +847,6 @@ void fa_debug_set(uint64_t timeout_ns, int debug_flags) {
   g_debug_flags.store(debug_flags);
 }
 
-int fa_version(void) { return 101; }
+int fa_version(void) { return 102; }
 
 }  // extern "C"

@@ -35,6 +35,9 @@ cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d64_split(const TcLaunch& L);
+// variable-length variants (bf16; L.p.cu_q / cu_k set, N_q / N_k = packed totals)
+cudaError_t launch_tc_bf16_d128_varlen(const TcLaunch& L);
+cudaError_t launch_tc_bf16_d64_varlen(const TcLaunch& L);
 
 // Backward pass (fa_bwd.cu): preprocess, tensor-core kernel and dQ
 // conversion on one stream.  bf16 only; d = 64 or 128.

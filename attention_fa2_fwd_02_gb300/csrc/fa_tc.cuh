@@ -36,6 +36,9 @@ constexpr float kLn2 = 0.69314718055994531f;
 // TcParams::causal value for "no causal mask" (the field is the mask's offset
 // otherwise; one int keeps the kernel's parameter block at its size)
 constexpr int kNoCausal = 0x7fffffff;
+// packed variable-length batches: bottom-right alignment per sequence (its
+// offset len_k - len_q differs between sequences)
+constexpr int kVarlenBottomRight = 0x7ffffffe;
 
 struct TcParams {
   int B, H, N_q, N_k;
@@ -46,8 +49,14 @@ struct TcParams {
   int n_tiles;            // B * H * n_qblk
   int n_split;            // key-range splits per tile (1 = none)
   int n_units;            // n_tiles * n_split work units
-  float* ws_o;            // split-KV partial outputs, fp32 [n_split][B*H*N_q][D]
-  float* ws_lse;          // split-KV partial LSE (natural log), [n_split][B*H*N_q]
+  union {
+    float* ws_o;          // split-KV: partial outputs, fp32 [n_split][B*H*N_q][D]
+    const int* cu_q;      // varlen: query offsets of the B packed sequences [B+1]
+  };
+  union {
+    float* ws_lse;        // split-KV: partial LSE (natural log), [n_split][B*H*N_q]
+    const int* cu_k;      // varlen: key offsets [B+1]
+  };
   int head_group;         // heads per schedule group (K/V L2 locality)
   int kv_group;           // query heads per K/V head (grouped-query attention; 1 = none)
   void* O;
@@ -59,9 +68,12 @@ struct TcParams {
   int debug_flags;
 };
 
-template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false>
+template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false, bool VARLEN_ = false>
 struct TcCfg {
   using Elem = T;
+  // variable-length instantiation: B packed sequences (offsets cu_q, cu_k;
+  // N_q, N_k = the packed totals), tiles over B x H x ceil(max_len_q / 256)
+  static constexpr bool kVarlen = VARLEN_;
   // split-KV instantiation: work units are key-range parts of a tile and write
   // partial results to the workspace (a separate kernel, so that the plain
   // path compiles without any of it)
@@ -116,6 +128,7 @@ struct TcCfg {
   static_assert(2 * BN + 2 * D <= 512, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(!kVt || NSLOT % 2 == 0, "K and V tiles must alternate ring slots");
+  static_assert(!(kSplit && kVarlen), "split-KV and varlen are separate instantiations");
 };
 
 struct Bars {
@@ -137,7 +150,10 @@ struct Bars {
 };
 
 struct TileInfo {
-  int b, h, hk, q0;      // hk: the K/V head of query head h
+  int b, h, hk, q0;      // hk: the K/V head of query head h; q0: first query row (of the sequence)
+  int qrow0, krow0;      // varlen: packed rows of the sequence's first query and key (0 otherwise)
+  int len_q, len_k;      // varlen: the sequence's lengths
+  int coff;              // varlen: the sequence's causal offset (kNoCausal: none)
   int split;   // key-range split of this work unit
   int j0;      // first key tile of the unit
   int n_kv;    // key tiles of the unit (0: nothing to do)
@@ -152,6 +168,35 @@ struct TileInfo {
 template <class C>
 __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   constexpr int BN = C::BN;
+  if constexpr (C::kVarlen) {
+    // virtual tiles: query-block rank major (last blocks first when causal),
+    // then (b, h); a block past its sequence's end is empty
+    TileInfo ti;
+    const int BH = p.B * p.H;
+    const int qi = u / BH;
+    const int bh = u - qi * BH;
+    const bool causal = p.causal != kNoCausal;
+    ti.b = bh / p.H;
+    ti.h = bh - ti.b * p.H;
+    ti.hk = ti.h / p.kv_group;
+    ti.q0 = (causal ? (p.n_qblk - 1 - qi) : qi) * 256;
+    ti.qrow0 = p.cu_q[ti.b];
+    ti.krow0 = p.cu_k[ti.b];
+    ti.len_q = p.cu_q[ti.b + 1] - ti.qrow0;
+    ti.len_k = p.cu_k[ti.b + 1] - ti.krow0;
+    ti.coff = !causal ? kNoCausal : (p.causal == kVarlenBottomRight ? ti.len_k - ti.len_q : 0);
+    ti.split = 0;
+    ti.j0 = 0;
+    if (ti.q0 >= ti.len_q) {
+      ti.n_kv = 0;
+      return ti;
+    }
+    int kv_end = ti.len_k;
+    if (causal) kv_end = min(kv_end, min(ti.q0 + 256, ti.len_q) + ti.coff);
+    const int n_tot = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+    ti.n_kv = n_tot > 0 ? n_tot : 1;  // rows that see no key take one masked tile
+    return ti;
+  }
   const int t = C::kSplit ? u / p.n_split : u;
   const int split = C::kSplit ? u - t * p.n_split : 0;
   const int BH = p.B * p.H;
@@ -167,6 +212,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   ti.h = bh - ti.b * p.H;
   ti.hk = ti.h / p.kv_group;
   ti.q0 = qb * 256;
+  ti.qrow0 = ti.krow0 = 0;
   ti.split = split;
   int kv_end = p.N_k;
   if (p.causal != kNoCausal) kv_end = min(kv_end, min(ti.q0 + 256, p.N_q) + p.causal);
@@ -217,7 +263,7 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(tmQ, &bars.q_full[stage], dst + pn * C::kQPanelBytes, pn * C::kPanelElems,
-                  ti.q0 + stage * C::BM, ti.h, ti.b, pol_q);
+                  ti.qrow0 + ti.q0 + stage * C::BM, ti.h, C::kVarlen ? 0 : ti.b, pol_q);
     if (stage == 0) ++q_armed0; else ++q_armed1;
     return true;
   };
@@ -234,14 +280,14 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(map, &bars.kv_full[slot], dst + pn * C::kKVPanelBytes, pn * C::kPanelElems,
-                  (ti.j0 + j) * C::BN, ti.hk, ti.b, pol_kv);
+                  ti.krow0 + (ti.j0 + j) * C::BN, ti.hk, C::kVarlen ? 0 : ti.b, pol_kv);
     return true;
   };
 
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
-    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
     const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
     ok = load_q(0, ti) && load_kv(tmK, 0, ti, false) && load_q(1, ti) &&
@@ -331,7 +377,7 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
-    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
     const uint32_t par_k = tile_k & 1u;
     const int n = ti.n_kv;
@@ -412,10 +458,11 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
-    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
     const int q = ti.q0 + stage * C::BM + row;
-    const int vis_end = p.causal != kNoCausal ? min(p.N_k, q + 1 + p.causal) : p.N_k;  // keys < vis_end are visible
+    int vis_end = p.causal != kNoCausal ? min(p.N_k, q + 1 + p.causal) : p.N_k;  // keys < vis_end are visible
+    if constexpr (C::kVarlen) vis_end = ti.coff != kNoCausal ? min(ti.len_k, q + 1 + ti.coff) : ti.len_k;
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < ti.n_kv; ++j) {
       if (!warp_wait(&bars.s_full[stage], s_par, wd, 0x30 + stage)) return;
@@ -628,7 +675,7 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
-    counted = C::kSplit ? (ti.n_kv != 0) : 1u;
+    counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
     if constexpr (C::kVt) {
       // same order as the load warp: Q_0, K_0, Q_1, V_0, then K_j, V_j
@@ -657,9 +704,13 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
       const float2 st = stats[s * C::BM + row];
       mbar_arrive(&bars.st_empty[s]);
       const int q = ti.q0 + s * C::BM + row;
-      const bool valid = q < p.N_q;
-      T* orow = reinterpret_cast<T*>(p.O) + ti.b * p.o_stride[0] + ti.h * p.o_stride[1] +
-                static_cast<long long>(q) * p.o_stride[2];
+      // varlen: rows of this sequence only, stored at their packed index (the
+      // bound on the packed total also keeps bad offsets from writing out of range)
+      const int qo = ti.qrow0 + q;
+      const bool valid = C::kVarlen ? (q < ti.len_q && qo < p.N_q && ti.qrow0 >= 0) : q < p.N_q;
+      const int ob = C::kVarlen ? 0 : ti.b;
+      T* orow = reinterpret_cast<T*>(p.O) + ob * p.o_stride[0] + ti.h * p.o_stride[1] +
+                static_cast<long long>(qo) * p.o_stride[2];
       // split-KV: this unit's normalised partial O (fp32) and LSE go to the
       // workspace; the combine kernel merges the splits into O and LSE
       constexpr bool partial = C::kSplit;
@@ -702,7 +753,7 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
       if (partial && valid)
         p.ws_lse[wrow] = st.y;
       else if (valid && p.LSE)
-        p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
+        p.LSE[ob * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(qo) * p.lse_stride[2]] = st.y;
     }
   }
 }

@@ -14,6 +14,7 @@ axial-attention transcript (B=4, H=W=32, 4 heads of dim 16).
 from __future__ import annotations
 
 import math
+import itertools
 from dataclasses import dataclass
 
 import torch
@@ -32,6 +33,25 @@ def qkv(q_shape, kv_shape, seed: int, dtype=torch.float32):
     return (normal(q_shape, 3 * seed, dtype),
             normal(kv_shape, 3 * seed + 1, dtype),
             normal(kv_shape, 3 * seed + 2, dtype))
+
+
+def packed(lens_q, lens_k, H: int, H_kv: int, d: int, seed: int, dtype=torch.bfloat16):
+    """A packed variable-length batch: q [sum lens_q, H, d], k and v
+    [sum lens_k, H_kv, d] (N(0,1), seeded), and the int32 offsets
+    cu_q = [0, cumsum(lens_q)], cu_k = [0, cumsum(lens_k)] (CPU tensors)."""
+    cu_q = torch.tensor([0] + list(itertools.accumulate(int(n) for n in lens_q)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(int(n) for n in lens_k)), dtype=torch.int32)
+    q, k, v = (normal((int(cu_q[-1]), H, d), 3 * seed, dtype),
+               normal((int(cu_k[-1]), H_kv, d), 3 * seed + 1, dtype),
+               normal((int(cu_k[-1]), H_kv, d), 3 * seed + 2, dtype))
+    return q, k, v, cu_q, cu_k
+
+
+def seq_lengths(n: int, lo: int, hi: int, seed: int):
+    """n sequence lengths drawn uniformly from [lo, hi] with a seeded generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
 
 
 @dataclass(frozen=True)
@@ -192,3 +212,46 @@ class AxialBlockWorkload:
 
 
 AXIAL_BLOCK = AxialBlockWorkload()
+
+
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of self-attention sequences of mixed lengths (a training
+    batch of packed documents): n_seq lengths drawn uniformly from [lo, hi]
+    with a seeded generator, H heads of dim d, bf16, N(0, 1) inputs."""
+    name: str
+    n_seq: int
+    lo: int
+    hi: int
+    H: int
+    d: int
+    causal: bool
+    seed: int
+    H_kv: int = 0
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
+
+    @property
+    def lens(self):
+        return seq_lengths(self.n_seq, self.lo, self.hi, self.seed)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """4 H d L^2 per sequence (two matmuls), halved under the causal mask."""
+        f = sum(4.0 * self.H * self.d * n * n for n in self.lens)
+        return f / 2 if self.causal else f
+
+    def make(self):
+        return packed(self.lens, self.lens, self.H, self.kv_heads, self.d, self.seed, torch.bfloat16)
+
+
+VARLEN = {
+    "varlen_mix": VarlenWorkload("varlen_mix", 16, 512, 8192, 32, 128, False, seed=31),
+    "varlen_mix_causal": VarlenWorkload("varlen_mix_causal", 16, 512, 8192, 32, 128, True, seed=31),
+}

@@ -196,7 +196,15 @@ def whole_job_value(flops_per_step: float, world: int, slowest_ms_per_step: floa
 
 
 def workload_desc(w) -> dict:
-    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload, AxialWorkload
+    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload, AxialWorkload, VarlenWorkload
+    if isinstance(w, VarlenWorkload):
+        lens = w.lens
+        kind = "causal (top-left, per sequence)" if w.causal else "non-causal"
+        return {"workload": f"{w.name}: packed batch of {w.n_seq} sequences, lengths uniform in [{w.lo}, {w.hi}] "
+                            f"(seed {w.seed}; total {sum(lens)} tokens, max {max(lens)}), H={w.H} d={w.d} bf16 "
+                            f"{kind}, scale={w.scale:.6g}",
+                "lengths": lens, "H": w.H, "H_kv": w.kv_heads, "d": w.d, "dtype": "bf16", "causal": w.causal,
+                "scale": w.scale}
     if isinstance(w, AxialBlockWorkload):
         return {"workload": f"axial attention block x[{w.B},{w.H},{w.W},{w.D}] fp32, {w.heads} heads: LayerNorm + "
                             f"QKV + attention + out-projection + residual, row pass then column pass, "
@@ -218,15 +226,17 @@ def workload_desc(w) -> dict:
 def get_workload(name):
     """The workload; names ending in ``_bwd`` time the backward pass of the
     named forward workload (bf16, d = 64 or 128)."""
-    from attention_fa2_fwd_02_gb300.inputs import AXIAL, AXIAL_BLOCK, WORKLOADS
+    from attention_fa2_fwd_02_gb300.inputs import AXIAL, AXIAL_BLOCK, VARLEN, WORKLOADS
+    if name in VARLEN:
+        return VARLEN[name]
     if name == "axial":
         return AXIAL
     if name == "axial_block":
         return AXIAL_BLOCK
     base = name[:-4] if name.endswith("_bwd") else name
     if base not in WORKLOADS:
-        raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)}, axial, "
-                         f"or <bf16 workload>_bwd")
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)}, {sorted(VARLEN)}, "
+                         f"axial, axial_block, or <bf16 workload>_bwd")
     w = WORKLOADS[base]
     if name.endswith("_bwd") and (w.dtype != torch.bfloat16 or w.d not in (64, 128)):
         raise SystemExit(f"{name}: the backward runs on bf16 workloads with d = 64 or 128")
@@ -309,6 +319,32 @@ def oracle_sample(w, Q, K, V, budget_s: float, rows_per_call: int = 512):
     return flops, dt, f"{n_rows} query rows ({rows_per_call}-row blocks of random (b,h) slices)"
 
 
+def varlen_oracle_sample(w, q, k, v, cu, budget_s: float, rows_per_call: int = 512):
+    """The oracle (as it stands) on blocks of query rows of random (sequence,
+    head) pairs of the packed batch until ~budget_s seconds of CPU work;
+    returns (flops, seconds, description)."""
+    import oracle
+    oracle.build()
+    g = np.random.default_rng(0)
+    G = w.H // w.kv_heads
+    flops, n_rows = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = int(g.integers(w.n_seq)), int(g.integers(w.H))
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        n = s1 - s0
+        r0 = int(g.integers(0, max(1, n - rows_per_call + 1)))
+        rows = np.arange(r0, min(n, r0 + rows_per_call))
+        oracle.attention(q[s0:s1, h], k[s0:s1, h // G], v[s0:s1, h // G], w.scale, w.causal, rows=rows)
+        nvis = np.minimum(rows + 1, n) if w.causal else np.full(rows.size, n)
+        flops += float(4.0 * w.d * nvis.sum())
+        n_rows += rows.size
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops, dt, f"{n_rows} query rows ({rows_per_call}-row blocks of random (sequence, head) pairs)"
+
+
 def axial_block_oracle_step(w, x, row, col):
     import oracle
     return oracle.axial_block(x, row, col, w.heads)
@@ -340,6 +376,29 @@ def run_reference(args, w):
             "data": "synthetic", "config": workload_desc(w),
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": "the full block (row + column pass) per step, numpy fp64"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+    from attention_fa2_fwd_02_gb300.inputs import VarlenWorkload
+    if isinstance(w, VarlenWorkload):  # bounded row samples of the packed batch per step
+        q, k, v, cu, _ = w.make()
+        steps, warm = args.steps, max(3, args.warmup)
+        budget = max(0.05, 120.0 / (steps + warm))
+        for _ in range(warm):
+            varlen_oracle_sample(w, q, k, v, cu, budget)
+        tot_f, tot_t, desc = 0.0, 0.0, ""
+        for _ in range(steps):
+            f, dt, desc = varlen_oracle_sample(w, q, k, v, cu, budget)
+            tot_f += f
+            tot_t += dt
+        val = tot_f / tot_t / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": "attention fwd TFLOP/s", "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": tot_t / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(w),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": desc},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
             flush=True)
         return
@@ -514,15 +573,116 @@ def run_axial_block(args, w):
         dist.destroy_process_group()
 
 
+def run_varlen(args, w):
+    """A packed variable-length batch: one fa_fwd_varlen launch per step,
+    tensor-core roofline, end to end with q, k, v and the offsets copied in
+    and O, LSE copied out every step."""
+    import attention_fa2_fwd_02_gb300 as fa
+    world, rank, local, dist = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.build()
+    warm, steps = max(3, args.warmup), max(1, args.steps)
+    qh, kh, vh, cuh, _ = w.make()
+    max_len = max(w.lens)
+    qd, kd, vd, cud = qh.to(dev), kh.to(dev), vh.to(dev), cuh.to(dev)
+    od = torch.empty_like(qd)
+    ld = torch.empty((w.H, qh.shape[0]), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2**20
+    in_bytes = sum(x.numel() * x.element_size() for x in (qd, kd, vd, cud))
+    flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if in_bytes <= l2_bytes else None
+
+    def step():
+        return fa.fwd_varlen(qd, kd, vd, cud, cud, max_len, scale=w.scale, is_causal=w.causal, out=od, lse=ld)
+    for _ in range(warm):
+        step()
+    fa.check()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for k in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    fa.check()
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    step_ms = max_over_ranks(kernel_ms, dist)
+    value = whole_job_value(w.flops, world, step_ms)
+    peaks, peak_src = load_peaks()
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(args.workload), "peak_source": f"bf16_tflops burst (of {peak_src})"}
+    e2e = None
+    if not args.no_e2e:
+        hp = [x.pin_memory() for x in (qh, kh, vh, cuh)]
+        op, lp = torch.empty(qh.shape, dtype=qh.dtype).pin_memory(), torch.empty(ld.shape).pin_memory()
+
+        def e2e_step():
+            for dst, src in zip((qd, kd, vd, cud), hp):
+                dst.copy_(src, non_blocking=True)
+            step()
+            op.copy_(od, non_blocking=True)
+            lp.copy_(ld, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(3, min(steps, 20))
+        a.record(stream)
+        for _ in range(n):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(a.elapsed_time(b) / n, dist)
+        e2e = {"value": whole_job_value(w.flops, world, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": int(in_bytes), "d2h_bytes_per_step": int(od.numel() * 2 + ld.numel() * 4)}
+        fa.check()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        f, dt, desc = varlen_oracle_sample(w, qh, kh, vh, cuh, budget_s=args.cpu_seconds)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{desc}; {dt:.1f} s of fp64 CPU work"}
+    if rank == 0:
+        cfg = workload_desc(w)
+        cfg["l2"] = ("inputs larger than L2: %.0f MB vs %.0f MB" % (in_bytes / 2**20, l2_bytes / 2**20)
+                     if flush is None else "L2 flushed between steps")
+        cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
+        print(json.dumps({
+            "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded i.i.d. N(0,1), seeded lengths)",
+            "config": cfg, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": steps, "kernel_ms": kernel_ms}), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     w = get_workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
         return
-    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload
+    from attention_fa2_fwd_02_gb300.inputs import AxialBlockWorkload, VarlenWorkload
     if isinstance(w, AxialBlockWorkload):
         run_axial_block(args, w)
+        return
+    if isinstance(w, VarlenWorkload):
+        run_varlen(args, w)
         return
     import attention_fa2_fwd_02_gb300 as fa
     from attention_fa2_fwd_02_gb300.inputs import AxialWorkload

@@ -254,6 +254,31 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
                    size_t workspace_bytes, void* stream);
 
 /*
+ * fa_fwd_varlen -- fa_fwd_gqa over B packed sequences of different lengths
+ * (variable-length batch): sequence b has queries at packed rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and keys at cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1, and attends only within itself.
+ *
+ *   cu_seqlens_q, cu_seqlens_k  device int32 arrays of B + 1 non-decreasing
+ *                  offsets starting at 0, ending at total_q / total_k.  They
+ *                  are read on the device: not validated on the host (a row
+ *                  whose packed index falls outside [0, total_q) is not
+ *                  written).  Sequences may be empty.
+ *   total_q, total_k  packed rows (>= 1 each); max_len_q  host upper bound of
+ *                  the query lengths, 1 .. total_q (it sizes the tile grid).
+ *   Q, O           [1, H, total_q, d] views (stride[1] head, stride[2] row),
+ *                  K, V [1, H_kv, total_k, d]; the rules of fa_fwd.
+ *   LSE            [1, H, total_q] (lse_stride[1] head, [2] row), or NULL.
+ *   is_causal      0, 1 (top-left) or 2 (bottom-right), per sequence.
+ * Supported: bf16, d = 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ */
+fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
+                          int64_t max_len_q, int64_t d, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                          int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                          void* stream);
+
+/*
  * fa_axial_block_fwd -- the axial attention block of the axial-attention
  * transcript (its module's forward), fused per sequence, fp32: on x
  * [B, H, W, D] (contiguous), a row pass over the W-long rows and then a

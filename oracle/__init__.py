@@ -147,6 +147,39 @@ def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
     return O.reshape(*lead, n_rows, d), L.reshape(*lead, n_rows)
 
 
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, is_causal=False):
+    """fp64 attention of a packed batch of sequences of different lengths.
+
+    q: [total_q, H, d], k and v: [total_k, H, d]; sequence b holds the packed
+    rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q (and the same for k, v
+    with cu_seqlens_k) and attends to its own keys only: the definition applied
+    to each sequence as its own [H, len, d] problem (the causal alignment, too,
+    is per sequence).  Returns (O [total_q, H, d], LSE [H, total_q]) float64.
+    """
+    q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    if q.ndim != 3 or k.shape != v.shape or k.shape[1:] != q.shape[1:] or len(cq) != len(ck) \
+            or cq[0] != 0 or ck[0] != 0 or cq[-1] != q.shape[0] or ck[-1] != k.shape[0]:
+        raise ValueError("bad packed shapes or offsets")
+    total_q, H, d = q.shape
+    O = np.zeros((total_q, H, d), dtype=np.float64)
+    L = np.full((H, total_q), -np.inf, dtype=np.float64)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 < q0 or k1 < k0:
+            raise ValueError("offsets must not decrease")
+        if q1 == q0:
+            continue
+        if k1 == k0:  # a sequence without keys: every row sees none
+            continue
+        Ob, Lb = attention(q[q0:q1].transpose(1, 0, 2), k[k0:k1].transpose(1, 0, 2),
+                           v[k0:k1].transpose(1, 0, 2), scale, is_causal)
+        O[q0:q1] = Ob.transpose(1, 0, 2)
+        L[:, q0:q1] = Lb
+    return O, L
+
+
 def attention_bwd(Q, K, V, dO, scale: float, is_causal: bool = False, q_rows=None, k_rows=None):
     """fp64 gradients (dQ, dK, dV) of sum(dO * O) for every (batch..., head) slice.
 

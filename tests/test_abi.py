@@ -47,7 +47,7 @@ def test_library_is_built_for_sm103a():
 def test_status_strings(L):
     assert L.fa_status_string(0) == b"ok"
     assert L.fa_status_string(4) == b"device wait timed out"
-    assert L.fa_version() == 101
+    assert L.fa_version() == 102
 
 
 def _t(ptr, strides):
@@ -190,3 +190,30 @@ def test_gqa_heads_must_divide(L):
     st = L.fa_fwd_gqa(fa.FA_BF16, 1, 6, 0, 256, 256, 64, ctypes.byref(t[0]), ctypes.byref(t[1]),
                       ctypes.byref(t[2]), 0.1, 0, ctypes.byref(t[3]), None, ls, None)
     assert st == fa.FA_ERR_INVALID_ARG
+
+
+def _varlen(L, dtype=fa.FA_BF16, B=2, H=4, H_kv=4, total_q=300, total_k=300, max_len=200, d=128,
+            cu_q=0x50000, cu_k=0x60000, causal=0):
+    sq = (total_q * H * d, d, H * d, 1)  # [total, H, d] packed rows seen as [1, H, total, d]
+    sk = (total_k * H_kv * d, d, H_kv * d, 1)
+    t = [_t(0x10000, sq), _t(0x20000, sk), _t(0x30000, sk), _t(0x40000, sq)]
+    ls = (ctypes.c_int64 * 3)(0, total_q, 1)
+    return L.fa_fwd_varlen(dtype, B, H, H_kv, total_q, total_k, max_len, d, ctypes.c_void_p(cu_q),
+                           ctypes.c_void_p(cu_k), ctypes.byref(t[0]), ctypes.byref(t[1]), ctypes.byref(t[2]),
+                           0.1, causal, ctypes.byref(t[3]), None, ls, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cu_q=0), fa.FA_ERR_INVALID_ARG),           # offsets are required
+    (dict(cu_k=0), fa.FA_ERR_INVALID_ARG),
+    (dict(max_len=0), fa.FA_ERR_INVALID_ARG),        # max length >= 1
+    (dict(max_len=301), fa.FA_ERR_INVALID_ARG),      # ... and <= total_q
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(H_kv=3), fa.FA_ERR_INVALID_ARG),           # K/V heads must divide the query heads
+    (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),  # bf16 only
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),             # tensor-core head dims only
+])
+def test_varlen_host_validation(L, kw, status):
+    assert _varlen(L, **kw) == status
+    assert L.fa_last_error() != b""

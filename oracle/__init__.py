@@ -58,13 +58,13 @@ def _load():
     with _lock:
         if _lib is None:
             lib = ctypes.CDLL(str(build()))
-            f = lib.oracle_attention_slice
+            f = lib.oracle_attention_slice_v
             f.restype = ctypes.c_int
             f.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_int64,
-                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_double, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p,
@@ -113,17 +113,20 @@ def _causal_code(is_causal) -> int:
 def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
     """fp64 attention of every (batch..., head) slice.
 
-    Q: [..., N_q, d]; K, V: [..., N_k, d] with the same leading dims.
+    Q: [..., N_q, d]; K: [..., N_k, d]; V: [..., N_k, d_v] with the same
+    leading dims (d_v may differ from d: "Blackwell Attention Example",
+    blackwell_attention).
     rows: optional 1-D sequence of query rows to evaluate in every slice.
-    Returns (O, LSE) as float64 numpy arrays [..., n_rows, d] and [..., n_rows].
+    Returns (O, LSE) as float64 numpy arrays [..., n_rows, d_v] and [..., n_rows].
     """
     Q, K, V = _as_f32(Q), _as_f32(K), _as_f32(V)
-    if Q.ndim < 2 or K.shape != V.shape or Q.shape[:-2] != K.shape[:-2] \
+    if Q.ndim < 2 or K.shape[:-1] != V.shape[:-1] or K.ndim != V.ndim or Q.shape[:-2] != K.shape[:-2] \
             or Q.shape[-1] != K.shape[-1]:
         raise ValueError(f"bad shapes Q{Q.shape} K{K.shape} V{V.shape}")
     lead = Q.shape[:-2]
     N_q, d = Q.shape[-2:]
     N_k = K.shape[-2]
+    d_v = V.shape[-1]
     if rows is None:
         rows_arr = None
         n_rows = N_q
@@ -132,38 +135,38 @@ def attention(Q, K, V, scale: float, is_causal: bool = False, rows=None):
         n_rows = rows_arr.size
     Qs = np.ascontiguousarray(Q.reshape(-1, N_q, d))
     Ks = np.ascontiguousarray(K.reshape(-1, N_k, d))
-    Vs = np.ascontiguousarray(V.reshape(-1, N_k, d))
-    O = np.empty((Qs.shape[0], n_rows, d), dtype=np.float64)
+    Vs = np.ascontiguousarray(V.reshape(-1, N_k, d_v))
+    O = np.empty((Qs.shape[0], n_rows, d_v), dtype=np.float64)
     L = np.empty((Qs.shape[0], n_rows), dtype=np.float64)
     lib = _load()
     rows_ptr = None if rows_arr is None else rows_arr.ctypes.data
     for s in range(Qs.shape[0]):
-        rc = lib.oracle_attention_slice(
-            Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d,
-            N_q, N_k, d, float(scale), _causal_code(is_causal),
+        rc = lib.oracle_attention_slice_v(
+            Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d_v,
+            N_q, N_k, d, d_v, float(scale), _causal_code(is_causal),
             rows_ptr, n_rows, O[s].ctypes.data, L[s].ctypes.data)
         if rc != 0:
-            raise RuntimeError(f"oracle_attention_slice failed with {rc}")
-    return O.reshape(*lead, n_rows, d), L.reshape(*lead, n_rows)
+            raise RuntimeError(f"oracle_attention_slice_v failed with {rc}")
+    return O.reshape(*lead, n_rows, d_v), L.reshape(*lead, n_rows)
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, is_causal=False):
     """fp64 attention of a packed batch of sequences of different lengths.
 
-    q: [total_q, H, d], k and v: [total_k, H, d]; sequence b holds the packed
+    q: [total_q, H, d], k: [total_k, H, d], v: [total_k, H, d_v]; sequence b holds the packed
     rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q (and the same for k, v
     with cu_seqlens_k) and attends to its own keys only: the definition applied
     to each sequence as its own [H, len, d] problem (the causal alignment, too,
-    is per sequence).  Returns (O [total_q, H, d], LSE [H, total_q]) float64.
+    is per sequence).  Returns (O [total_q, H, d_v], LSE [H, total_q]) float64.
     """
     q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
     cq = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
     ck = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
-    if q.ndim != 3 or k.shape != v.shape or k.shape[1:] != q.shape[1:] or len(cq) != len(ck) \
+    if q.ndim != 3 or v.ndim != 3 or k.shape[:2] != v.shape[:2] or k.shape[1:] != q.shape[1:] or len(cq) != len(ck) \
             or cq[0] != 0 or ck[0] != 0 or cq[-1] != q.shape[0] or ck[-1] != k.shape[0]:
         raise ValueError("bad packed shapes or offsets")
     total_q, H, d = q.shape
-    O = np.zeros((total_q, H, d), dtype=np.float64)
+    O = np.zeros((total_q, H, v.shape[2]), dtype=np.float64)
     L = np.full((H, total_q), -np.inf, dtype=np.float64)
     for b in range(len(cq) - 1):
         q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]

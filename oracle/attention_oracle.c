@@ -23,7 +23,9 @@
  *    counted from 0, i.e. top-left alignment when N_q != N_k).
  *  - "Blackwell Attention Example", section "Attention Kernel Implementation",
  *    docstring of blackwell_attention_kernel: Attention(Q,K,V) =
- *    softmax(Q K^T * scale) V with Q [..., seq_q, d] and K, V [..., seq_k, d].
+ *    softmax(Q K^T * scale) V with Q [..., seq_q, d] and K, V [..., seq_k, d];
+ *    the same section's blackwell_attention takes V with a head dim Dv of its
+ *    own (Q and K share d) and returns O with Dv columns.
  *
  * The evaluation is untiled: for each requested query row all visible scores
  * are formed in fp64, their maximum m is taken, and l = sum exp(s - m);
@@ -70,19 +72,20 @@ int oracle_num_threads(void) {
 /*
  * One (batch, head) slice.
  *   Q: N_q rows of d floats, row i at Q + i*q_row_stride (elements).
- *   K, V: N_k rows, row j at K + j*k_row_stride, V + j*v_row_stride.
+ *   K: N_k rows of d floats, row j at K + j*k_row_stride.
+ *   V: N_k rows of d_v floats, row j at V + j*v_row_stride.
  *   rows[0..n_rows): the query rows to evaluate (NULL = all N_q rows in order).
- *   O: n_rows x d doubles, row r at O + r*d.   LSE: n_rows doubles.
+ *   O: n_rows x d_v doubles, row r at O + r*d_v.   LSE: n_rows doubles.
  * Returns 0 on success, -1 on bad arguments, -2 if scratch allocation failed.
  */
-int oracle_attention_slice(const float* Q, int64_t q_row_stride,
-                           const float* K, int64_t k_row_stride,
-                           const float* V, int64_t v_row_stride,
-                           int64_t N_q, int64_t N_k, int64_t d,
-                           double scale, int is_causal,
-                           const int64_t* rows, int64_t n_rows,
-                           double* O, double* LSE) {
-  if (!Q || !K || !V || !O || !LSE || N_q < 0 || N_k <= 0 || d <= 0 || n_rows < 0 ||
+int oracle_attention_slice_v(const float* Q, int64_t q_row_stride,
+                             const float* K, int64_t k_row_stride,
+                             const float* V, int64_t v_row_stride,
+                             int64_t N_q, int64_t N_k, int64_t d, int64_t d_v,
+                             double scale, int is_causal,
+                             const int64_t* rows, int64_t n_rows,
+                             double* O, double* LSE) {
+  if (!Q || !K || !V || !O || !LSE || N_q < 0 || N_k <= 0 || d <= 0 || d_v <= 0 || n_rows < 0 ||
       is_causal < 0 || is_causal > 2)
     return -1;
   if (!rows && n_rows != N_q) return -1;
@@ -99,7 +102,7 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
     for (int64_t r = 0; r < n_rows; ++r) {
       if (!s) continue;
       int64_t i = rows ? rows[r] : r;
-      double* o = O + r * d;
+      double* o = O + r * d_v;
       if (i < 0 || i >= N_q) {
 #pragma omp atomic write
         failed = 1;
@@ -107,7 +110,7 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
       }
       const int64_t n_vis = visible_keys(i, N_q, N_k, is_causal);
       if (n_vis == 0) { /* no visible key: empty sum */
-        for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+        for (int64_t c = 0; c < d_v; ++c) o[c] = 0.0;
         LSE[r] = -INFINITY;
         continue;
       }
@@ -122,19 +125,31 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
         if (s[j] > m) m = s[j];
       }
       double l = 0.0;
-      for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t c = 0; c < d_v; ++c) o[c] = 0.0;
       for (int64_t j = 0; j < n_vis; ++j) {
         double p = exp(s[j] - m);
         const float* v = V + j * v_row_stride;
         l += p;
-        for (int64_t c = 0; c < d; ++c) o[c] += p * (double)v[c];
+        for (int64_t c = 0; c < d_v; ++c) o[c] += p * (double)v[c];
       }
-      for (int64_t c = 0; c < d; ++c) o[c] /= l;
+      for (int64_t c = 0; c < d_v; ++c) o[c] /= l;
       LSE[r] = m + log(l);
     }
     free(s);
   }
   return failed == 1 ? -1 : (failed == 2 ? -2 : 0);
+}
+
+/* oracle_attention_slice_v with V of the same head dim as Q and K. */
+int oracle_attention_slice(const float* Q, int64_t q_row_stride,
+                           const float* K, int64_t k_row_stride,
+                           const float* V, int64_t v_row_stride,
+                           int64_t N_q, int64_t N_k, int64_t d,
+                           double scale, int is_causal,
+                           const int64_t* rows, int64_t n_rows,
+                           double* O, double* LSE) {
+  return oracle_attention_slice_v(Q, q_row_stride, K, k_row_stride, V, v_row_stride, N_q, N_k, d, d, scale,
+                                  is_causal, rows, n_rows, O, LSE);
 }
 
 /*

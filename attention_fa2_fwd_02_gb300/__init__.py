@@ -43,7 +43,8 @@ class FaProblem(ctypes.Structure):
                 ("N_k", ctypes.c_int64), ("d", ctypes.c_int64),
                 ("Q", FaTensor), ("K", FaTensor), ("V", FaTensor), ("O", FaTensor),
                 ("LSE", ctypes.c_void_p), ("lse_stride", ctypes.c_int64 * 3),
-                ("scale", ctypes.c_float), ("is_causal", ctypes.c_int), ("H_kv", ctypes.c_int64)]
+                ("scale", ctypes.c_float), ("is_causal", ctypes.c_int), ("H_kv", ctypes.c_int64),
+                ("Dv", ctypes.c_int64)]
 
 
 class AxialWeights(ctypes.Structure):
@@ -123,7 +124,7 @@ def lib() -> ctypes.CDLL:
                                      [ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_float, ctypes.c_int] +
                                      [P(FaTensor)] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
             L.fa_fwd_varlen.restype = ctypes.c_int
-            L.fa_fwd_varlen.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 7 + [ctypes.c_void_p] * 2 +
+            L.fa_fwd_varlen.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 8 + [ctypes.c_void_p] * 2 +
                                         [P(FaTensor)] * 3 + [ctypes.c_float, ctypes.c_int, P(FaTensor),
                                                              ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p])
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -192,22 +193,25 @@ def _problem(Q, K, V, scale, is_causal, out, lse, with_lse):
         raise ValueError("Q, K, V must be on one device")
     q4, k4, v4 = _as4(Q), _as4(K), _as4(V)
     B, H, N_q, d = q4.shape
-    if k4.shape != v4.shape or k4.shape[0] != B or k4.shape[3] != d or H % k4.shape[1] != 0:
+    if k4.shape[:3] != v4.shape[:3] or k4.shape[0] != B or k4.shape[3] != d or H % k4.shape[1] != 0:
         raise ValueError(f"shape mismatch: Q{tuple(Q.shape)} K{tuple(K.shape)} V{tuple(V.shape)} "
                          "(K/V heads must divide the query heads)")
     N_k = k4.shape[2]
+    d_v = v4.shape[3]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    o_shape = (*Q.shape[:-1], d_v)
     if out is None:
-        out = torch.empty(Q.shape, dtype=Q.dtype, device=Q.device)
+        out = torch.empty(o_shape, dtype=Q.dtype, device=Q.device)
     o4 = _as4(out)
-    if o4.shape != q4.shape or out.dtype != Q.dtype or out.device != Q.device:
-        raise ValueError("out must match Q's shape, dtype and device")
+    if tuple(out.shape) != o_shape or out.dtype != Q.dtype or out.device != Q.device:
+        raise ValueError("out must have Q's leading shape and V's head dim, Q's dtype and device")
     if with_lse and lse is None:
         lse = torch.empty(Q.shape[:-1], dtype=torch.float32, device=Q.device)
     pb = FaProblem()
     pb.B, pb.H, pb.N_q, pb.N_k, pb.d = B, H, N_q, N_k, d
     pb.H_kv = k4.shape[1]
+    pb.Dv = d_v
     pb.Q, pb.K, pb.V, pb.O = _ft(q4), _ft(k4), _ft(v4), _ft(o4)
     if lse is not None:
         if lse.dtype != torch.float32 or lse.device != Q.device or lse.shape != Q.shape[:-1]:
@@ -244,10 +248,12 @@ def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None =
     with torch.cuda.device(Q.device):
         lse_stride = (ctypes.c_int64 * 3)(*pb.lse_stride)
         n_split = 1
-        if pb.d in (64, 128) and pb.H_kv == pb.H:  # (split-KV takes K/V with the query heads)
+        if pb.d in (64, 128) and pb.H_kv == pb.H and pb.Dv == pb.d:  # (split-KV: K/V with the query heads, Dv = d)
             n_split = (L.fa_fwd_splitkv_choose(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.is_causal)
                        if split_kv is None else int(split_kv))
-        if n_split == 1:
+        if pb.Dv != pb.d:  # V with a head dim of its own: the one-problem grouped entry
+            st = L.fa_fwd_grouped(code, 1, ctypes.byref(pb), _stream_ptr(Q.device, stream))
+        elif n_split == 1:
             st = L.fa_fwd_gqa(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
                           ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
                           pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
@@ -287,11 +293,8 @@ def fwd_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: torch.Te
     L = lib()
     code = _dtype_code(Q)
     with torch.cuda.device(Q.device):
-        if pb.H_kv != pb.H:  # grouped K/V heads: the unsplit kernel, which needs no scratch
-            st = L.fa_fwd_gqa(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
-                              ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
-                              pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE,
-                              (ctypes.c_int64 * 3)(*pb.lse_stride), _stream_ptr(Q.device, stream))
+        if pb.H_kv != pb.H or pb.Dv != pb.d:  # grouped K/V heads or Dv != d: the unsplit kernel (no scratch)
+            st = L.fa_fwd_grouped(code, 1, ctypes.byref(pb), _stream_ptr(Q.device, stream))
             _raise_on(st)
             return out, lse
         n_split = 1
@@ -313,18 +316,19 @@ def fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
                with_lse: bool = True, stream=None):
     """Attention over a packed batch of sequences of different lengths.
 
-    q: [total_q, H, d], k and v: [total_k, H_kv, d] (H_kv divides H), bf16,
-    d = 64 or 128, rows of sequence b at cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+    q: [total_q, H, d], k: [total_k, H_kv, d], v: [total_k, H_kv, d_v] (H_kv
+    divides H; d_v may differ from d), bf16, d and d_v multiples of 8 up to
+    128, rows of sequence b at cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
     (and likewise for the keys); the offsets are int32 CUDA tensors of B + 1
     entries from 0 to total.  Each sequence attends only to itself;
     ``is_causal`` (False, True / "top_left", "bottom_right") applies per
     sequence.  ``max_seqlen_q`` bounds the query lengths (it sizes the grid).
-    Returns (out [total_q, H, d], lse [H, total_q] fp32 or None).
+    Returns (out [total_q, H, d_v], lse [H, total_q] fp32 or None).
     """
     if not (q.is_cuda and k.is_cuda and v.is_cuda and cu_seqlens_q.is_cuda and cu_seqlens_k.is_cuda):
         raise ValueError("q, k, v and the offsets must be CUDA tensors (this library has no CPU path)")
-    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or k.shape[2] != q.shape[2]:
-        raise ValueError(f"expected q [total_q, H, d], k/v [total_k, H_kv, d]: "
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape[:2] != v.shape[:2] or k.shape[2] != q.shape[2]:
+        raise ValueError(f"expected q [total_q, H, d], k [total_k, H_kv, d], v [total_k, H_kv, d_v]: "
                          f"{tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
@@ -338,10 +342,11 @@ def fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
     B = cu_seqlens_q.numel() - 1
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    o_shape = (total_q, H, v.shape[2])
     if out is None:
-        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
-    if out.shape != q.shape or out.dtype != q.dtype or out.device != q.device:
-        raise ValueError("out must match q's shape, dtype and device")
+        out = torch.empty(o_shape, dtype=q.dtype, device=q.device)
+    if out.shape != o_shape or out.dtype != q.dtype or out.device != q.device:
+        raise ValueError("out must be [total_q, H, d_v] in q's dtype, on q's device")
     if with_lse and lse is None:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     if lse is not None and (lse.shape != (H, total_q) or lse.dtype != torch.float32 or lse.device != q.device):
@@ -353,7 +358,7 @@ def fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
     lse_stride = (ctypes.c_int64 * 3)(0, *(lse.stride() if lse is not None else (0, 0)))
     L = lib()
     with torch.cuda.device(q.device):
-        st = L.fa_fwd_varlen(_dtype_code(q), B, H, H_kv, total_q, total_k, int(max_seqlen_q), d,
+        st = L.fa_fwd_varlen(_dtype_code(q), B, H, H_kv, total_q, total_k, int(max_seqlen_q), d, v.shape[2],
                              ctypes.c_void_p(cu_seqlens_q.data_ptr()), ctypes.c_void_p(cu_seqlens_k.data_ptr()),
                              ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), float(scale),
                              causal_code(is_causal), ctypes.byref(to),

@@ -106,8 +106,15 @@ enum class Path { kTensorCore, kSmall };
 bool tensor_ok(const fa_tensor_t& t) { return t.ptr != nullptr && t.stride[3] == 1; }
 long long kv_heads(const fa_problem_t& pb) { return pb.H_kv > 0 ? pb.H_kv : pb.H; }
 
-// Validate one problem and choose its kernel.
-fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* path) {
+long long v_dim(const fa_problem_t& pb) { return pb.Dv > 0 ? pb.Dv : pb.d; }
+// Tensor-core tile width for head dims d (Q, K) and dv (V, O): 64 or 128
+// columns; columns past d or dv are loaded as zeros.
+int tc_tile_dim(long long d, long long dv) { return (d > 64 || dv > 64) ? 128 : 64; }
+
+// Validate one problem and choose its kernel (tensor_core_only: never the
+// small-head path).
+fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* path,
+                     bool tensor_core_only = false) {
   const std::string at = "problem " + std::to_string(idx) + ": ";
   if (dtype != FA_BF16 && dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, at + "unknown dtype");
   if (pb.B <= 0 || pb.H <= 0 || pb.N_q <= 0 || pb.N_k <= 0 || pb.d <= 0)
@@ -127,15 +134,19 @@ fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* pa
       if (t->stride[i] < 0) return fail(FA_ERR_UNSUPPORTED, at + "negative strides are not supported");
   if (pb.N_q >= (1ll << 31) || pb.N_k >= (1ll << 31) || pb.B >= (1ll << 31) || pb.H >= (1ll << 31))
     return fail(FA_ERR_UNSUPPORTED, at + "sizes must be below 2^31");
-  if (pb.d == 16 || pb.d == 32) {
+  if (pb.Dv < 0) return fail(FA_ERR_INVALID_ARG, at + "Dv must be >= 0 (0 = d)");
+  const long long dv = v_dim(pb);
+  if ((pb.d == 16 || pb.d == 32) && dv == pb.d && !tensor_core_only) {
     const long long items = pb.B * pb.H * ((pb.N_q + 31) / 32);
     if (items >= (1ll << 40)) return fail(FA_ERR_UNSUPPORTED, at + "too many query blocks");
     *path = Path::kSmall;
     return FA_OK;
   }
-  if (pb.d != 64 && pb.d != 128)
-    return fail(FA_ERR_UNSUPPORTED, at + "head dim " + std::to_string(pb.d) + " not supported (16, 32, 64, 128)");
   const long long E = dtype == FA_FP32 ? 4 : 2;
+  if (pb.d > 128 || dv > 128 || (pb.d * E) % 16 != 0 || (dv * E) % 16 != 0)
+    return fail(FA_ERR_UNSUPPORTED, at + "head dims d = " + std::to_string(pb.d) + ", Dv = " + std::to_string(dv) +
+                                        " not supported (up to 128, rows of a multiple of 16 bytes; or d = Dv in "
+                                        "{16, 32} on the small-head path)");
   for (auto* t : ts) {
     if (reinterpret_cast<uintptr_t>(t->ptr) % 16 != 0)
       return fail(FA_ERR_UNSUPPORTED, at + "tensor-core path needs 16-byte aligned base pointers");
@@ -192,13 +203,16 @@ SplitWs split_ws_layout(void* ws, long long B, long long H, long long N_q, long 
 fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const DevState& ds, cudaStream_t stream,
                                int n_split = 1, SplitWs ws = SplitWs{}) {
   const bool fp32 = dtype == FA_FP32;
-  const int d = static_cast<int>(pb.d);
+  const int dv = static_cast<int>(v_dim(pb));
+  const int d = tc_tile_dim(pb.d, dv);  // the kernel's tile width
+  if (n_split > 1 && (pb.d != d || dv != d))
+    return fail(FA_ERR_UNSUPPORTED, "split-KV needs d = Dv in {64, 128}");
   const int bn = tc_key_tile(fp32, d);
   TcLaunch L;
   fa_status_t st;
-  if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, d, 128, "Q")) != FA_OK) return st;
-  if ((st = make_map(&L.tmK, pb.K, fp32, pb.B, kv_heads(pb), pb.N_k, d, bn, "K")) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, kv_heads(pb), pb.N_k, d, bn, "V")) != FA_OK) return st;
+  if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, pb.d, 128, "Q")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, pb.K, fp32, pb.B, kv_heads(pb), pb.N_k, pb.d, bn, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, kv_heads(pb), pb.N_k, dv, bn, "V")) != FA_OK) return st;
   TcParams& p = L.p;
   p.B = (int)pb.B;
   p.H = (int)pb.H;
@@ -208,12 +222,15 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   p.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
   p.n_qblk = (int)((pb.N_q + 255) / 256);
   p.n_tiles = (int)(pb.B * pb.H * p.n_qblk);
-  p.n_split = n_split;
+  if (n_split > 1)
+    p.n_split = n_split;
+  else
+    p.dv = dv;
   p.n_units = p.n_tiles * n_split;
   p.ws_o = ws.o;
   p.ws_lse = ws.lse;
   // Heads per schedule group: keep the K/V of a group within ~48 MB of L2.
-  const long long kv_bytes = 2ll * pb.N_k * pb.d * (fp32 ? 4 : 2);
+  const long long kv_bytes = pb.N_k * (pb.d + dv) * (fp32 ? 4 : 2);
   long long g = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
   if (g < 1) g = 1;
   if (g > pb.B * pb.H) g = pb.B * pb.H;
@@ -530,7 +547,8 @@ fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, 
   Path path;
   fa_status_t st = validate(dtype, pb, 0, &path);
   if (st != FA_OK) return st;
-  if (path != Path::kTensorCore) return fail(FA_ERR_UNSUPPORTED, "split-KV needs the tensor-core path (d = 64, 128)");
+  if (path != Path::kTensorCore || (d != 64 && d != 128))
+    return fail(FA_ERR_UNSUPPORTED, "split-KV needs the tensor-core path with d = 64 or 128");
   if (B * H * ((N_q + 255) / 256) * n_split >= (1ll << 31))
     return fail(FA_ERR_UNSUPPORTED, "too many split-KV work units");
   if (!workspace) return fail(FA_ERR_INVALID_ARG, "split-KV needs a workspace");
@@ -679,7 +697,8 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
 }
 
 fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
-                          int64_t max_len_q, int64_t d, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int64_t max_len_q, int64_t d, int64_t d_v, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k,
                           const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
                           int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
                           void* stream) {
@@ -696,6 +715,7 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   pb.N_q = total_q;
   pb.N_k = total_k;
   pb.d = d;
+  pb.Dv = d_v;
   pb.Q = *Q;
   pb.K = *K;
   pb.V = *V;
@@ -705,18 +725,19 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   pb.scale = scale;
   pb.is_causal = is_causal;
   Path path;
-  fa_status_t st = validate(dtype, pb, 0, &path);
+  fa_status_t st = validate(dtype, pb, 0, &path, /*tensor_core_only=*/true);
   if (st != FA_OK) return st;
-  if (dtype != FA_BF16 || path != Path::kTensorCore)
-    return fail(FA_ERR_UNSUPPORTED, "packed variable-length batches take bf16 with d = 64 or 128");
+  if (dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "packed variable-length batches take bf16");
+  const int dv = static_cast<int>(v_dim(pb));
+  const int D = tc_tile_dim(d, dv);
   const long long n_qblk = (max_len_q + 255) / 256;
   if (B * H * n_qblk >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query tiles");
   DevState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
   TcLaunch L;
-  if ((st = make_map(&L.tmQ, pb.Q, false, 1, H, total_q, (int)d, 128, "Q")) != FA_OK) return st;
-  if ((st = make_map(&L.tmK, pb.K, false, 1, H_kv, total_k, (int)d, 128, "K")) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, pb.V, false, 1, H_kv, total_k, (int)d, 128, "V")) != FA_OK) return st;
+  if ((st = make_map(&L.tmQ, pb.Q, false, 1, H, total_q, d, 128, "Q")) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, pb.K, false, 1, H_kv, total_k, d, 128, "K")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, pb.V, false, 1, H_kv, total_k, dv, 128, "V")) != FA_OK) return st;
   TcParams& p = L.p;
   p.B = (int)B;
   p.H = (int)H;
@@ -726,7 +747,7 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.n_qblk = (int)n_qblk;
   p.n_tiles = (int)(B * H * n_qblk);
-  p.n_split = 1;
+  p.dv = dv;
   p.n_units = p.n_tiles;
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
@@ -744,7 +765,7 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   L.grid = p.n_units < ds->sm_count ? p.n_units : ds->sm_count;
   L.device = ds->device;
   L.stream = static_cast<cudaStream_t>(stream);
-  cudaError_t e = d == 128 ? launch_tc_bf16_d128_varlen(L) : launch_tc_bf16_d64_varlen(L);
+  cudaError_t e = D == 128 ? launch_tc_bf16_d128_varlen(L) : launch_tc_bf16_d64_varlen(L);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("varlen kernel launch", e));
   return FA_OK;
 }
@@ -847,6 +868,6 @@ void fa_debug_set(uint64_t timeout_ns, int debug_flags) {
   g_debug_flags.store(debug_flags);
 }
 
-int fa_version(void) { return 102; }
+int fa_version(void) { return 103; }
 
 }  // extern "C"

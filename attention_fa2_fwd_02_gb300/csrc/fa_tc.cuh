@@ -47,7 +47,11 @@ struct TcParams {
   float scale_log2;       // scale * log2(e)
   int n_qblk;             // ceil(N_q / 256)
   int n_tiles;            // B * H * n_qblk
-  int n_split;            // key-range splits per tile (1 = none)
+  union {
+    int n_split;          // split-KV instantiations: key-range splits per tile
+    int dv;               // the others: output columns written (V's head dim, <= D; the
+                          // columns of Q, K, V past their extents load as zeros)
+  };
   int n_units;            // n_tiles * n_split work units
   union {
     float* ws_o;          // split-KV: partial outputs, fp32 [n_split][B*H*N_q][D]
@@ -716,8 +720,9 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
       constexpr bool partial = C::kSplit;
       const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
       const uint32_t tO = tmem + lane_base + C::col_o(s);
+      const int dv = C::kSplit ? C::D : p.dv;  // columns of O to store
 #pragma unroll 1
-      for (int c = 0; c < C::D; c += 32) {
+      for (int c = 0; c < dv; c += 32) {
         uint32_t o[32];
         tmem_ld32(tO + c, o);
         tmem_ld_wait32(o);
@@ -732,12 +737,14 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
             float4* dst = reinterpret_cast<float4*>(orow + c);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
-                                   __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
+              if (c + 4 * k < dv)
+                dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
+                                     __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+              if (c + 8 * k >= dv) break;
               uint4 w;
               w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * st.x, __uint_as_float(o[8 * k + 1]) * st.x);
               w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * st.x, __uint_as_float(o[8 * k + 3]) * st.x);

@@ -39,7 +39,7 @@ def _fwd_op(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
 
 @_fwd_op.register_fake
 def _(q, k, v, scale, is_causal):
-    return torch.empty_like(q), q.new_empty(q.shape[:-1], dtype=torch.float32)
+    return q.new_empty((*q.shape[:-1], v.shape[-1])), q.new_empty(q.shape[:-1], dtype=torch.float32)
 
 
 @torch.library.custom_op("fa_gb300::bwd", mutates_args=())
@@ -76,17 +76,18 @@ def scaled_dot_product_attention(query: torch.Tensor, key: torch.Tensor, value: 
                                  enable_gqa: bool = False) -> torch.Tensor:
     """``torch.nn.functional.scaled_dot_product_attention`` on this library.
 
-    query [..., H, N_q, d], key / value [..., H_kv, N_k, d] (H_kv = H unless
-    ``enable_gqa``, then H_kv must divide H).  The causal mask is the top-left
-    one, as in PyTorch.  bf16 or fp32; the head dims and layouts fa_fwd
-    supports (the backward: bf16, d = 64 or 128).
+    query [..., H, N_q, d], key [..., H_kv, N_k, d], value [..., H_kv, N_k, d_v]
+    (H_kv = H unless ``enable_gqa``, then H_kv must divide H; d_v may differ
+    from d, as in PyTorch).  The causal mask is the top-left one, as in
+    PyTorch.  bf16 or fp32; the head dims and layouts fa_fwd supports (the
+    backward: bf16, d = d_v = 64 or 128).
     """
     if attn_mask is not None:
         raise NotImplementedError("attn_mask is not supported (only is_causal)")
     if dropout_p != 0.0:
         raise NotImplementedError("dropout is not supported")
-    if query.dim() < 2 or key.dim() != query.dim() or value.shape != key.shape:
-        raise ValueError("query, key, value must share their rank; key and value their shape")
+    if query.dim() < 2 or key.dim() != query.dim() or value.dim() != key.dim() or value.shape[:-1] != key.shape[:-1]:
+        raise ValueError("query, key, value must share their rank; key and value all but their last dim")
     if query.dim() >= 3 and key.shape[-3] != query.shape[-3] and not enable_gqa:
         raise ValueError("query and key/value head counts differ: pass enable_gqa=True")
     if scale is None:

@@ -82,11 +82,15 @@ typedef struct {
  *                  or NULL to skip it (lse_stride is then ignored).
  *   stream         cudaStream_t to launch on.
  *
- * Supported: d in {64, 128} on the tensor-core path (bf16 or fp32), which also
- * needs 16-byte aligned Q/K/V/O base pointers and strides[0..2] * element size
- * that are multiples of 16 bytes (FA_ERR_UNSUPPORTED otherwise); d in {16, 32}
- * on the small-head path (any alignment, N_k <= 1024).  Any N_q, N_k >= 1: the
- * tail of a tile is masked, not required to divide.
+ * Supported: d in {16, 32} on the small-head path (any alignment); any other
+ * d up to 128 that makes a row a multiple of 16 bytes (d % 8 == 0 in bf16,
+ * d % 4 == 0 in fp32) on the tensor-core path, which also needs 16-byte
+ * aligned Q/K/V/O base pointers and strides[0..2] * element size that are
+ * multiples of 16 bytes (FA_ERR_UNSUPPORTED otherwise).  The tensor-core tiles
+ * have 64 or 128 columns: a smaller d is computed on tiles whose extra columns
+ * are loaded as zeros (exact: they add nothing to Q.K and give O columns that
+ * are not stored), so d = 96 costs the tensor work of d = 128.  Any N_q, N_k
+ * >= 1: the tail of a tile is masked, not required to divide.
  */
 fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k,
                    int64_t d, const fa_tensor_t* Q, const fa_tensor_t* K,
@@ -105,7 +109,12 @@ fa_status_t fa_fwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
                        int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* stream);
 
 /* One problem of a grouped call: the arguments of fa_fwd_gqa, by value.
- * H_kv = 0 means H_kv = H (K and V have the query heads). */
+ * H_kv = 0 means H_kv = H (K and V have the query heads).
+ * Dv: head dim of V and O when it differs from d ("Blackwell Attention
+ * Example", blackwell_attention: Q and K share d, V and O have Dv columns);
+ * 0 means Dv = d.  V is then [B, H_kv, N_k, Dv] and O [B, H, N_q, Dv].  A
+ * problem with Dv != d takes the tensor-core path (Dv <= 128, a multiple of
+ * 16 bytes like d); fa_fwd_grouped with one problem is the entry point for it. */
 typedef struct {
   int64_t B, H, N_q, N_k, d;
   fa_tensor_t Q, K, V, O;
@@ -114,6 +123,7 @@ typedef struct {
   float scale;
   int is_causal;
   int64_t H_kv;
+  int64_t Dv;
 } fa_problem_t;
 
 /*
@@ -266,14 +276,18 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
  *                  written).  Sequences may be empty.
  *   total_q, total_k  packed rows (>= 1 each); max_len_q  host upper bound of
  *                  the query lengths, 1 .. total_q (it sizes the tile grid).
- *   Q, O           [1, H, total_q, d] views (stride[1] head, stride[2] row),
- *                  K, V [1, H_kv, total_k, d]; the rules of fa_fwd.
+ *   d, d_v         head dims of Q, K and of V, O (d_v = 0 means d_v = d).
+ *   Q              [1, H, total_q, d] view (stride[1] head, stride[2] row),
+ *                  K [1, H_kv, total_k, d], V [1, H_kv, total_k, d_v],
+ *                  O [1, H, total_q, d_v]; the rules of fa_fwd.
  *   LSE            [1, H, total_q] (lse_stride[1] head, [2] row), or NULL.
  *   is_causal      0, 1 (top-left) or 2 (bottom-right), per sequence.
- * Supported: bf16, d = 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ * Supported: bf16, d and d_v multiples of 8 up to 128, always on the
+ * tensor-core path (FA_ERR_UNSUPPORTED otherwise).
  */
 fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t total_q, int64_t total_k,
-                          int64_t max_len_q, int64_t d, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int64_t max_len_q, int64_t d, int64_t d_v, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k,
                           const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
                           int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
                           void* stream);

@@ -47,7 +47,7 @@ def test_library_is_built_for_sm103a():
 def test_status_strings(L):
     assert L.fa_status_string(0) == b"ok"
     assert L.fa_status_string(4) == b"device wait timed out"
-    assert L.fa_version() == 102
+    assert L.fa_version() == 103
 
 
 def _t(ptr, strides):
@@ -77,7 +77,8 @@ def _call(L, dtype=fa.FA_BF16, B=1, H=1, Nq=256, Nk=256, d=128, qptr=0x10000, st
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(causal=3), fa.FA_ERR_INVALID_ARG),   # 0, 1 (top-left), 2 (bottom-right)
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
-    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=100), fa.FA_ERR_UNSUPPORTED),   # a row of 200 bytes: not a multiple of 16
+    (dict(d=136), fa.FA_ERR_UNSUPPORTED),   # above the 128-column tile
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),
     (dict(qptr=0x10002), fa.FA_ERR_UNSUPPORTED),                     # misaligned base
     (dict(strides=(256 * 128, 256 * 128, 129, 1)), fa.FA_ERR_UNSUPPORTED),  # odd row stride
@@ -198,7 +199,7 @@ def _varlen(L, dtype=fa.FA_BF16, B=2, H=4, H_kv=4, total_q=300, total_k=300, max
     sk = (total_k * H_kv * d, d, H_kv * d, 1)
     t = [_t(0x10000, sq), _t(0x20000, sk), _t(0x30000, sk), _t(0x40000, sq)]
     ls = (ctypes.c_int64 * 3)(0, total_q, 1)
-    return L.fa_fwd_varlen(dtype, B, H, H_kv, total_q, total_k, max_len, d, ctypes.c_void_p(cu_q),
+    return L.fa_fwd_varlen(dtype, B, H, H_kv, total_q, total_k, max_len, d, 0, ctypes.c_void_p(cu_q),
                            ctypes.c_void_p(cu_k), ctypes.byref(t[0]), ctypes.byref(t[1]), ctypes.byref(t[2]),
                            0.1, causal, ctypes.byref(t[3]), None, ls, None)
 
@@ -212,7 +213,7 @@ def _varlen(L, dtype=fa.FA_BF16, B=2, H=4, H_kv=4, total_q=300, total_k=300, max
     (dict(causal=3), fa.FA_ERR_INVALID_ARG),
     (dict(H_kv=3), fa.FA_ERR_INVALID_ARG),           # K/V heads must divide the query heads
     (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),  # bf16 only
-    (dict(d=32), fa.FA_ERR_UNSUPPORTED),             # tensor-core head dims only
+    (dict(d=36), fa.FA_ERR_UNSUPPORTED),             # rows of a multiple of 16 bytes only
 ])
 def test_varlen_host_validation(L, kw, status):
     assert _varlen(L, **kw) == status

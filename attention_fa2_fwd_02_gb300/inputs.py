@@ -68,15 +68,21 @@ class Workload:
     scale: float
     seed: int
     H_kv: int = 0  # K/V heads (grouped-query attention); 0 = H
+    Dv: int = 0    # head dim of V and O; 0 = d
 
     @property
     def kv_heads(self) -> int:
         return self.H_kv or self.H
 
     @property
+    def v_dim(self) -> int:
+        return self.Dv or self.d
+
+    @property
     def flops(self) -> float:
-        """4 * B * H * N_q * N_k * d, halved for causal attention."""
-        f = 4.0 * self.B * self.H * self.N_q * self.N_k * self.d
+        """2 * B * H * N_q * N_k * (d + Dv) (Q K^T and P V; 4 B H N_q N_k d
+        when Dv = d), halved for causal attention."""
+        f = 2.0 * self.B * self.H * self.N_q * self.N_k * (self.d + self.v_dim)
         return f / 2 if self.causal else f
 
     @property
@@ -88,19 +94,22 @@ class Workload:
         """Q, K, V read once; O written once (input dtype); LSE written (fp32)."""
         e = self.elem_bytes
         q = self.B * self.H * self.N_q * self.d * e
-        kv = 2 * self.B * self.kv_heads * self.N_k * self.d * e
-        o = q
+        kv = self.B * self.kv_heads * self.N_k * (self.d + self.v_dim) * e
+        o = self.B * self.H * self.N_q * self.v_dim * e
         lse = self.B * self.H * self.N_q * 4
         return float(q + kv + o + lse)
 
     def make(self):
-        return qkv((self.B, self.H, self.N_q, self.d),
-                   (self.B, self.kv_heads, self.N_k, self.d), self.seed, self.dtype)
+        Q, K, V = qkv((self.B, self.H, self.N_q, self.d),
+                      (self.B, self.kv_heads, self.N_k, self.d), self.seed, self.dtype)
+        if self.v_dim != self.d:
+            V = normal((self.B, self.kv_heads, self.N_k, self.v_dim), 3 * self.seed + 2, self.dtype)
+        return Q, K, V
 
 
-def _w(name, B, H, Nq, Nk, d, dtype, causal, scale=None, seed=0, H_kv=0):
+def _w(name, B, H, Nq, Nk, d, dtype, causal, scale=None, seed=0, H_kv=0, Dv=0):
     return Workload(name, B, H, Nq, Nk, d, dtype, causal,
-                    1.0 / math.sqrt(d) if scale is None else scale, seed, H_kv)
+                    1.0 / math.sqrt(d) if scale is None else scale, seed, H_kv, Dv)
 
 
 # The five configurations (non-causal and causal variants where both are run).
@@ -116,6 +125,11 @@ WORKLOADS = {
     # grouped-query attention: the large self-attention shape with 8 K/V heads
     "large_gqa_nc": _w("large_gqa_nc", 4, 32, 8192, 8192, 128, torch.bfloat16, False, seed=9, H_kv=8),
     "large_gqa_causal": _w("large_gqa_causal", 4, 32, 8192, 8192, 128, torch.bfloat16, True, seed=9, H_kv=8),
+    # other head dims: d = 96 (computed on 128-column tiles), and V with 64
+    # columns against d = 128
+    "large_d96_nc": _w("large_d96_nc", 4, 32, 8192, 8192, 96, torch.bfloat16, False, seed=10),
+    "large_d96_causal": _w("large_d96_causal", 4, 32, 8192, 8192, 96, torch.bfloat16, True, seed=10),
+    "large_dv64_nc": _w("large_dv64_nc", 4, 32, 8192, 8192, 128, torch.bfloat16, False, seed=11, Dv=64),
     # profiling-size cases of the same kernels: inputs still larger than the
     # 129 MB L2, but small enough for a many-pass ncu capture
     "prof_nc": _w("prof_nc", 1, 32, 8192, 8192, 128, torch.bfloat16, False, seed=7),

@@ -217,10 +217,11 @@ def workload_desc(w) -> dict:
     kind = "causal" if w.causal else "non-causal"
     dt = "bf16" if w.dtype == torch.bfloat16 else "fp32"
     gqa = f" H_kv={w.kv_heads}" if w.kv_heads != w.H else ""
-    return {"workload": f"{w.name}: B={w.B} H={w.H}{gqa} N_q={w.N_q} N_k={w.N_k} d={w.d} {dt} {kind}, "
+    dv = f" Dv={w.v_dim}" if w.v_dim != w.d else ""
+    return {"workload": f"{w.name}: B={w.B} H={w.H}{gqa} N_q={w.N_q} N_k={w.N_k} d={w.d}{dv} {dt} {kind}, "
                         f"scale={w.scale:.6g}",
-            "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N_q": w.N_q, "N_k": w.N_k, "d": w.d, "dtype": dt,
-            "causal": w.causal, "scale": w.scale}
+            "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N_q": w.N_q, "N_k": w.N_k, "d": w.d, "Dv": w.v_dim,
+            "dtype": dt, "causal": w.causal, "scale": w.scale}
 
 
 def get_workload(name):
@@ -311,7 +312,7 @@ def oracle_sample(w, Q, K, V, budget_s: float, rows_per_call: int = 512):
         hk = h // (w.H // w.kv_heads)  # the K/V head of query head h
         oracle.attention(Q[b, h], K[b, hk], V[b, hk], w.scale, w.causal, rows=rows)
         nvis = np.minimum(rows + 1, w.N_k) if w.causal else np.full(rows.size, w.N_k)
-        flops += float(4.0 * w.d * nvis.sum())
+        flops += float(2.0 * (w.d + w.v_dim) * nvis.sum())
         n_rows += rows.size
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -440,7 +441,7 @@ def run_reference(args, w):
             oracle_sample(w, Q, K, V, budget_s=0.0)
         step_flops = w.flops
     else:
-        rows = max(1, min(w.N_q, int(rate * per_step_s / (4.0 * w.d * w.N_k))))
+        rows = max(1, min(w.N_q, int(rate * per_step_s / (2.0 * (w.d + w.v_dim) * w.N_k))))
         g = np.random.default_rng(1)
         sample_desc = f"{rows} query rows of one random (b,h) slice per step"
         def step():
@@ -448,7 +449,7 @@ def run_reference(args, w):
             hk = h // (w.H // w.kv_heads)
             oracle.attention(Q[b, h], K[b, hk], V[b, hk], w.scale, w.causal, rows=np.arange(rows))
         nvis = np.minimum(np.arange(rows) + 1, w.N_k) if w.causal else np.full(rows, w.N_k)
-        step_flops = float(4.0 * w.d * nvis.sum())
+        step_flops = float(2.0 * (w.d + w.v_dim) * nvis.sum())
     for _ in range(warm):
         step()
     t0 = time.perf_counter()
@@ -725,10 +726,10 @@ def main():
         def step():
             return fa.axial(Qd, Kd, Vd, scale=w.scale, with_lse=True)
     else:
-        Od = torch.empty_like(Qd)
+        Od = torch.empty((*Qd.shape[:-1], Vd.shape[-1]), dtype=Qd.dtype, device=dev)
         Ld = torch.empty(Qd.shape[:-1], dtype=torch.float32, device=dev)
         code = fa.FA_BF16 if w.dtype == torch.bfloat16 else fa.FA_FP32
-        if w.d in (64, 128) and w.kv_heads == w.H:  # (split-KV takes K/V with the query heads)
+        if w.d in (64, 128) and w.kv_heads == w.H and w.v_dim == w.d:  # (split-KV: K/V with the query heads, Dv = d)
             n_split = fa.lib().fa_fwd_splitkv_choose(code, w.B, w.H, w.N_q, w.N_k, w.d, int(w.causal))
         ws = None
         if n_split > 1:  # the split path's scratch, allocated once outside the timed region
@@ -743,7 +744,7 @@ def main():
             import torch.nn.functional as F
             from attention_fa2_fwd_02_gb300 import sdpa
             n_split = fa.lib().fa_fwd_splitkv_choose(code, w.B, w.H, w.N_q, w.N_k, w.d, int(w.causal)) \
-                if (w.d in (64, 128) and w.kv_heads == w.H) else 1
+                if (w.d in (64, 128) and w.kv_heads == w.H and w.v_dim == w.d) else 1
 
             def step():
                 with sdpa.routed():
@@ -828,6 +829,10 @@ def main():
                 "frac": achieved / peak, "traffic": traffic, "peak_source": note}
         if n_split > 1:  # the events bracket both launches of a split step
             roof["timed"] = f"split-KV attention kernel (n_split={n_split}) + merge kernel"
+        tile = 128 if max(w.d, w.v_dim) > 64 else 64
+        if not axial and not bwd and (w.d != tile or w.v_dim != tile) and w.d not in (16, 32):
+            roof["tile_columns"] = (f"d={w.d}, Dv={w.v_dim} run on {tile}-column tiles: the tensor work is "
+                                    f"{2 * tile / (w.d + w.v_dim):.3f}x the FLOPs counted")
         if bwd:  # the events bracket the three launches of a backward step
             roof["timed"] = "backward preprocess + tensor-core backward kernel + dQ conversion"
 
@@ -869,7 +874,7 @@ def main():
         fa.check()
     elif not args.no_e2e:
         Qp, Kp, Vp = (x.pin_memory() for x in (Qh, Kh, Vh))
-        Op = torch.empty(Qh.shape, dtype=Qh.dtype).pin_memory()
+        Op = torch.empty((*Qh.shape[:-1], Vh.shape[-1]), dtype=Qh.dtype).pin_memory()
         Lp = torch.empty(Qh.shape[:-1], dtype=torch.float32).pin_memory()
         if axial:
             Op2 = torch.empty_like(Op)

@@ -107,9 +107,12 @@ bool tensor_ok(const fa_tensor_t& t) { return t.ptr != nullptr && t.stride[3] ==
 long long kv_heads(const fa_problem_t& pb) { return pb.H_kv > 0 ? pb.H_kv : pb.H; }
 
 long long v_dim(const fa_problem_t& pb) { return pb.Dv > 0 ? pb.Dv : pb.d; }
-// Tensor-core tile width for head dims d (Q, K) and dv (V, O): 64 or 128
-// columns; columns past d or dv are loaded as zeros.
-int tc_tile_dim(long long d, long long dv) { return (d > 64 || dv > 64) ? 128 : 64; }
+// Tensor-core tile width for head dims d (Q, K) and dv (V, O): 64, 128 or
+// 256 columns (256: the bf16 kernel for head dims above 128); columns past d
+// or dv are loaded as zeros.
+int tc_tile_dim(long long d, long long dv) {
+  return (d > 128 || dv > 128) ? 256 : ((d > 64 || dv > 64) ? 128 : 64);
+}
 
 // Validate one problem and choose its kernel (tensor_core_only: never the
 // small-head path).
@@ -143,10 +146,11 @@ fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* pa
     return FA_OK;
   }
   const long long E = dtype == FA_FP32 ? 4 : 2;
-  if (pb.d > 128 || dv > 128 || (pb.d * E) % 16 != 0 || (dv * E) % 16 != 0)
+  const long long max_dim = dtype == FA_FP32 ? 128 : 256;
+  if (pb.d > max_dim || dv > max_dim || (pb.d * E) % 16 != 0 || (dv * E) % 16 != 0)
     return fail(FA_ERR_UNSUPPORTED, at + "head dims d = " + std::to_string(pb.d) + ", Dv = " + std::to_string(dv) +
-                                        " not supported (up to 128, rows of a multiple of 16 bytes; or d = Dv in "
-                                        "{16, 32} on the small-head path)");
+                                        " not supported (up to 256 in bf16, 128 in fp32, rows of a multiple of 16 "
+                                        "bytes; or d = Dv in {16, 32} on the small-head path)");
   for (auto* t : ts) {
     if (reinterpret_cast<uintptr_t>(t->ptr) % 16 != 0)
       return fail(FA_ERR_UNSUPPORTED, at + "tensor-core path needs 16-byte aligned base pointers");
@@ -154,7 +158,7 @@ fa_status_t validate(fa_dtype_t dtype, const fa_problem_t& pb, int idx, Path* pa
       if ((t->stride[i] * E) % 16 != 0)
         return fail(FA_ERR_UNSUPPORTED, at + "tensor-core path needs strides that are multiples of 16 bytes");
   }
-  const long long tiles = pb.B * pb.H * ((pb.N_q + 255) / 256);
+  const long long tiles = pb.B * pb.H * ((pb.N_q + 127) / 128);  // (128-row tiles of the wide kernel)
   if (tiles >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, at + "too many query tiles");
   *path = Path::kTensorCore;
   return FA_OK;
@@ -205,9 +209,11 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   const bool fp32 = dtype == FA_FP32;
   const int dv = static_cast<int>(v_dim(pb));
   const int d = tc_tile_dim(pb.d, dv);  // the kernel's tile width
-  if (n_split > 1 && (pb.d != d || dv != d))
+  const bool wide = d == 256;            // head dims above 128: fa_tc_wide.cuh
+  if (n_split > 1 && (pb.d != d || dv != d || wide))
     return fail(FA_ERR_UNSUPPORTED, "split-KV needs d = Dv in {64, 128}");
-  const int bn = tc_key_tile(fp32, d);
+  const int bn = wide ? kWideKeyTile : tc_key_tile(fp32, d);
+  const int bm = wide ? kWideQueryTile : 256;  // query rows of a CTA tile
   TcLaunch L;
   fa_status_t st;
   if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, pb.d, 128, "Q")) != FA_OK) return st;
@@ -220,7 +226,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   p.N_k = (int)pb.N_k;
   p.causal = pb.is_causal == 0 ? kNoCausal : (pb.is_causal == 2 ? (int)(pb.N_k - pb.N_q) : 0);
   p.scale_log2 = static_cast<float>(static_cast<double>(pb.scale) * 1.4426950408889634);
-  p.n_qblk = (int)((pb.N_q + 255) / 256);
+  p.n_qblk = (int)((pb.N_q + bm - 1) / bm);
   p.n_tiles = (int)(pb.B * pb.H * p.n_qblk);
   if (n_split > 1)
     p.n_split = n_split;
@@ -249,7 +255,9 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   L.device = ds.device;
   L.stream = stream;
   cudaError_t e;
-  if (n_split > 1) {
+  if (wide) {
+    e = launch_tc_wide_bf16_d256(L);
+  } else if (n_split > 1) {
     if (fp32)
       e = d == 128 ? launch_tc_fp32_d128_split(L) : launch_tc_fp32_d64_split(L);
     else
@@ -730,6 +738,7 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   if (dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "packed variable-length batches take bf16");
   const int dv = static_cast<int>(v_dim(pb));
   const int D = tc_tile_dim(d, dv);
+  if (D > 128) return fail(FA_ERR_UNSUPPORTED, "packed variable-length batches take head dims up to 128");
   const long long n_qblk = (max_len_q + 255) / 256;
   if (B * H * n_qblk >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query tiles");
   DevState* ds = nullptr;

@@ -126,6 +126,8 @@ struct TcCfg {
   static constexpr uint32_t kRegEpilogue = kTF32 ? 88 : 64;  // fp32: also rounds and transposes
   static constexpr uint32_t kRegProducer = kTF32 ? 56 : 80;  // load warp + MMA warp
   static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 4 * 128, "register split");
+  static_assert(kRegSoftmax >= 128 && kRegEpilogue <= 128 && kRegProducer <= 128,
+                "setmaxnreg.inc raises, setmaxnreg.dec lowers");
 
   static_assert(D % kPanelElems == 0, "head dim must fill whole swizzle rows");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");

@@ -1,0 +1,27 @@
+// fa_tc_wide.cu -- the bf16 forward for head dims above 128 (up to 256): one
+// 128-row query block per CTA tile, 64-key tiles, a ring of 4 K/V slots.
+#include <atomic>
+
+#include "fa_launch.h"
+#include "fa_tc_wide.cuh"
+
+namespace fa {
+
+using CfgWideD256 = TcWideCfg<256, 64, 4>;
+static_assert(CfgWideD256::BN == kWideKeyTile && CfgWideD256::BM == kWideQueryTile, "host tile geometry");
+
+cudaError_t launch_tc_wide_bf16_d256(const TcLaunch& L) {
+  using C = CfgWideD256;
+  static std::atomic<bool> ready[kMaxDevices];
+  if (L.device < 0 || L.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!ready[L.device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(fa_tc_wide_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    ready[L.device].store(true, std::memory_order_release);
+  }
+  fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

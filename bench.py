@@ -829,7 +829,7 @@ def main():
                 "frac": achieved / peak, "traffic": traffic, "peak_source": note}
         if n_split > 1:  # the events bracket both launches of a split step
             roof["timed"] = f"split-KV attention kernel (n_split={n_split}) + merge kernel"
-        tile = 128 if max(w.d, w.v_dim) > 64 else 64
+        tile = 256 if max(w.d, w.v_dim) > 128 else (128 if max(w.d, w.v_dim) > 64 else 64)
         if not axial and not bwd and (w.d != tile or w.v_dim != tile) and w.d not in (16, 32):
             roof["tile_columns"] = (f"d={w.d}, Dv={w.v_dim} run on {tile}-column tiles: the tensor work is "
                                     f"{2 * tile / (w.d + w.v_dim):.3f}x the FLOPs counted")

@@ -78,8 +78,8 @@ def _call(L, dtype=fa.FA_BF16, B=1, H=1, Nq=256, Nk=256, d=128, qptr=0x10000, st
     (dict(causal=3), fa.FA_ERR_INVALID_ARG),   # 0, 1 (top-left), 2 (bottom-right)
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
     (dict(d=100), fa.FA_ERR_UNSUPPORTED),   # a row of 200 bytes: not a multiple of 16
-    (dict(d=136), fa.FA_ERR_UNSUPPORTED),   # above the 128-column tile
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=264), fa.FA_ERR_UNSUPPORTED),   # above the 256-column tile
+    (dict(d=136, dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),  # fp32: up to 128
     (dict(qptr=0x10002), fa.FA_ERR_UNSUPPORTED),                     # misaligned base
     (dict(strides=(256 * 128, 256 * 128, 129, 1)), fa.FA_ERR_UNSUPPORTED),  # odd row stride
     (dict(strides=(256 * 128, -128, 128, 1)), fa.FA_ERR_UNSUPPORTED),

@@ -3,9 +3,10 @@
 have Dv columns), on the tensor-core path, against the oracle element by
 element.
 
-The tiles are 64 or 128 columns wide; a smaller d or Dv is computed on tiles
-whose extra columns are loaded as zeros.  Every case writes O into a view of a
-wider buffer whose extra columns hold NaN, so a store past Dv is caught."""
+The tiles are 64, 128 or (bf16, the single-stage kernel for head dims above
+128) 256 columns wide; a smaller d or Dv is computed on tiles whose extra
+columns are loaded as zeros.  Every case writes O into a view of a wider
+buffer whose extra columns hold NaN, so a store past Dv is caught."""
 from __future__ import annotations
 
 import math
@@ -116,10 +117,49 @@ def test_sdpa_value_dim(oracle_mod):
     assert float(np.abs(O.float().cpu().numpy() - O_ref).max()) <= 2e-2
 
 
+@pytest.mark.parametrize("d,dv", [(256, 256), (192, 192), (136, 136), (192, 128), (256, 64), (64, 256),
+                                  (128, 200)])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"], ids=["nc", "top_left", "bottom_right"])
+def test_bf16_wide_head_dims(oracle_mod, d, dv, causal):
+    # 128-row query blocks and 64-key tiles: 300 / 333 rows leave ragged tails on both
+    _run(oracle_mod, torch.bfloat16, d, dv, causal, nq=300, nk=333 if causal != "bottom_right" else 200,
+         seed=5 * d + dv)
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 1), (1, 700), (129, 64), (64, 65), (700, 1)])
+def test_bf16_wide_edge_lengths(oracle_mod, nq, nk):
+    for causal in (False, True, "bottom_right"):
+        _run(oracle_mod, torch.bfloat16, 256, 256, causal, B=1, H=2, nq=nq, nk=nk, seed=nq + nk)
+
+
+def test_bf16_wide_grouped_heads_and_noalloc(oracle_mod):
+    _run(oracle_mod, torch.bfloat16, 256, 256, True, H=6, H_kv=2, nq=257, nk=257, seed=31)
+    _run(oracle_mod, torch.bfloat16, 192, 128, False, H=4, H_kv=1, nq=200, nk=640, seed=32)
+    _run(oracle_mod, torch.bfloat16, 256, 256, False, via="noalloc", seed=33)
+
+
+def test_bf16_wide_many_tiles_sampled(oracle_mod):
+    # more query blocks than SMs (persistent schedule) and long key ranges: sampled rows
+    B, H, N, d = 2, 16, 2048, 256
+    Q, K, V = qkv((B, H, N, d), (B, H, N, d), 2500, torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        O, L = fa.fwd(Q.cuda(), K.cuda(), V.cuda(), scale=scale, is_causal=causal)
+        fa.check()
+        rows = np.array([0, 1, 127, 128, 1000, 2047])
+        for b, h in ((0, 0), (1, 15), (0, 7)):
+            Or, Lr = oracle_mod.attention(Q[b, h], K[b, h], V[b, h], scale, causal, rows=rows)
+            assert float(np.abs(O[b, h, rows].float().cpu().numpy() - Or).max()) <= 2e-2
+            assert float(np.abs(L[b, h, rows].cpu().numpy() - Lr).max()) <= 1e-2
+
+
 def test_unsupported_dims_raise():
-    Q, K, V = (torch.zeros((1, 1, 64, n), dtype=torch.bfloat16, device="cuda") for n in (136, 136, 136))
+    Q, K, V = (torch.zeros((1, 1, 64, n), dtype=torch.bfloat16, device="cuda") for n in (264, 264, 264))
     with pytest.raises(fa.FaError):
-        fa.fwd(Q, K, V)                      # above the 128-column tile
+        fa.fwd(Q, K, V)                      # above the 256-column tile
+    Q, K, V = (torch.zeros((1, 1, 64, 136), dtype=torch.float32, device="cuda") for _ in range(3))
+    with pytest.raises(fa.FaError):
+        fa.fwd(Q, K, V)                      # fp32 stops at 128
     Q, K, V = (torch.zeros((1, 1, 64, 100), dtype=torch.bfloat16, device="cuda") for _ in range(3))
     with pytest.raises(fa.FaError):
         fa.fwd(Q, K, V)                      # a 200-byte row

@@ -37,10 +37,10 @@ cudaError_t launch_tc_fp32_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_fp32_d64_split(const TcLaunch& L);
 // variable-length variants (bf16; L.p.cu_q / cu_k set, N_q / N_k = packed totals)
 cudaError_t launch_tc_bf16_d128_varlen(const TcLaunch& L);
-// head dims above 128 (bf16, up to 256): 128-row query blocks, 64-key tiles
+// head dims above 128 (bf16, up to 256): 128-row query blocks, 128-key tiles
 cudaError_t launch_tc_wide_bf16_d256(const TcLaunch& L);
 constexpr int kWideQueryTile = 128;
-constexpr int kWideKeyTile = 64;
+constexpr int kWideKeyTile = 128;
 cudaError_t launch_tc_bf16_d64_varlen(const TcLaunch& L);
 
 // Backward pass (fa_bwd.cu): preprocess, tensor-core kernel and dQ

@@ -121,12 +121,12 @@ def test_sdpa_value_dim(oracle_mod):
                                   (128, 200)])
 @pytest.mark.parametrize("causal", [False, True, "bottom_right"], ids=["nc", "top_left", "bottom_right"])
 def test_bf16_wide_head_dims(oracle_mod, d, dv, causal):
-    # 128-row query blocks and 64-key tiles: 300 / 333 rows leave ragged tails on both
+    # 128-row query blocks and 128-key tiles: 300 / 333 rows leave ragged tails on both
     _run(oracle_mod, torch.bfloat16, d, dv, causal, nq=300, nk=333 if causal != "bottom_right" else 200,
          seed=5 * d + dv)
 
 
-@pytest.mark.parametrize("nq,nk", [(1, 1), (1, 700), (129, 64), (64, 65), (700, 1)])
+@pytest.mark.parametrize("nq,nk", [(1, 1), (1, 700), (129, 128), (64, 129), (700, 1)])
 def test_bf16_wide_edge_lengths(oracle_mod, nq, nk):
     for causal in (False, True, "bottom_right"):
         _run(oracle_mod, torch.bfloat16, 256, 256, causal, B=1, H=2, nq=nq, nk=nk, seed=nq + nk)

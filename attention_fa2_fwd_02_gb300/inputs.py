@@ -139,6 +139,7 @@ WORKLOADS = {
     "prof_causal": _w("prof_causal", 1, 32, 8192, 8192, 128, torch.bfloat16, True, seed=7),
     "prof_cross": _w("prof_cross", 1, 16, 4096, 32768, 64, torch.bfloat16, False, seed=8),
     "prof_tutorial": _w("prof_tutorial", 96, 1, 512, 512, 128, torch.float32, False, seed=2),
+    "prof_d256_nc": _w("prof_d256_nc", 1, 32, 8192, 8192, 256, torch.bfloat16, False, seed=13),
 }
 
 
@@ -263,6 +264,12 @@ class VarlenWorkload:
         """4 H d L^2 per sequence (two matmuls), halved under the causal mask."""
         f = sum(4.0 * self.H * self.d * n * n for n in self.lens)
         return f / 2 if self.causal else f
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """q, k, v read once; O written once (bf16); LSE written (fp32)."""
+        T = sum(self.lens)
+        return float(2 * T * self.H * self.d * 2 + 2 * T * self.kv_heads * self.d * 2 + self.H * T * 4)
 
     def make(self):
         return packed(self.lens, self.lens, self.H, self.kv_heads, self.d, self.seed, torch.bfloat16)

@@ -83,14 +83,15 @@ typedef struct {
  *   stream         cudaStream_t to launch on.
  *
  * Supported: d in {16, 32} on the small-head path (any alignment); any other
- * d up to 128 that makes a row a multiple of 16 bytes (d % 8 == 0 in bf16,
- * d % 4 == 0 in fp32) on the tensor-core path, which also needs 16-byte
- * aligned Q/K/V/O base pointers and strides[0..2] * element size that are
- * multiples of 16 bytes (FA_ERR_UNSUPPORTED otherwise).  The tensor-core tiles
- * have 64 or 128 columns: a smaller d is computed on tiles whose extra columns
- * are loaded as zeros (exact: they add nothing to Q.K and give O columns that
- * are not stored), so d = 96 costs the tensor work of d = 128.  Any N_q, N_k
- * >= 1: the tail of a tile is masked, not required to divide.
+ * d that makes a row a multiple of 16 bytes (d % 8 == 0 in bf16, d % 4 == 0
+ * in fp32), up to 256 in bf16 and 128 in fp32, on the tensor-core path, which
+ * also needs 16-byte aligned Q/K/V/O base pointers and strides[0..2] * element
+ * size that are multiples of 16 bytes (FA_ERR_UNSUPPORTED otherwise).  The
+ * tensor-core tiles have 64, 128 or (bf16, head dims above 128) 256 columns: a
+ * smaller d is computed on tiles whose extra columns are loaded as zeros
+ * (exact: they add nothing to Q.K and give O columns that are not stored), so
+ * d = 96 costs the tensor work of d = 128.  Any N_q, N_k >= 1: the tail of a
+ * tile is masked, not required to divide.
  */
 fa_status_t fa_fwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k,
                    int64_t d, const fa_tensor_t* Q, const fa_tensor_t* K,
@@ -113,8 +114,9 @@ fa_status_t fa_fwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
  * Dv: head dim of V and O when it differs from d ("Blackwell Attention
  * Example", blackwell_attention: Q and K share d, V and O have Dv columns);
  * 0 means Dv = d.  V is then [B, H_kv, N_k, Dv] and O [B, H, N_q, Dv].  A
- * problem with Dv != d takes the tensor-core path (Dv <= 128, a multiple of
- * 16 bytes like d); fa_fwd_grouped with one problem is the entry point for it. */
+ * problem with Dv != d takes the tensor-core path (Dv up to 256 in bf16, 128
+ * in fp32, a multiple of 16 bytes like d); fa_fwd_grouped with one problem is
+ * the entry point for it. */
 typedef struct {
   int64_t B, H, N_q, N_k, d;
   fa_tensor_t Q, K, V, O;

@@ -214,6 +214,7 @@ def _varlen(L, dtype=fa.FA_BF16, B=2, H=4, H_kv=4, total_q=300, total_k=300, max
     (dict(H_kv=3), fa.FA_ERR_INVALID_ARG),           # K/V heads must divide the query heads
     (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),  # bf16 only
     (dict(d=36), fa.FA_ERR_UNSUPPORTED),             # rows of a multiple of 16 bytes only
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),            # head dims up to 128
 ])
 def test_varlen_host_validation(L, kw, status):
     assert _varlen(L, **kw) == status

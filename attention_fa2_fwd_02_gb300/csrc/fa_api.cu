@@ -760,7 +760,14 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   p.n_units = p.n_tiles;
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
-  p.head_group = 1;
+  // Heads per schedule group, as for the batched tiles: keep the K/V of a
+  // group within ~48 MB of L2 (the longest query length stands in for the
+  // key lengths, which only the device knows).
+  const long long kv_bytes = max_len_q * (d + dv) * 2;
+  long long hg = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+  if (hg < 1) hg = 1;
+  if (hg > B * H) hg = B * H;
+  p.head_group = (int)hg;
   p.kv_group = (int)(H / H_kv);
   p.O = O->ptr;
   for (int i = 0; i < 3; ++i) {

@@ -175,12 +175,18 @@ template <class C>
 __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   constexpr int BN = C::BN;
   if constexpr (C::kVarlen) {
-    // virtual tiles: query-block rank major (last blocks first when causal),
-    // then (b, h); a block past its sequence's end is empty
+    // virtual tiles in the order of the batched tiles: groups of head_group
+    // (b, h) pairs (sized on the host so that their K/V stay in L2), inside a
+    // group the query-block ranks of its heads interleaved (last blocks first
+    // when causal); a block past its sequence's end is empty
     TileInfo ti;
     const int BH = p.B * p.H;
-    const int qi = u / BH;
-    const int bh = u - qi * BH;
+    const int per_group = p.head_group * p.n_qblk;
+    const int g = u / per_group;
+    const int r = u - g * per_group;
+    const int heads = min(p.head_group, BH - g * p.head_group);
+    const int qi = r / heads;
+    const int bh = g * p.head_group + (r - qi * heads);
     const bool causal = p.causal != kNoCausal;
     ti.b = bh / p.H;
     ti.h = bh - ti.b * p.H;

@@ -70,12 +70,12 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p,
             ]
             lib.oracle_num_threads.restype = ctypes.c_int
-            g = lib.oracle_attention_bwd_slice
+            g = lib.oracle_attention_bwd_slice_v
             g.restype = ctypes.c_int
             g.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
-                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_double, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -186,17 +186,20 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, is_causa
 def attention_bwd(Q, K, V, dO, scale: float, is_causal: bool = False, q_rows=None, k_rows=None):
     """fp64 gradients (dQ, dK, dV) of sum(dO * O) for every (batch..., head) slice.
 
-    Q, dO: [..., N_q, d]; K, V: [..., N_k, d].  q_rows / k_rows: optional 1-D
-    sequences of query / key rows to evaluate in every slice (default all).
-    Returns float64 numpy arrays dQ [..., n_q_rows, d], dK and dV [..., n_k_rows, d].
+    Q: [..., N_q, d]; K: [..., N_k, d]; V: [..., N_k, d_v]; dO: [..., N_q, d_v]
+    (d_v may differ from d).  q_rows / k_rows: optional 1-D sequences of query
+    / key rows to evaluate in every slice (default all).  Returns float64 numpy
+    arrays dQ [..., n_q_rows, d], dK [..., n_k_rows, d], dV [..., n_k_rows, d_v].
     """
     Q, K, V, dO = _as_f32(Q), _as_f32(K), _as_f32(V), _as_f32(dO)
-    if Q.ndim < 2 or K.shape != V.shape or Q.shape != dO.shape or Q.shape[:-2] != K.shape[:-2] \
-            or Q.shape[-1] != K.shape[-1]:
+    if Q.ndim < 2 or K.ndim != V.ndim or Q.ndim != dO.ndim or K.shape[:-1] != V.shape[:-1] \
+            or Q.shape[:-1] != dO.shape[:-1] or Q.shape[:-2] != K.shape[:-2] or Q.shape[-1] != K.shape[-1] \
+            or dO.shape[-1] != V.shape[-1]:
         raise ValueError(f"bad shapes Q{Q.shape} K{K.shape} V{V.shape} dO{dO.shape}")
     lead = Q.shape[:-2]
     N_q, d = Q.shape[-2:]
     N_k = K.shape[-2]
+    d_v = V.shape[-1]
 
     def rows_of(rows, n):
         if rows is None:
@@ -206,22 +209,22 @@ def attention_bwd(Q, K, V, dO, scale: float, is_causal: bool = False, q_rows=Non
     qr, nq = rows_of(q_rows, N_q)
     kr, nk = rows_of(k_rows, N_k)
     Qs = np.ascontiguousarray(Q.reshape(-1, N_q, d))
-    Gs = np.ascontiguousarray(dO.reshape(-1, N_q, d))
+    Gs = np.ascontiguousarray(dO.reshape(-1, N_q, d_v))
     Ks = np.ascontiguousarray(K.reshape(-1, N_k, d))
-    Vs = np.ascontiguousarray(V.reshape(-1, N_k, d))
+    Vs = np.ascontiguousarray(V.reshape(-1, N_k, d_v))
     dQ = np.empty((Qs.shape[0], nq, d), dtype=np.float64)
     dK = np.empty((Qs.shape[0], nk, d), dtype=np.float64)
-    dV = np.empty((Qs.shape[0], nk, d), dtype=np.float64)
+    dV = np.empty((Qs.shape[0], nk, d_v), dtype=np.float64)
     lib = _load()
     for s in range(Qs.shape[0]):
-        rc = lib.oracle_attention_bwd_slice(
-            Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d, Gs[s].ctypes.data, d,
-            N_q, N_k, d, float(scale), _causal_code(is_causal),
+        rc = lib.oracle_attention_bwd_slice_v(
+            Qs[s].ctypes.data, d, Ks[s].ctypes.data, d, Vs[s].ctypes.data, d_v, Gs[s].ctypes.data, d_v,
+            N_q, N_k, d, d_v, float(scale), _causal_code(is_causal),
             None if qr is None else qr.ctypes.data, nq, None if kr is None else kr.ctypes.data, nk,
             dQ[s].ctypes.data, dK[s].ctypes.data, dV[s].ctypes.data)
         if rc != 0:
-            raise RuntimeError(f"oracle_attention_bwd_slice failed with {rc}")
-    return dQ.reshape(*lead, nq, d), dK.reshape(*lead, nk, d), dV.reshape(*lead, nk, d)
+            raise RuntimeError(f"oracle_attention_bwd_slice_v failed with {rc}")
+    return dQ.reshape(*lead, nq, d), dK.reshape(*lead, nk, d), dV.reshape(*lead, nk, d_v)
 
 
 def layer_norm(x, weight, bias, eps: float = 1e-5):

@@ -168,23 +168,26 @@ int oracle_attention_slice(const float* Q, int64_t q_row_stride,
  *   dQ_i    = scale * sum_j dS_ij K_j
  *   dK_j    = scale * sum_i dS_ij Q_i
  *
+ * Q, K and dQ, dK have d columns; V, dO and dV have d_v (V with a head dim of
+ * its own, as "Blackwell Attention Example" blackwell_attention allows).
+ *
  * Untiled: first every query row's max, sum, O and delta (all rows, since dK
  * and dV need them), then dQ for the requested query rows and dK, dV for the
  * requested key rows, each by a plain loop over the other index.
  *   q_rows[0..n_q_rows), k_rows[0..n_k_rows): rows to evaluate (NULL = all).
- *   dQ: n_q_rows x d, dK and dV: n_k_rows x d doubles.
+ *   dQ: n_q_rows x d, dK: n_k_rows x d, dV: n_k_rows x d_v doubles.
  * Returns 0 on success, -1 on bad arguments, -2 if scratch allocation failed.
  */
-int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
-                               const float* K, int64_t k_row_stride,
-                               const float* V, int64_t v_row_stride,
-                               const float* dO, int64_t do_row_stride,
-                               int64_t N_q, int64_t N_k, int64_t d,
-                               double scale, int is_causal,
-                               const int64_t* q_rows, int64_t n_q_rows,
-                               const int64_t* k_rows, int64_t n_k_rows,
-                               double* dQ, double* dK, double* dV) {
-  if (!Q || !K || !V || !dO || N_q <= 0 || N_k <= 0 || d <= 0 || n_q_rows < 0 || n_k_rows < 0 ||
+int oracle_attention_bwd_slice_v(const float* Q, int64_t q_row_stride,
+                                 const float* K, int64_t k_row_stride,
+                                 const float* V, int64_t v_row_stride,
+                                 const float* dO, int64_t do_row_stride,
+                                 int64_t N_q, int64_t N_k, int64_t d, int64_t d_v,
+                                 double scale, int is_causal,
+                                 const int64_t* q_rows, int64_t n_q_rows,
+                                 const int64_t* k_rows, int64_t n_k_rows,
+                                 double* dQ, double* dK, double* dV) {
+  if (!Q || !K || !V || !dO || N_q <= 0 || N_k <= 0 || d <= 0 || d_v <= 0 || n_q_rows < 0 || n_k_rows < 0 ||
       is_causal < 0 || is_causal > 2)
     return -1;
   if ((!q_rows && n_q_rows != N_q) || (!k_rows && n_k_rows != N_k)) return -1;
@@ -207,7 +210,7 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
 #pragma omp parallel
   {
     double* s = (double*)malloc((size_t)N_k * sizeof(double));
-    double* o = (double*)malloc((size_t)d * sizeof(double));
+    double* o = (double*)malloc((size_t)d_v * sizeof(double));
     if (!s || !o) {
 #pragma omp atomic write
       failed = 2;
@@ -231,16 +234,16 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
         if (s[j] > m) m = s[j];
       }
       double l = 0.0;
-      for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t c = 0; c < d_v; ++c) o[c] = 0.0;
       for (int64_t j = 0; j < n_vis; ++j) {
         const double p = exp(s[j] - m);
         const float* v = V + j * v_row_stride;
         l += p;
-        for (int64_t c = 0; c < d; ++c) o[c] += p * (double)v[c];
+        for (int64_t c = 0; c < d_v; ++c) o[c] += p * (double)v[c];
       }
       const float* g = dO + i * do_row_stride;
       double dl = 0.0;
-      for (int64_t c = 0; c < d; ++c) dl += (double)g[c] * (o[c] / l);
+      for (int64_t c = 0; c < d_v; ++c) dl += (double)g[c] * (o[c] / l);
       lse[i] = m + log(l);
       delta[i] = dl;
     }
@@ -262,10 +265,8 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
       const float* k = K + j * k_row_stride;
       const float* v = V + j * v_row_stride;
       double dot = 0.0, dp = 0.0;
-      for (int64_t c = 0; c < d; ++c) {
-        dot += (double)q[c] * (double)k[c];
-        dp += (double)g[c] * (double)v[c];
-      }
+      for (int64_t c = 0; c < d; ++c) dot += (double)q[c] * (double)k[c];
+      for (int64_t c = 0; c < d_v; ++c) dp += (double)g[c] * (double)v[c];
       const double p = exp(scale * dot - lse[i]);
       const double ds = p * (dp - delta[i]);
       for (int64_t c = 0; c < d; ++c) out[c] += scale * ds * (double)k[c];
@@ -280,26 +281,37 @@ int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
     const float* k = K + j * k_row_stride;
     const float* v = V + j * v_row_stride;
     double* gk = dK + r * d;
-    double* gv = dV + r * d;
-    for (int64_t c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+    double* gv = dV + r * d_v;
+    for (int64_t c = 0; c < d; ++c) gk[c] = 0.0;
+    for (int64_t c = 0; c < d_v; ++c) gv[c] = 0.0;
     for (int64_t i = 0; i < N_q; ++i) {
       if (j >= visible_keys(i, N_q, N_k, is_causal)) continue; /* query i does not see key j */
       const float* q = Q + i * q_row_stride;
       const float* g = dO + i * do_row_stride;
       double dot = 0.0, dp = 0.0;
-      for (int64_t c = 0; c < d; ++c) {
-        dot += (double)q[c] * (double)k[c];
-        dp += (double)g[c] * (double)v[c];
-      }
+      for (int64_t c = 0; c < d; ++c) dot += (double)q[c] * (double)k[c];
+      for (int64_t c = 0; c < d_v; ++c) dp += (double)g[c] * (double)v[c];
       const double p = exp(scale * dot - lse[i]);
       const double ds = p * (dp - delta[i]);
-      for (int64_t c = 0; c < d; ++c) {
-        gv[c] += p * (double)g[c];
-        gk[c] += scale * ds * (double)q[c];
-      }
+      for (int64_t c = 0; c < d_v; ++c) gv[c] += p * (double)g[c];
+      for (int64_t c = 0; c < d; ++c) gk[c] += scale * ds * (double)q[c];
     }
   }
   free(lse);
   free(delta);
   return failed ? -2 : 0;
+}
+
+/* oracle_attention_bwd_slice_v with V and dO of the same head dim as Q and K. */
+int oracle_attention_bwd_slice(const float* Q, int64_t q_row_stride,
+                               const float* K, int64_t k_row_stride,
+                               const float* V, int64_t v_row_stride,
+                               const float* dO, int64_t do_row_stride,
+                               int64_t N_q, int64_t N_k, int64_t d,
+                               double scale, int is_causal,
+                               const int64_t* q_rows, int64_t n_q_rows,
+                               const int64_t* k_rows, int64_t n_k_rows,
+                               double* dQ, double* dK, double* dV) {
+  return oracle_attention_bwd_slice_v(Q, q_row_stride, K, k_row_stride, V, v_row_stride, dO, do_row_stride, N_q,
+                                      N_k, d, d, scale, is_causal, q_rows, n_q_rows, k_rows, n_k_rows, dQ, dK, dV);
 }

@@ -199,3 +199,46 @@ def test_each_bwd_mistake_trips_a_pin(kind):
         except AssertionError:
             tripped.append(pin.__name__)
     assert tripped, f"mutant {kind} passed every pin"
+
+
+# ----------------------------------------------------------------------------
+# V with a head dim of its own (d_v != d): the same two independent pins
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True, 2])
+def test_value_dim_finite_differences(oracle_mod, causal):
+    eps = 2.0 ** -12
+    Q, K, V, dO = _grid((9, 8), 21), _grid((11, 8), 22), _grid((11, 12), 23), _grid((9, 12), 24)
+    scale = 0.375
+    dQ, dK, dV = oracle_mod.attention_bwd(Q, K, V, dO, scale, causal)
+    assert dQ.shape == (9, 8) and dK.shape == (11, 8) and dV.shape == (11, 12)
+    r = np.random.default_rng(25)
+    for which, g in ((0, dQ), (1, dK), (2, dV)):
+        E = r.choice([-1.0, 1.0], size=[Q, K, V][which].shape).astype(np.float32)
+
+        def central(h):
+            args_p = [a + h * E if i == which else a for i, a in enumerate((Q, K, V))]
+            args_m = [a - h * E if i == which else a for i, a in enumerate((Q, K, V))]
+            return (_loss(oracle_mod.attention, *args_p, dO, scale, causal)
+                    - _loss(oracle_mod.attention, *args_m, dO, scale, causal)) / (2 * h)
+        num = (4.0 * central(eps / 2) - central(eps)) / 3.0
+        ana = float(np.sum(g * E))
+        assert abs(num - ana) <= 1e-6 * (1.0 + abs(ana)), (which, causal, num, ana)
+
+
+@pytest.mark.parametrize("d,d_v", [(16, 24), (24, 8)])
+def test_value_dim_torch_autograd(oracle_mod, d, d_v):
+    r = np.random.default_rng(26)
+    for causal, (nq, nk) in ((False, (13, 10)), (True, (13, 10)), (2, (8, 15))):
+        Q, K = r.standard_normal((nq, d)).astype(np.float32), r.standard_normal((nk, d)).astype(np.float32)
+        V, dO = r.standard_normal((nk, d_v)).astype(np.float32), r.standard_normal((nq, d_v)).astype(np.float32)
+        dQ, dK, dV = oracle_mod.attention_bwd(Q, K, V, dO, 0.3, causal)
+        q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+        if causal is not True and causal == 2:
+            mask = torch.ones(nq, nk, dtype=torch.bool).tril(diagonal=nk - nq)
+        else:
+            mask = torch.ones(nq, nk, dtype=torch.bool).tril() if causal else None
+        o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], attn_mask=mask, scale=0.3)[0]
+        (o * torch.tensor(dO, dtype=torch.float64)).sum().backward()
+        for got, want in ((dQ, q.grad), (dK, k.grad), (dV, v.grad)):
+            np.testing.assert_allclose(got, want.numpy(), rtol=0, atol=1e-12)

@@ -127,6 +127,10 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_varlen.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 8 + [ctypes.c_void_p] * 2 +
                                         [P(FaTensor)] * 3 + [ctypes.c_float, ctypes.c_int, P(FaTensor),
                                                              ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p])
+            L.fa_bwd_dv.restype = ctypes.c_int
+            L.fa_bwd_dv.argtypes = ([ctypes.c_int] + [ctypes.c_int64] * 7 + [P(FaTensor)] * 5 +
+                                    [ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_float, ctypes.c_int] +
+                                    [P(FaTensor)] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64] * 4
             L.fa_bwd.restype = ctypes.c_int
@@ -374,19 +378,23 @@ def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE:
         workspace: torch.Tensor | None = None, stream=None):
     """(dQ, dK, dV) of sum(dO * O) for O, LSE = fwd(Q, K, V, scale, is_causal).
 
-    bf16 tensors, head dim 64 or 128; LSE fp32 as ``fwd`` returns it.
-    Missing outputs and the scratch ``workspace`` (a CUDA uint8 tensor of
-    fa_bwd_workspace_bytes) are allocated here from PyTorch's allocator.
-    Asynchronous on the current (or given) stream.
+    bf16 tensors; Q, K (and dQ, dK) of head dim d, V, O, dO (and dV) of head
+    dim d_v (= d unless V has its own), both multiples of 8 up to 128; LSE
+    fp32 as ``fwd`` returns it.  Missing outputs and the scratch
+    ``workspace`` (a CUDA uint8 tensor of fa_bwd_workspace_bytes(B, H, N_q,
+    max(d, d_v))) are allocated here from PyTorch's allocator.  Asynchronous
+    on the current (or given) stream.
     """
     if not all(t.is_cuda for t in (Q, K, V, O, LSE, dO)):
         raise ValueError("Q, K, V, O, LSE, dO must be CUDA tensors (this library has no CPU path)")
     q4, k4, v4, o4, g4 = _as4(Q), _as4(K), _as4(V), _as4(O), _as4(dO)
     B, H, N_q, d = q4.shape
     N_k = k4.shape[2]
-    if o4.shape != q4.shape or g4.shape != q4.shape or v4.shape != k4.shape or k4.shape[0] != B or \
-            H % k4.shape[1] != 0 or k4.shape[3] != d:
-        raise ValueError("shape mismatch between Q, K, V, O and dO (K/V heads must divide the query heads)")
+    d_v = v4.shape[3]
+    if o4.shape[:3] != q4.shape[:3] or o4.shape[3] != d_v or g4.shape != o4.shape or \
+            v4.shape[:3] != k4.shape[:3] or k4.shape[0] != B or H % k4.shape[1] != 0 or k4.shape[3] != d:
+        raise ValueError("shape mismatch between Q, K, V, O and dO (K/V heads must divide the query heads; "
+                         "V, O, dO share their head dim)")
     H_kv = k4.shape[1]
     if LSE.dtype != torch.float32 or LSE.shape != Q.shape[:-1]:
         raise ValueError("LSE must be fp32 with Q's leading shape")
@@ -399,7 +407,7 @@ def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE:
         if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
             raise ValueError(f"{name} must match the shape, dtype and device of its input")
     L = lib()
-    need = L.fa_bwd_workspace_bytes(B, H, N_q, d)
+    need = L.fa_bwd_workspace_bytes(B, H, N_q, max(d, d_v))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
     if workspace.device != Q.device or workspace.numel() * workspace.element_size() < need:
@@ -408,7 +416,7 @@ def bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE:
     while l3.dim() < 3:
         l3 = l3.unsqueeze(0)
     with torch.cuda.device(Q.device):
-        st = L.fa_bwd_gqa(_dtype_code(Q), B, H, H_kv, N_q, N_k, d,
+        st = L.fa_bwd_dv(_dtype_code(Q), B, H, H_kv, N_q, N_k, d, d_v,
                       ctypes.byref(_ft(q4)), ctypes.byref(_ft(k4)), ctypes.byref(_ft(v4)), ctypes.byref(_ft(o4)),
                       ctypes.byref(_ft(g4)), ctypes.c_void_p(l3.data_ptr()), (ctypes.c_int64 * 3)(*l3.stride()),
                       float(scale), causal_code(is_causal),

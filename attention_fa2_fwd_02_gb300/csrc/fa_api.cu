@@ -573,8 +573,8 @@ fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, 
 }
 
 size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d) {
-  if (B <= 0 || H <= 0 || N_q <= 0 || d <= 0 || N_q >= (1ll << 31)) return 0;
-  return bwd_ws_bytes(B, H, N_q, d);
+  if (B <= 0 || H <= 0 || N_q <= 0 || d <= 0 || d > 128 || N_q >= (1ll << 31)) return 0;
+  return bwd_ws_bytes(B, H, N_q, tc_tile_dim(d, d));  // the accumulator has the tile's columns
 }
 
 fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t N_k, int64_t d,
@@ -591,6 +591,15 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
                        const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale,
                        int is_causal, const fa_tensor_t* dQ, const fa_tensor_t* dK, const fa_tensor_t* dV,
                        void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_dv(dtype, B, H, H_kv, N_q, N_k, d, d, Q, K, V, O, dO, LSE, lse_stride, scale, is_causal, dQ, dK, dV,
+                   workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_dv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                      int64_t d_v, const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V,
+                      const fa_tensor_t* O, const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3],
+                      float scale, int is_causal, const fa_tensor_t* dQ, const fa_tensor_t* dK,
+                      const fa_tensor_t* dV, void* workspace, size_t workspace_bytes, void* stream) {
   if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
   if (H_kv <= 0) return fail(FA_ERR_INVALID_ARG, "H_kv must divide H");
   if (!LSE || !lse_stride) return fail(FA_ERR_INVALID_ARG, "the backward needs the forward's LSE and its strides");
@@ -600,6 +609,7 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   pb.N_q = N_q;
   pb.N_k = N_k;
   pb.d = d;
+  pb.Dv = d_v;
   pb.Q = *Q;
   pb.K = *K;
   pb.V = *V;
@@ -613,29 +623,33 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   fa_status_t st = validate(dtype, pb, 0, &path);
   if (st != FA_OK) return st;
   if (dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "the backward supports bf16 inputs only");
-  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "the backward supports head dims 64 and 128");
+  if (d_v <= 0 || d > 128 || d_v > 128 || d % 8 != 0 || d_v % 8 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "the backward supports head dims d, d_v that are multiples of 8 up to 128");
+  // the kernel's tile width: 64 or 128 columns; the columns of Q, K (past d) and
+  // of V, dO (past d_v) load as zeros, and only d / d_v columns are stored
+  const long long D = tc_tile_dim(d, d_v);
   if ((st = check_bwd_tensor(dO, "dO")) != FA_OK || (st = check_bwd_tensor(dQ, "dQ")) != FA_OK ||
       (st = check_bwd_tensor(dK, "dK")) != FA_OK || (st = check_bwd_tensor(dV, "dV")) != FA_OK)
     return st;
-  const long long bm = d == 128 ? 64 : 128;  // query rows per step of the backward kernel
+  const long long bm = D == 128 ? 64 : 128;  // query rows per step of the backward kernel
   const long long n_kt = (N_k + 127) / 128, n_qt = (N_q + bm - 1) / bm;
   if (B * H_kv * n_kt >= (1ll << 31) || B * H * n_qt * 128 >= (1ll << 40) || (H / H_kv) * n_qt >= (1ll << 31))
     return fail(FA_ERR_UNSUPPORTED, "too many backward work units");
   if (!workspace) return fail(FA_ERR_INVALID_ARG, "the backward needs a workspace");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(FA_ERR_INVALID_ARG, "the backward workspace must be 256-byte aligned");
-  const size_t need = bwd_ws_bytes(B, H, N_q, d);
+  const size_t need = bwd_ws_bytes(B, H, N_q, D);
   if (workspace_bytes < need)
     return fail(FA_ERR_INVALID_ARG, "backward workspace too small: " + std::to_string(workspace_bytes) + " < " +
                                         std::to_string(need) + " bytes");
   DevState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
-  const BwdWs ws = bwd_ws_layout(workspace, B, H, N_q, d);
+  const BwdWs ws = bwd_ws_layout(workspace, B, H, N_q, D);
   BwdLaunch L{};
   if ((st = make_map(&L.tmQ, *Q, false, B, H, N_q, (int)d, (int)bm, "Q")) != FA_OK) return st;
-  if ((st = make_map(&L.tmdO, *dO, false, B, H, N_q, (int)d, (int)bm, "dO")) != FA_OK) return st;
+  if ((st = make_map(&L.tmdO, *dO, false, B, H, N_q, (int)d_v, (int)bm, "dO")) != FA_OK) return st;
   if ((st = make_map(&L.tmK, *K, false, B, H_kv, N_k, (int)d, 128, "K")) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, *V, false, B, H_kv, N_k, (int)d, 128, "V")) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, *V, false, B, H_kv, N_k, (int)d_v, 128, "V")) != FA_OK) return st;
   const int N_qp = (int)((N_q + 127) / 128 * 128);  // workspace row pitch
   BwdParams& p = L.p;
   p.B = (int)B;
@@ -653,7 +667,7 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   p.kv_group = (int)(H / H_kv);
   p.n_units = (int)(B * H_kv * n_kt);
   {  // K/V heads per schedule group: their query heads' fp32 dQ rows, Q and dO within ~48 MB of L2
-    const long long per_head = (N_qp * d * 4 + 2 * N_q * d * 2) * (H / H_kv);
+    const long long per_head = (N_qp * D * 4 + N_q * (d + d_v) * 2) * (H / H_kv);
     long long g = (48ll << 20) / (per_head > 0 ? per_head : 1);
     if (g < 1) g = 1;
     if (g > B * H_kv) g = B * H_kv;
@@ -670,6 +684,8 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   }
   p.err = ds->err;
   p.timeout_ns = g_timeout_ns.load();
+  p.d_qk = (int)d;
+  p.d_v = (int)d_v;
   BwdPreParams& pre = L.pre;
   pre.B = (int)B;
   pre.H = (int)H;
@@ -686,6 +702,7 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   pre.nlse2 = ws.nlse2;
   pre.delta = ws.delta;
   pre.dq_acc = ws.dq_acc;
+  pre.d_v = (int)d_v;
   BwdPostParams& post = L.post;
   post.B = (int)B;
   post.H = (int)H;
@@ -695,7 +712,8 @@ fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
   post.dq_acc = ws.dq_acc;
   post.dQ = dQ->ptr;
   for (int i = 0; i < 3; ++i) post.dq_stride[i] = dQ->stride[i];
-  L.d = (int)d;
+  post.d_qk = (int)d;
+  L.d = (int)D;
   L.grid = p.n_units < ds->sm_count ? p.n_units : ds->sm_count;
   L.device = ds->device;
   L.stream = static_cast<cudaStream_t>(stream);
@@ -884,6 +902,6 @@ void fa_debug_set(uint64_t timeout_ns, int debug_flags) {
   g_debug_flags.store(debug_flags);
 }
 
-int fa_version(void) { return 103; }
+int fa_version(void) { return 104; }
 
 }  // extern "C"

@@ -58,6 +58,8 @@ struct BwdParams {
   long long dk_stride[3], dv_stride[3];  // elements: b, h, n
   unsigned int* err;
   unsigned long long timeout_ns;
+  int d_qk, d_v;          // columns of dK and of dV to store (<= D; the columns of Q, K, V, dO
+                          // past their extents load as zeros)
 };
 
 template <int D_>
@@ -181,6 +183,7 @@ struct BwdPreParams {
   float* nlse2;
   float* delta;
   float* dq_acc;
+  int d_v;  // columns of O and dO (<= D)
 };
 template <typename T, int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__ BwdPreParams p) {
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = 0.f;
   float dl = 0.f;
-  if (q < p.N_q) {
+  if (q < p.N_q && lane * PER < p.d_v) {  // (d_v is a multiple of 8: a lane's columns are all in or all out)
     const T* o = reinterpret_cast<const T*>(p.O) + b * p.o_stride[0] + h * p.o_stride[1] +
                  static_cast<long long>(q) * p.o_stride[2] + lane * PER;
     const T* g = reinterpret_cast<const T*>(p.dO) + b * p.do_stride[0] + h * p.do_stride[1] +
@@ -222,6 +225,7 @@ struct BwdPostParams {
   const float* dq_acc;
   void* dQ;
   long long dq_stride[3];
+  int d_qk;  // columns of dQ (<= D)
 };
 template <typename T, int D>
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const __grid_constant__ BwdPostParams p) {
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const __grid_constant_
   const long long rows = static_cast<long long>(p.B) * p.H * p.N_q;
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
+  if (lane * PER >= p.d_qk) return;  // padded columns of the accumulator
   const int q = static_cast<int>(row % p.N_q);
   const long long bh = row / p.N_q;
   const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H);
@@ -516,8 +521,8 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
     if (w.n_steps == 0) {  // keys no query sees: zero gradients
       if (key < p.N_k)
         for (int c = 0; c < C::D; c += 8) {
-          *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
+          if (c < p.d_qk) *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0, 0, 0, 0);
+          if (c < p.d_v) *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
         }
       continue;
     }
@@ -560,16 +565,18 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
       if (valid) {
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
-          *reinterpret_cast<uint4*>(dv_row + c + k) =
-              make_uint4(pack_bf16x2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
-                         pack_bf16x2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
-                         pack_bf16x2(__uint_as_float(v[k + 4]), __uint_as_float(v[k + 5])),
-                         pack_bf16x2(__uint_as_float(v[k + 6]), __uint_as_float(v[k + 7])));
-          *reinterpret_cast<uint4*>(dk_row + c + k) =
-              make_uint4(pack_bf16x2(__uint_as_float(k2[k]) * p.scale, __uint_as_float(k2[k + 1]) * p.scale),
-                         pack_bf16x2(__uint_as_float(k2[k + 2]) * p.scale, __uint_as_float(k2[k + 3]) * p.scale),
-                         pack_bf16x2(__uint_as_float(k2[k + 4]) * p.scale, __uint_as_float(k2[k + 5]) * p.scale),
-                         pack_bf16x2(__uint_as_float(k2[k + 6]) * p.scale, __uint_as_float(k2[k + 7]) * p.scale));
+          if (c + k < p.d_v)
+            *reinterpret_cast<uint4*>(dv_row + c + k) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                           pack_bf16x2(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])),
+                           pack_bf16x2(__uint_as_float(v[k + 4]), __uint_as_float(v[k + 5])),
+                           pack_bf16x2(__uint_as_float(v[k + 6]), __uint_as_float(v[k + 7])));
+          if (c + k < p.d_qk)
+            *reinterpret_cast<uint4*>(dk_row + c + k) =
+                make_uint4(pack_bf16x2(__uint_as_float(k2[k]) * p.scale, __uint_as_float(k2[k + 1]) * p.scale),
+                           pack_bf16x2(__uint_as_float(k2[k + 2]) * p.scale, __uint_as_float(k2[k + 3]) * p.scale),
+                           pack_bf16x2(__uint_as_float(k2[k + 4]) * p.scale, __uint_as_float(k2[k + 5]) * p.scale),
+                           pack_bf16x2(__uint_as_float(k2[k + 6]) * p.scale, __uint_as_float(k2[k + 7]) * p.scale));
         }
       }
     }

@@ -228,7 +228,9 @@ fa_status_t fa_fwd_splitkv_noalloc(fa_dtype_t dtype, int64_t B, int64_t H, int64
  * P recomputed from Q, K and the forward's LSE).
  *
  *   dtype          FA_BF16 (FA_ERR_UNSUPPORTED for FA_FP32); every tensor bf16.
- *   d              64 or 128.
+ *   d              a multiple of 8 up to 128 (64 and 128 fill the kernel's
+ *                  tiles; other head dims run on 64- or 128-column tiles
+ *                  whose extra columns load as zeros).
  *   Q, K, V        the forward's inputs; O and LSE / lse_stride its outputs
  *                  (LSE natural log, as fa_fwd writes it).  Same views and
  *                  rules as fa_fwd (16-byte aligned bases and strides).
@@ -238,9 +240,10 @@ fa_status_t fa_fwd_splitkv_noalloc(fa_dtype_t dtype, int64_t B, int64_t H, int64
  *                  query sees (causal, N_k > N_q) get zero gradients.
  *   scale, is_causal  as in the forward call.
  *   workspace      device memory of at least fa_bwd_workspace_bytes(B, H,
- *                  N_q, d) bytes, 256-byte aligned, caller-owned scratch (an
- *                  fp32 dQ accumulator and two per-row vectors).  Concurrent
- *                  calls need separate workspaces.
+ *                  N_q, d) bytes (fa_bwd_dv: N_q, max(d, d_v)), 256-byte
+ *                  aligned, caller-owned scratch (an fp32 dQ accumulator of the
+ *                  tile's width and two per-row vectors).  Concurrent calls need
+ *                  separate workspaces.
  * Asynchronous on `stream` (three kernels).  Argument errors are reported on
  * the host before any launch.
  */
@@ -253,6 +256,19 @@ size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d);
  * fa_bwd_workspace_bytes(B, H, N_q, d) (query heads).  Other arguments as
  * fa_bwd.
  */
+/*
+ * fa_bwd_dv -- fa_bwd_gqa with V, O, dO and dV of head dim d_v ("Blackwell
+ * Attention Example", blackwell_attention takes V with Dv columns): Q, K, dQ,
+ * dK are [.., d], V, dV [B, H_kv, N_k, d_v], O, dO [B, H, N_q, d_v]; d and d_v
+ * multiples of 8 up to 128.  Workspace: fa_bwd_workspace_bytes(B, H, N_q,
+ * max(d, d_v)).  Other arguments as fa_bwd_gqa.
+ */
+fa_status_t fa_bwd_dv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                      int64_t d_v, const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V,
+                      const fa_tensor_t* O, const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3],
+                      float scale, int is_causal, const fa_tensor_t* dQ, const fa_tensor_t* dK,
+                      const fa_tensor_t* dV, void* workspace, size_t workspace_bytes, void* stream);
+
 fa_status_t fa_bwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
                        const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, const fa_tensor_t* O,
                        const fa_tensor_t* dO, const float* LSE, const int64_t lse_stride[3], float scale,

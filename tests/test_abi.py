@@ -47,7 +47,7 @@ def test_library_is_built_for_sm103a():
 def test_status_strings(L):
     assert L.fa_status_string(0) == b"ok"
     assert L.fa_status_string(4) == b"device wait timed out"
-    assert L.fa_version() == 103
+    assert L.fa_version() == 104
 
 
 def _t(ptr, strides):
@@ -161,8 +161,8 @@ def _bwd(L, dtype=fa.FA_BF16, d=128, ws=0x100000, ws_bytes=1 << 30, lse=0x50000,
 
 @pytest.mark.parametrize("kw,status", [
     (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),  # bf16 only
-    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=100), fa.FA_ERR_UNSUPPORTED),            # a 200-byte row
+    (dict(d=136), fa.FA_ERR_UNSUPPORTED),            # the backward stops at 128
     (dict(lse=0), fa.FA_ERR_INVALID_ARG),             # the forward's LSE is required
     (dict(ws=0), fa.FA_ERR_INVALID_ARG),
     (dict(ws=0x100080), fa.FA_ERR_INVALID_ARG),       # not 256-byte aligned
@@ -179,6 +179,10 @@ def test_bwd_workspace_size(L):
     want = ((rows * 64 * 4 + 255) // 256) * 256 + 2 * (((rows * 4) + 255) // 256) * 256
     assert L.fa_bwd_workspace_bytes(2, 3, 200, 64) == want
     assert L.fa_bwd_workspace_bytes(0, 3, 200, 64) == 0
+    # other head dims take the accumulator of their tile (64 or 128 columns); above 128: none
+    assert L.fa_bwd_workspace_bytes(2, 3, 200, 40) == want
+    assert L.fa_bwd_workspace_bytes(2, 3, 200, 96) == L.fa_bwd_workspace_bytes(2, 3, 200, 128)
+    assert L.fa_bwd_workspace_bytes(2, 3, 200, 256) == 0
 
 
 def test_gqa_heads_must_divide(L):

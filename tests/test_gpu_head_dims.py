@@ -163,8 +163,7 @@ def test_unsupported_dims_raise():
     Q, K, V = (torch.zeros((1, 1, 64, 100), dtype=torch.bfloat16, device="cuda") for _ in range(3))
     with pytest.raises(fa.FaError):
         fa.fwd(Q, K, V)                      # a 200-byte row
-    Q, K = (torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16, device="cuda") for _ in range(2))
-    V = torch.zeros((1, 1, 64, 64), dtype=torch.bfloat16, device="cuda")
+    Q, K, V = (torch.zeros((1, 1, 64, 256), dtype=torch.bfloat16, device="cuda") for _ in range(3))
     O, L = fa.fwd(Q, K, V)
-    with pytest.raises(ValueError):
-        fa.bwd(Q, K, V, O, L, O.clone())     # the backward takes Dv = d
+    with pytest.raises(fa.FaError):
+        fa.bwd(Q, K, V, O, L, O.clone())     # the backward stops at 128

@@ -7,11 +7,16 @@ if the library is missing, every call raises.
 
     O, LSE = fwd(Q, K, V, scale=None, is_causal=False)
 
-Q: [B, H, N_q, d], K and V: [B, H, N_k, d] CUDA tensors (bf16 or fp32; any
-strides with a contiguous last dim).  O has Q's dtype, LSE is fp32 [B, H, N_q]
-(natural log).  The default scale is 1/sqrt(d), as in "Extend Thunder with
-CUDA-Python" (flash_attention_reference) and "Blackwell Attention Example"
-(blackwell_attention).
+Q: [B, H, N_q, d], K: [B, H_kv, N_k, d], V: [B, H_kv, N_k, d_v] CUDA tensors
+(bf16 or fp32; any strides with a contiguous last dim; H_kv divides H; d_v
+may differ from d).  O has Q's dtype and V's head dim, LSE is fp32
+[B, H, N_q] (natural log).  The default scale is 1/sqrt(d), as in "Extend
+Thunder with CUDA-Python" (flash_attention_reference) and "Blackwell Attention
+Example" (blackwell_attention).
+
+Also: ``bwd`` (dQ, dK, dV), ``attention`` (autograd), ``fwd_varlen`` (packed
+sequences of different lengths), ``fwd_noalloc``, ``fwd_grouped``, ``axial``
+and ``axial_block``; ``sdpa`` routes torch's scaled_dot_product_attention here.
 """
 from __future__ import annotations
 

@@ -239,15 +239,17 @@ def get_workload(name):
         raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS)}, {sorted(VARLEN)}, "
                          f"axial, axial_block, or <bf16 workload>_bwd")
     w = WORKLOADS[base]
-    if name.endswith("_bwd") and (w.dtype != torch.bfloat16 or w.d not in (64, 128)):
-        raise SystemExit(f"{name}: the backward runs on bf16 workloads with d = 64 or 128")
+    if name.endswith("_bwd") and (w.dtype != torch.bfloat16 or max(w.d, w.v_dim) > 128):
+        raise SystemExit(f"{name}: the backward runs on bf16 workloads with head dims up to 128")
     return w
 
 
 def bwd_flops(w) -> float:
-    """Backward FLOPs: five products of 2*N_q*N_k*d each per (b, h) (S, dP, dV,
-    dK, dQ), i.e. 2.5x the forward's two; halved when causal."""
-    return 2.5 * w.flops
+    """Backward FLOPs: five products per (b, h), 2*N_q*N_k times d for S, dK and
+    dQ and times Dv for dP and dV (2.5x the forward's two when Dv = d); halved
+    when causal."""
+    f = 2.0 * w.B * w.H * w.N_q * w.N_k * (3 * w.d + 2 * w.v_dim)
+    return f / 2 if w.causal else f
 
 
 def bwd_oracle_sample(w, Q, K, V, G, budget_s: float):
@@ -266,7 +268,7 @@ def bwd_oracle_sample(w, Q, K, V, G, budget_s: float):
         hk = h // (w.H // w.kv_heads)
         oracle.attention_bwd(Q[b, h, :nq], K[b, hk, :nk], V[b, hk, :nk], G[b, h, :nq], w.scale, w.causal)
         one = time.perf_counter() - t1
-        flops += 10.0 * nq * nk * w.d * (0.5 if w.causal else 1.0)
+        flops += 2.0 * nq * nk * (3 * w.d + 2 * w.v_dim) * (0.5 if w.causal else 1.0)
         calls += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -407,7 +409,7 @@ def run_reference(args, w):
     steps, warm = args.steps, max(3, args.warmup)
     if args.workload.endswith("_bwd"):
         from attention_fa2_fwd_02_gb300.inputs import normal
-        G = normal(Q.shape, 4242, torch.bfloat16)
+        G = normal(Q.shape[:-1] + V.shape[-1:], 4242, torch.bfloat16)  # dO: O's shape
         budget = max(0.05, 120.0 / (steps + warm))
         for _ in range(warm):
             bwd_oracle_sample(w, Q, K, V, G, budget)
@@ -700,7 +702,7 @@ def main():
     Qd, Kd, Vd = Qh.to(dev), Kh.to(dev), Vh.to(dev)
     if bwd:
         from attention_fa2_fwd_02_gb300.inputs import normal
-        Gh = normal(Qh.shape, 4242, torch.bfloat16)
+        Gh = normal(Qh.shape[:-1] + Vh.shape[-1:], 4242, torch.bfloat16)  # dO: O's shape
         Gd = Gh.to(dev)
     stream = torch.cuda.current_stream(dev)
     props = torch.cuda.get_device_properties(dev)
@@ -717,7 +719,8 @@ def main():
         # forward outputs (not timed), then the backward as the step
         Od, Ld = fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, split_kv=1)
         dQd, dKd, dVd = torch.empty_like(Qd), torch.empty_like(Kd), torch.empty_like(Vd)
-        ws = torch.empty(fa.lib().fa_bwd_workspace_bytes(w.B, w.H, w.N_q, w.d), dtype=torch.uint8, device=dev)
+        ws = torch.empty(fa.lib().fa_bwd_workspace_bytes(w.B, w.H, w.N_q, max(w.d, w.v_dim)), dtype=torch.uint8,
+                         device=dev)
 
         def step():
             return fa.bwd(Qd, Kd, Vd, Od, Ld, Gd, scale=w.scale, is_causal=w.causal, dQ=dQd, dK=dKd, dV=dVd,

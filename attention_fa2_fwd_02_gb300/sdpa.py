@@ -80,7 +80,7 @@ def scaled_dot_product_attention(query: torch.Tensor, key: torch.Tensor, value: 
     (H_kv = H unless ``enable_gqa``, then H_kv must divide H; d_v may differ
     from d, as in PyTorch).  The causal mask is the top-left one, as in
     PyTorch.  bf16 or fp32; the head dims and layouts fa_fwd supports (the
-    backward: bf16, d = d_v = 64 or 128).
+    backward: bf16, d and d_v multiples of 8 up to 128).
     """
     if attn_mask is not None:
         raise NotImplementedError("attn_mask is not supported (only is_causal)")

@@ -226,7 +226,7 @@ def workload_desc(w) -> dict:
 
 def get_workload(name):
     """The workload; names ending in ``_bwd`` time the backward pass of the
-    named forward workload (bf16, d = 64 or 128)."""
+    named forward workload (bf16, head dims up to 128)."""
     from attention_fa2_fwd_02_gb300.inputs import AXIAL, AXIAL_BLOCK, VARLEN, WORKLOADS
     if name in VARLEN:
         return VARLEN[name]

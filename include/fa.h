@@ -293,7 +293,8 @@ fa_status_t fa_bwd(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, int64_t 
  *                  whose packed index falls outside [0, total_q) is not
  *                  written).  Sequences may be empty.
  *   total_q, total_k  packed rows (>= 1 each); max_len_q  host upper bound of
- *                  the query lengths, 1 .. total_q (it sizes the tile grid).
+ *                  the query lengths, 1 .. total_q (it sizes the tile grid:
+ *                  query rows of a sequence past max_len_q are not computed).
  *   d, d_v         head dims of Q, K and of V, O (d_v = 0 means d_v = d).
  *   Q              [1, H, total_q, d] view (stride[1] head, stride[2] row),
  *                  K [1, H_kv, total_k, d], V [1, H_kv, total_k, d_v],

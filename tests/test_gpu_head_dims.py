@@ -167,3 +167,18 @@ def test_unsupported_dims_raise():
     O, L = fa.fwd(Q, K, V)
     with pytest.raises(fa.FaError):
         fa.bwd(Q, K, V, O, L, O.clone())     # the backward stops at 128
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
+def test_bf16_wide_strided_head_major(oracle_mod, causal):
+    # Q, K, V, O as [B, H, N, d] views of [B, N, H, d] storage (no copies): the tensor maps take the strides
+    B, H, N, d = 2, 3, 300, 256
+    Q, K, V = qkv((B, H, N, d), (B, H, N, d), 2600, torch.bfloat16)
+    dev = [x.transpose(1, 2).contiguous().cuda().transpose(1, 2) for x in (Q, K, V)]
+    O = torch.full((B, N, H, d), float("nan"), dtype=torch.bfloat16, device="cuda").transpose(1, 2)
+    scale = 1.0 / math.sqrt(d)
+    _, L = fa.fwd(*dev, scale=scale, is_causal=causal, out=O)
+    fa.check()
+    O_ref, L_ref = oracle_mod.attention(Q, K, V, scale, causal)
+    assert float(np.abs(O.float().cpu().numpy() - O_ref).max()) <= 2e-2
+    assert float(np.abs(L.cpu().numpy() - L_ref).max()) <= 1e-2

@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, stride[3] != 1, non-finite scale */
-  FA_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for (head dim, alignment) */
+  FA_ERR_UNSUPPORTED = 2,  /* valid arguments the library has no kernel for (head dim, alignment) */
   FA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed (launch, attribute, device query) */
   FA_ERR_TIMEOUT = 4       /* a kernel's bounded pipeline wait expired; its outputs are undefined */
 } fa_status_t;

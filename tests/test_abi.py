@@ -223,3 +223,42 @@ def _varlen(L, dtype=fa.FA_BF16, B=2, H=4, H_kv=4, total_q=300, total_k=300, max
 def test_varlen_host_validation(L, kw, status):
     assert _varlen(L, **kw) == status
     assert L.fa_last_error() != b""
+
+
+def _bwd_dv(L, dtype=fa.FA_BF16, d=128, d_v=64, ws_bytes=1 << 30, N=256):
+    sq = (N * d, N * d, d, 1)
+    sv = (N * d_v, N * d_v, d_v, 1)
+    # Q, K, V, O, dO, then dQ, dK, dV
+    t = [_t(a, s) for a, s in zip((0x10000, 0x20000, 0x30000, 0x40000, 0x60000, 0x70000, 0x80000, 0x90000),
+                                  (sq, sq, sv, sv, sv, sq, sq, sv))]
+    ls = (ctypes.c_int64 * 3)(N, N, 1)
+    return L.fa_bwd_dv(dtype, 1, 1, 1, N, N, d, d_v, *(ctypes.byref(x) for x in t[:5]), 0x50000, ls, 0.1, 0,
+                       *(ctypes.byref(x) for x in t[5:]), 0x100000, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),      # bf16 only
+    (dict(d_v=136), fa.FA_ERR_UNSUPPORTED),              # the backward stops at 128
+    (dict(d=256, d_v=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d_v=100), fa.FA_ERR_UNSUPPORTED),              # a 200-byte row
+    (dict(ws_bytes=4096), fa.FA_ERR_INVALID_ARG),        # workspace for max(d, d_v) required
+])
+def test_bwd_dv_host_validation(L, kw, status):
+    assert _bwd_dv(L, **kw) == status
+    assert L.fa_last_error() != b""
+
+
+def test_problem_value_dim_validation(L):
+    # fa_problem_t.Dv: negative is an argument error; above the tiles, unsupported
+    s = (256 * 64, 256 * 64, 64, 1)
+    pb = fa.FaProblem()
+    pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.H_kv = 1, 2, 256, 256, 64, 0
+    pb.Q, pb.K, pb.V, pb.O = (_t(a, s) for a in (0x10000, 0x20000, 0x30000, 0x40000))
+    pb.LSE = None
+    pb.scale, pb.is_causal = 0.125, 0
+    pb.Dv = -8
+    assert L.fa_fwd_grouped(fa.FA_BF16, 1, ctypes.byref(pb), None) == fa.FA_ERR_INVALID_ARG
+    pb.Dv = 264
+    assert L.fa_fwd_grouped(fa.FA_BF16, 1, ctypes.byref(pb), None) == fa.FA_ERR_UNSUPPORTED
+    pb.Dv = 136
+    assert L.fa_fwd_grouped(fa.FA_FP32, 1, ctypes.byref(pb), None) == fa.FA_ERR_UNSUPPORTED  # fp32 stops at 128

@@ -174,7 +174,9 @@ fa_status_t make_map(CUtensorMap* map, const fa_tensor_t& t, bool fp32, long lon
                            (cuuint64_t)(t.stride[0] * E)};
   cuuint32_t box[4] = {(cuuint32_t)tc_box_inner(fp32), (cuuint32_t)box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.ptr, dims,
+  // fp32 inputs go to the tf32 tensor cores: a tf32-typed map makes the copy
+  // round each value to tf32 (nearest, ties to even) on its way to shared memory
+  CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_TFLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.ptr, dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -209,9 +211,11 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   const bool fp32 = dtype == FA_FP32;
   const int dv = static_cast<int>(v_dim(pb));
   const int d = tc_tile_dim(pb.d, dv);  // the kernel's tile width
-  const bool wide = d == 256;            // head dims above 128: fa_tc_wide.cuh
-  if (n_split > 1 && (pb.d != d || dv != d || wide))
+  if (n_split > 1 && (pb.d != d || dv != d || d == 256))
     return fail(FA_ERR_UNSUPPORTED, "split-KV needs d = Dv in {64, 128}");
+  // the single-stage kernel (fa_tc_wide.cuh): bf16 tiles of 256 columns and
+  // every fp32 problem (split or not)
+  const bool wide = d == 256 || fp32;
   const int bn = wide ? kWideKeyTile : tc_key_tile(fp32, d);
   const int bm = wide ? kWideQueryTile : 256;  // query rows of a CTA tile
   TcLaunch L;
@@ -255,15 +259,14 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   L.device = ds.device;
   L.stream = stream;
   cudaError_t e;
-  if (wide) {
+  if (fp32 && n_split > 1) {
+    e = d == 128 ? launch_tc_wide_fp32_d128_split(L) : launch_tc_wide_fp32_d64_split(L);
+  } else if (fp32) {
+    e = d == 128 ? launch_tc_wide_fp32_d128(L) : launch_tc_wide_fp32_d64(L);
+  } else if (wide) {
     e = launch_tc_wide_bf16_d256(L);
   } else if (n_split > 1) {
-    if (fp32)
-      e = d == 128 ? launch_tc_fp32_d128_split(L) : launch_tc_fp32_d64_split(L);
-    else
-      e = d == 128 ? launch_tc_bf16_d128_split(L) : launch_tc_bf16_d64_split(L);
-  } else if (fp32) {
-    e = d == 128 ? launch_tc_fp32_d128(L) : launch_tc_fp32_d64(L);
+    e = d == 128 ? launch_tc_bf16_d128_split(L) : launch_tc_bf16_d64_split(L);
   } else {
     e = d == 128 ? launch_tc_bf16_d128(L) : launch_tc_bf16_d64(L);
   }
@@ -278,6 +281,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
     c.causal_off = pb.is_causal == 2 ? (int)(pb.N_k - pb.N_q) : 0;
     c.n_split = n_split;
     c.bn = bn;
+    c.bm = bm;
     c.rows = pb.B * pb.H * pb.N_q;
     c.ws_o = ws.o;
     c.ws_lse = ws.lse;
@@ -557,7 +561,7 @@ fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, 
   if (st != FA_OK) return st;
   if (path != Path::kTensorCore || (d != 64 && d != 128))
     return fail(FA_ERR_UNSUPPORTED, "split-KV needs the tensor-core path with d = 64 or 128");
-  if (B * H * ((N_q + 255) / 256) * n_split >= (1ll << 31))
+  if (B * H * ((N_q + 127) / 128) * n_split >= (1ll << 31))
     return fail(FA_ERR_UNSUPPORTED, "too many split-KV work units");
   if (!workspace) return fail(FA_ERR_INVALID_ARG, "split-KV needs a workspace");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)

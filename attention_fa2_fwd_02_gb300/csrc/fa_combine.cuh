@@ -19,6 +19,7 @@ constexpr int kMaxSplit = 8;
 
 struct CombineParams {
   int B, H, N_q, N_k, causal, n_split, bn;  // bn: key-tile width used by the split kernel
+  int bm;                                   // query rows of a tile of the split kernel
   int causal_off;                           // as TcParams::causal_off
   long long rows;                           // B * H * N_q
   const float* ws_o;                        // [n_split][rows][D]
@@ -38,10 +39,10 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const __grid_constant__
   const int q = static_cast<int>(row % p.N_q);
   const long long bh = row / p.N_q;
   const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H);
-  // splits that exist for this row's 256-row tile (same rule as the split kernel)
-  const int q0 = (q / 256) * 256;
+  // splits that exist for this row's tile (same rule as the split kernel)
+  const int q0 = (q / p.bm) * p.bm;
   int kv_end = p.N_k;
-  if (p.causal) kv_end = min(kv_end, min(q0 + 256, p.N_q) + p.causal_off);
+  if (p.causal) kv_end = min(kv_end, min(q0 + p.bm, p.N_q) + p.causal_off);
   const int n_tot = kv_end > 0 ? (kv_end + p.bn - 1) / p.bn : 0;
   const int s_eff = min(p.n_split, n_tot);
 

@@ -25,23 +25,26 @@ struct TcLaunch {
 };
 
 // Kernel variants: (element type, head dim).  Each returns the CUDA error of
-// the launch (cudaSuccess when it was queued).
+// the launch (cudaSuccess when it was queued).  Two-stage kernel (fa_tc.cuh),
+// bf16, 256-row CTA tiles:
 cudaError_t launch_tc_bf16_d128(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64(const TcLaunch& L);
-cudaError_t launch_tc_fp32_d128(const TcLaunch& L);
-cudaError_t launch_tc_fp32_d64(const TcLaunch& L);
 // split-KV variants (L.p.n_split > 1, L.p.ws_o / ws_lse set)
 cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64_split(const TcLaunch& L);
-cudaError_t launch_tc_fp32_d128_split(const TcLaunch& L);
-cudaError_t launch_tc_fp32_d64_split(const TcLaunch& L);
 // variable-length variants (bf16; L.p.cu_q / cu_k set, N_q / N_k = packed totals)
 cudaError_t launch_tc_bf16_d128_varlen(const TcLaunch& L);
-// head dims above 128 (bf16, up to 256): 128-row query blocks, 128-key tiles
+cudaError_t launch_tc_bf16_d64_varlen(const TcLaunch& L);
+// single-stage kernel (fa_tc_wide.cuh): 128-row query blocks, 128-key tiles;
+// bf16 head dims above 128 (up to 256) and every fp32 input (kind::tf32),
+// the latter also split-KV
 cudaError_t launch_tc_wide_bf16_d256(const TcLaunch& L);
+cudaError_t launch_tc_wide_fp32_d128(const TcLaunch& L);
+cudaError_t launch_tc_wide_fp32_d64(const TcLaunch& L);
+cudaError_t launch_tc_wide_fp32_d128_split(const TcLaunch& L);
+cudaError_t launch_tc_wide_fp32_d64_split(const TcLaunch& L);
 constexpr int kWideQueryTile = 128;
 constexpr int kWideKeyTile = 128;
-cudaError_t launch_tc_bf16_d64_varlen(const TcLaunch& L);
 
 // Backward pass (fa_bwd.cu): preprocess, tensor-core kernel and dQ
 // conversion on one stream.  bf16 only; d = 64 or 128.
@@ -61,8 +64,10 @@ cudaError_t launch_bwd_bf16(const BwdLaunch& L);
 // (for entry points defined outside fa_api.cu).
 fa_status_t report_error(fa_status_t st, const std::string& msg);
 
-// Tile geometry shared with the instantiations in fa_tc_*.cu: key-tile width and TMA box width (one 128-byte swizzle row).
-constexpr int tc_key_tile(bool fp32, int d) { return fp32 ? (d == 128 ? 32 : 64) : 128; }
+// Tile geometry shared with the instantiations in fa_tc_*.cu: key-tile width
+// (128 keys for every instantiation) and TMA box width (one 128-byte swizzle
+// row: 64 bf16 or 32 fp32 values).
+constexpr int tc_key_tile(bool, int) { return 128; }
 constexpr int tc_box_inner(bool fp32) { return fp32 ? 32 : 64; }
 
 }  // namespace fa

@@ -9,6 +9,9 @@
 // scale, exp2 for P and for the correction factor), with the top-left causal
 // mask of the former.
 //
+// This kernel takes bf16 inputs (tcgen05 kind::f16) with head dims up to 128;
+// fp32 inputs and wider heads run on the single-stage kernel of fa_tc_wide.cuh.
+//
 // Design for GB300 (differs from both pages' kernels):
 //  * one CTA per SM, persistent; a CTA tile is 256 query rows of one (b, h),
 //    split into two 128-row halves ("stages") whose softmax runs on two
@@ -99,41 +102,34 @@ struct TcCfg {
   __host__ __device__ static constexpr uint32_t col_s(int s) { return s ? BN : 0; }
   __host__ __device__ static constexpr uint32_t col_o(int s) { return 2 * BN + (s ? D : 0); }
   static constexpr uint32_t kTmemCols = 512;
-  // fp32 inputs: the tensor core takes a tf32 B operand only K-major, so each
-  // V tile is transposed in shared memory into a double-buffered [D][BN] copy
-  // (keys contiguous) before P.V; bf16 V is used in place, MN-major.  The
-  // tensor core also truncates fp32 operands to tf32, so Q, K and V are first
-  // rounded to nearest in shared memory (epilogue warpgroup) and P is rounded
-  // before it is stored.
-  static constexpr bool kVt = kTF32;
-  static constexpr uint32_t kVtBytes = kVt ? D * BN * E : 0;
-  static constexpr uint32_t kVtPanelBytes = D * 128;  // 128-byte column of keys, all D rows
+  // V is used in place as an MN-major B operand (bf16 only: fp32 inputs run
+  // on the single-stage kernel of fa_tc_wide.cuh, which transposes V)
+  static constexpr bool kTransV = false;
   // shared memory
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQBytes;
-  static constexpr uint32_t kOffVt = kOffKV + NSLOT * kKVBytes;
-  static constexpr uint32_t kOffBar = kOffVt + 2 * kVtBytes;
-  static constexpr int kNumBars = 22 + 3 * NSLOT + 1;
+  static constexpr uint32_t kOffBar = kOffKV + NSLOT * kKVBytes;
+  static constexpr int kNumBars = 16 + 2 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMisc = kOffStats + 2 * BM * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
-  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, kVt ? 0u : 1u);
+  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, 1);
   static constexpr int kThreads = 512;
   // Register split (setmaxnreg) of the 4 warpgroups; 128 registers x 512
   // threads at launch, so the shares must add up to 4 x 128.
   static constexpr uint32_t kRegSoftmax = 184;
-  static constexpr uint32_t kRegEpilogue = kTF32 ? 88 : 64;  // fp32: also rounds and transposes
-  static constexpr uint32_t kRegProducer = kTF32 ? 56 : 80;  // load warp + MMA warp
+  static constexpr uint32_t kRegEpilogue = 64;
+  static constexpr uint32_t kRegProducer = 80;  // load warp + MMA warp
   static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 4 * 128, "register split");
   static_assert(kRegSoftmax >= 128 && kRegEpilogue <= 128 && kRegProducer <= 128,
                 "setmaxnreg.inc raises, setmaxnreg.dec lowers");
 
+  static_assert(!kTF32, "fp32 inputs run on the single-stage kernel (fa_tc_wide.cuh)");
   static_assert(D % kPanelElems == 0, "head dim must fill whole swizzle rows");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
   static_assert(2 * BN + 2 * D <= 512, "tensor memory budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert(!kVt || NSLOT % 2 == 0, "K and V tiles must alternate ring slots");
   static_assert(!(kSplit && kVarlen), "split-KV and varlen are separate instantiations");
 };
 
@@ -146,10 +142,6 @@ struct Bars {
   uint64_t* o_empty;    // [2] epilogue -> MMA (128 arrivals)
   uint64_t* st_full;    // [2] softmax -> epilogue: row stats written (128 arrivals)
   uint64_t* st_empty;   // [2] epilogue -> softmax (128 arrivals)
-  uint64_t* vt_full;    // [2] transposer -> MMA (V^T buffer ready; fp32 inputs only)
-  uint64_t* vt_empty;   // [2] MMA -> transposer
-  uint64_t* q_ready;    // [2] Q rounded to tf32 -> MMA (fp32 inputs only)
-  uint64_t* kv_ready;   // [NSLOT] K tile rounded to tf32 -> MMA (fp32 inputs only)
   uint64_t* kv_full;    // [NSLOT]
   uint64_t* kv_empty;   // [NSLOT]
   uint64_t* teardown;   // [1]
@@ -349,21 +341,26 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint3
 template <class C>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
                                          bool accumulate) {
-  // bf16: V is [BN keys][D] with D contiguous, an MN-major B operand (LBO =
-  // distance between 128-byte column panels, SBO = between 8-key row groups).
-  // fp32: V^T is [D][BN] with keys contiguous, K-major like K in Q.K^T.
-  const uint64_t b0 = C::kVt ? sdesc_sw128<16, 1024>(v_addr)
-                             : sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr);
+  if constexpr (C::kTransV) {
+    // tf32: V^T is [D][BN] with keys contiguous, a K-major B operand like K in
+    // Q.K^T, in panels of 32 keys (kVtPanelBytes apart); one MMA takes 8 keys
+    const uint64_t b0 = sdesc_sw128<16, 1024>(v_addr);
 #pragma unroll
-  for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
-    uint32_t b_off;
-    if constexpr (C::kVt) {
+    for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
       const uint32_t byte = kk * 32;
-      b_off = ((byte / 128) * C::kVtPanelBytes + byte % 128) >> 4;
-    } else {
-      b_off = (kk * C::kKStep * 128) >> 4;
+      const uint32_t b_off = ((byte / 128) * C::kVtPanelBytes + byte % 128) >> 4;
+      mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b0 + b_off, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
     }
-    mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b0 + b_off, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+  } else {
+    // bf16: V is [BN keys][D] with D contiguous, an MN-major B operand: LBO =
+    // distance between 128-byte column panels, SBO = between 8-key row
+    // groups; one MMA takes 16 keys
+    const uint64_t b0 = sdesc_sw128<C::kKVPanelBytes, 1024>(v_addr);
+#pragma unroll
+    for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
+      const uint32_t b_off = (kk * C::kKStep * 128) >> 4;
+      mma_ts<C::kTF32>(tmem_o, tmem_p + kk * 8, b0 + b_off, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+    }
   }
 }
 
@@ -374,15 +371,11 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
                             const Watchdog& wd) {
   const uint32_t q_addr0 = smem_u32(smem + C::kOffQ);
   const uint32_t kv_base = smem_u32(smem + C::kOffKV);
-  const uint32_t vt_base = smem_u32(smem + C::kOffVt);
-  uint32_t it = 0, tile_k = 0, vcount = 0;
+  uint32_t it = 0, tile_k = 0;
   uint32_t p_par[2] = {0, 0};
   bool ok = true;
-  // K tiles and Q tiles: straight from TMA (bf16) or after tf32 rounding (fp32)
-  uint64_t* const k_bar = C::kVt ? bars.kv_ready : bars.kv_full;
-  uint64_t* const q_bar = C::kVt ? bars.q_ready : bars.q_full;
   auto kv_wait = [&](uint32_t i) -> bool {
-    return warp_wait(&k_bar[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
+    return warp_wait(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
   };
   auto slot_addr = [&](uint32_t i) -> uint32_t { return kv_base + (i % C::NSLOT) * C::kKVBytes; };
 
@@ -396,7 +389,7 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     // S_s(0) = Q_s K_0^T for both stages
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
-      if (!(ok = warp_wait(&q_bar[s], par_k, wd, 0x21 + s) && (s == 1 || kv_wait(it)))) break;
+      if (!(ok = warp_wait(&bars.q_full[s], par_k, wd, 0x21 + s) && (s == 1 || kv_wait(it)))) break;
       tc_fence_after();
       if (elect_one()) {
         issue_qk<C>(tmem + C::col_s(s), q_addr0 + s * C::kQBytes, slot_addr(it));
@@ -412,14 +405,8 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     for (int j = 1; ok && j <= n; ++j) {
       const uint32_t iv = it, ik = it + 1;
       const bool last = (j == n);
-      const uint32_t vb = vcount & 1u;
-      bool v_ready;
-      if constexpr (C::kVt)
-        v_ready = warp_wait(&bars.vt_full[vb], (vcount >> 1) & 1u, wd, 0x27);
-      else
-        v_ready = kv_wait(iv);
-      if (!(ok = v_ready && (last || kv_wait(ik)))) break;
-      const uint32_t v_addr = C::kVt ? vt_base + vb * C::kVtBytes : slot_addr(iv);
+      if (!(ok = kv_wait(iv) && (last || kv_wait(ik)))) break;
+      const uint32_t v_addr = slot_addr(iv);
       const uint32_t k_addr = slot_addr(ik);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
@@ -429,7 +416,7 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
         tc_fence_after();
         if (elect_one()) {
           issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), v_addr, j > 1);
-          if (s == 1) tc_commit(C::kVt ? &bars.vt_empty[vb] : &bars.kv_empty[iv % C::NSLOT]);
+          if (s == 1) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
           if (last) {
             tc_commit(&bars.o_full[s]);
           } else {
@@ -442,7 +429,6 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
         __syncwarp();
       }
       if (!ok) break;
-      ++vcount;
       it += last ? 1 : 2;
     }
   }
@@ -567,25 +553,14 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
             if (c >= lim) v0 = 0.f;
             if (c + 1 >= lim) v1 = 0.f;
           }
-          if constexpr (C::kTF32) {  // l sums exactly the P that P.V uses
-            v0 = to_tf32(v0);
-            v1 = to_tf32(v1);
-          }
           e[k] = v0;
           e[k + 1] = v1;
           sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
         }
-        if constexpr (C::kTF32) {
-          uint32_t pw[32];
+        uint32_t pw[16];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) pw[k] = __float_as_uint(e[k]);
-          tmem_st32(tS + c0, pw);
-        } else {
-          uint32_t pw[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
-          tmem_st16(tS + c0 / 2, pw);
-        }
+        for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
+        tmem_st16(tS + c0 / 2, pw);
       }
 #pragma unroll
       for (int w = kAcc / 4; w > 0; w /= 2)
@@ -608,106 +583,20 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
 }
 
 // ------------------------------------------------------- epilogue warpgroup
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// fp32 inputs: V tile at ring index iv ([BN keys][D], 128-byte swizzled panels
-// of 32 d-values, as TMA wrote it) -> V^T buffer ([D][BN], panels of 32 keys).
-// Lane = key: each thread reads 16 bytes of its key row (the swizzle puts the
-// 8 rows of a phase on distinct banks) and writes 4 rows of V^T, where the 32
-// lanes fill one 128-byte row (no bank conflicts either).  The four warps
-// split the head dim.  Releases the ring slot and publishes the V^T buffer.
 template <class C>
-__device__ __forceinline__ bool transpose_v(uint8_t* smem, const Bars& bars, uint32_t iv,
-                                            uint32_t vcount, const Watchdog& wd) {
-  const uint32_t slot = iv % C::NSLOT;
-  const uint32_t vb = vcount & 1u;
-  if (!warp_wait(&bars.kv_full[slot], (iv / C::NSLOT) & 1u, wd, 0x50)) return false;
-  if (!warp_wait(&bars.vt_empty[vb], ((vcount >> 1) & 1u) ^ 1u, wd, 0x51)) return false;
-  const uint8_t* src = smem + C::kOffKV + slot * C::kKVBytes;
-  uint8_t* dst = smem + C::kOffVt + vb * C::kVtBytes;
-  const int wq = (threadIdx.x / 32) & 3;
-  const int lane = threadIdx.x & 31;
-  constexpr int kDPerWarp = C::D / 4;
-  const uint32_t wchunk = lane / 4, within = (lane % 4) * 4;
-#pragma unroll
-  for (int g = 0; g < C::BN / 32; ++g) {
-    const int k = g * 32 + lane;
-#pragma unroll 4
-    for (int n0 = wq * kDPerWarp; n0 < (wq + 1) * kDPerWarp; n0 += 4) {
-      const int pn = n0 / 32, chunk = (n0 % 32) / 4;
-      const float4 v = *reinterpret_cast<const float4*>(src + pn * C::kKVPanelBytes + k * 128 +
-                                                        ((chunk ^ (k & 7)) << 4));
-      const float vv[4] = {to_tf32(v.x), to_tf32(v.y), to_tf32(v.z), to_tf32(v.w)};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int nn = n0 + e;
-        *reinterpret_cast<float*>(dst + g * C::kVtPanelBytes + nn * 128 + ((wchunk ^ (nn & 7)) << 4) +
-                                  within) = vv[e];
-      }
-    }
-  }
-  fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-  named_barrier_sync(1, 128);
-  if ((threadIdx.x & 127) == 0) {
-    mbar_arrive(&bars.kv_empty[slot]);
-    mbar_arrive(&bars.vt_full[vb]);
-  }
-  return true;
-}
-
-// fp32 inputs: round a TMA-filled buffer to tf32 in place (elementwise, so the
-// swizzle does not matter; consecutive threads touch consecutive 16 bytes),
-// then publish it to the MMA warp through `ready`.
-__device__ __forceinline__ void round_tf32_publish(uint8_t* buf, uint32_t bytes, uint64_t* ready) {
-  for (uint32_t off = (threadIdx.x & 127) * 16; off < bytes; off += 128 * 16) {
-    float4* q = reinterpret_cast<float4*>(buf + off);
-    float4 v = *q;
-    v.x = to_tf32(v.x);
-    v.y = to_tf32(v.y);
-    v.z = to_tf32(v.z);
-    v.w = to_tf32(v.w);
-    *q = v;
-  }
-  fence_proxy_async_smem();
-  named_barrier_sync(1, 128);
-  if ((threadIdx.x & 127) == 0) mbar_arrive(ready);
-}
-
-template <class C>
-__device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const Bars& bars,
+__device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& bars,
                                  const float2* stats, const Watchdog& wd) {
   using T = typename C::Elem;
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  uint32_t tile_k = 0, it = 0, vcount = 0;
+  uint32_t tile_k = 0;
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
-    if constexpr (C::kVt) {
-      // same order as the load warp: Q_0, K_0, Q_1, V_0, then K_j, V_j
-      auto do_q = [&](int s) -> bool {
-        if (!warp_wait(&bars.q_full[s], tile_k & 1u, wd, 0x52 + s)) return false;
-        round_tf32_publish(smem + C::kOffQ + s * C::kQBytes, C::kQBytes, &bars.q_ready[s]);
-        return true;
-      };
-      auto do_k = [&](uint32_t i) -> bool {
-        const uint32_t slot = i % C::NSLOT;
-        if (!warp_wait(&bars.kv_full[slot], (i / C::NSLOT) & 1u, wd, 0x54)) return false;
-        round_tf32_publish(smem + C::kOffKV + slot * C::kKVBytes, C::kKVBytes, &bars.kv_ready[slot]);
-        return true;
-      };
-      if (!(do_q(0) && do_k(it) && do_q(1))) return;
-      for (int j = 0; j < ti.n_kv; ++j, it += 2, ++vcount) {
-        if (j > 0 && !do_k(it)) return;
-        if (!transpose_v<C>(smem, bars, it + 1, vcount, wd)) return;
-      }
-    }
 #pragma unroll 1
     for (int s = 0; s < 2; ++s) {
       if (!warp_wait(&bars.o_full[s], tile_k & 1u, wd, 0x40 + s)) return;
@@ -741,25 +630,16 @@ __device__ void tc_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem
             dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
                                  __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
         } else if (valid) {
-          if constexpr (C::kTF32) {
-            float4* dst = reinterpret_cast<float4*>(orow + c);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (c + 4 * k < dv)
-                dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
-                                     __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              if (c + 8 * k >= dv) break;
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * st.x, __uint_as_float(o[8 * k + 1]) * st.x);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * st.x, __uint_as_float(o[8 * k + 3]) * st.x);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * st.x, __uint_as_float(o[8 * k + 5]) * st.x);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * st.x, __uint_as_float(o[8 * k + 7]) * st.x);
-              dst[k] = w;
-            }
+          for (int k = 0; k < 4; ++k) {
+            if (c + 8 * k >= dv) break;
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * st.x, __uint_as_float(o[8 * k + 1]) * st.x);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * st.x, __uint_as_float(o[8 * k + 3]) * st.x);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * st.x, __uint_as_float(o[8 * k + 5]) * st.x);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * st.x, __uint_as_float(o[8 * k + 7]) * st.x);
+            dst[k] = w;
           }
         }
       }
@@ -790,13 +670,9 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   bars.o_empty = bar + 10;
   bars.st_full = bar + 12;
   bars.st_empty = bar + 14;
-  bars.vt_full = bar + 16;
-  bars.vt_empty = bar + 18;
-  bars.q_ready = bar + 20;
-  bars.kv_full = bar + 22;
-  bars.kv_empty = bar + 22 + C::NSLOT;
-  bars.kv_ready = bar + 22 + 2 * C::NSLOT;
-  bars.teardown = bar + 22 + 3 * C::NSLOT;
+  bars.kv_full = bar + 16;
+  bars.kv_empty = bar + 16 + C::NSLOT;
+  bars.teardown = bar + 16 + 2 * C::NSLOT;
   float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -813,14 +689,10 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&bars.o_empty[s], 128);
       mbar_init(&bars.st_full[s], 128);
       mbar_init(&bars.st_empty[s], 128);
-      mbar_init(&bars.vt_full[s], 1);
-      mbar_init(&bars.vt_empty[s], 1);
-      mbar_init(&bars.q_ready[s], 1);
     }
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
-      mbar_init(&bars.kv_ready[s], 1);
     }
     mbar_init(&bars.teardown[0], 1);
     *abort_flag = 0;
@@ -848,7 +720,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (warp == 13) tc_mma_role<C>(p, smem, tmem, bars, wd);
   } else if (wg == 2) {
     setmaxnreg_dec<C::kRegEpilogue>();
-    tc_epilogue_role<C>(p, smem, tmem, bars, stats, wd);
+    tc_epilogue_role<C>(p, tmem, bars, stats, wd);
   } else {
     setmaxnreg_inc<C::kRegSoftmax>();
     tc_softmax_role<C>(p, wg, tmem, bars, stats, wd);

@@ -6,6 +6,7 @@
 #include <atomic>
 
 #include "fa_launch.h"
+#include "fa_tc_wide.cuh"
 
 namespace fa {
 
@@ -22,6 +23,21 @@ static cudaError_t launch_tc(const TcLaunch& L) {
     ready[L.device].store(true, std::memory_order_release);
   }
   fa_tc_fwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaGetLastError();
+}
+
+// The same for the single-stage kernel (fa_tc_wide.cuh).
+template <class C>
+static cudaError_t launch_tc_wide(const TcLaunch& L) {
+  static std::atomic<bool> ready[kMaxDevices];
+  if (L.device < 0 || L.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!ready[L.device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(fa_tc_wide_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    ready[L.device].store(true, std::memory_order_release);
+  }
+  fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
   return cudaGetLastError();
 }
 

@@ -4,28 +4,15 @@
 // columns).  Measured against 64-key tiles with 4 or 5 slots, the wider key
 // tile is 15-20 % faster: the softmax's fixed cost per tile (waits, row max
 // tree, hand-offs) is paid half as often, and two slots still cover the loads.
-#include <atomic>
+#include <cuda_bf16.h>
 
-#include "fa_launch.h"
-#include "fa_tc_wide.cuh"
+#include "fa_tc_inst.cuh"
 
 namespace fa {
 
-using CfgWideD256 = TcWideCfg<256, 128, 2>;
+using CfgWideD256 = TcWideCfg<__nv_bfloat16, 256, 128, 2>;
 static_assert(CfgWideD256::BN == kWideKeyTile && CfgWideD256::BM == kWideQueryTile, "host tile geometry");
 
-cudaError_t launch_tc_wide_bf16_d256(const TcLaunch& L) {
-  using C = CfgWideD256;
-  static std::atomic<bool> ready[kMaxDevices];
-  if (L.device < 0 || L.device >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!ready[L.device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(fa_tc_wide_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    ready[L.device].store(true, std::memory_order_release);
-  }
-  fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
-  return cudaGetLastError();
-}
+cudaError_t launch_tc_wide_bf16_d256(const TcLaunch& L) { return launch_tc_wide<CfgWideD256>(L); }
 
 }  // namespace fa

@@ -1,18 +1,22 @@
-// fa_tc_wide.cuh -- the FlashAttention-2 forward for head dims above 128 (up
-// to 256; bf16), on the 5th-generation tensor cores.
+// fa_tc_wide.cuh -- the FlashAttention-2 forward with one 128-row query
+// block per CTA tile, on the 5th-generation tensor cores: bf16 head dims above
+// 128 (up to 256), and every fp32 input (kind::tf32, head dims up to 128).
 //
 // Same computation as fa_tc.cuh (the online softmax of "Extend Thunder with
 // CUDA-Python", flash_attention_reference, in the base-2 form of "Blackwell
 // Attention Example"), with V and O of up to 256 columns ("Blackwell
 // Attention Example", blackwell_attention: Q and K share d, V and O have Dv).
 //
-// Why a kernel of its own: a 128-row O accumulator of 256 fp32 columns takes
-// half of the 512 tensor-memory columns, so the two-stage ping-pong of
-// fa_tc.cuh (two query halves, each with its own S and O) no longer fits.
-// Here a CTA tile is one 128-row query block, and the overlap comes from
-// double-buffered S instead:
-//  * tensor memory: S_0 | S_1 (BN columns each) | O (D columns); key tile j
-//    uses S_{j mod 2}, P overwrites it in place;
+// Why a kernel of its own: a 128-row tile of Q, K or V of 512 bytes per row
+// (bf16 d = 256, fp32 d = 128) takes 64 KB of shared memory, so two query
+// halves (the two-stage ping-pong of fa_tc.cuh) and a K/V ring no longer fit
+// next to each other, and at bf16 d = 256 neither do their accumulators in
+// tensor memory.  Here a CTA tile is one 128-row query block, and the overlap
+// comes from double-buffered S instead:
+//  * tensor memory: S_0 | S_1 (BN columns each) | O_0 [| O_1] (D columns; a
+//    second O buffer where it fits, so that the first P.V of the next tile
+//    need not wait for the epilogue); key tile j uses S_{j mod 2}, P
+//    overwrites it in place (bf16 pairs, or tf32-rounded fp32);
 //  * the MMA warp issues S(0), S(1), then per key tile j: O += P(j) V_j and
 //    S(j+2) = Q K_{j+2}^T, so the softmax of tile j+1 runs while the tensor
 //    core computes P(j) V_j and S(j+2) (tcgen05 MMAs from one thread execute in
@@ -22,7 +26,17 @@
 //    finish before it scales O;
 //  * ring order of the K/V tiles: K_0, K_1, then V_j, K_{j+2} -- the order in
 //    which the MMA warp consumes them;
-//  * warpgroup 1 has no role (its registers go to the softmax);
+//  * fp32 inputs: tf32-typed tensor maps round Q, K and V to tf32 during the
+//    copy.  The tensor core takes tf32 operands K-major only, so V (keys x
+//    dims, dims contiguous) must become V^T (dims x keys, keys contiguous):
+//    warpgroup 1 transposes each V tile in shared memory -- in its ring slot
+//    when the tile is square (D = BN), else into a buffer of its own -- with a
+//    lane mapping under which no two lanes of a quarter-warp touch the same
+//    bank group (transpose_v_tile).  For bf16, V is used in place as an
+//    MN-major operand and warpgroup 1 has no role;
+//  * split-KV instantiations (SPLIT): work unit u is the key range u mod s of
+//    tile u / s, and writes a normalised partial O and its LSE to the caller's
+//    workspace (merged by fa_combine_kernel), as in fa_tc.cuh;
 //  * every wait is bounded (Watchdog), as in fa_tc.cuh.
 #pragma once
 
@@ -30,54 +44,64 @@
 
 namespace fa {
 
-template <int D_, int BN_, int NSLOT_>
+template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false>
 struct TcWideCfg {
-  using Elem = __nv_bfloat16;
-  static constexpr bool kTF32 = false;
-  static constexpr bool kVt = false;
-  static constexpr int E = 2;
+  using Elem = T;
+  static constexpr bool kSplit = SPLIT_;
+  static constexpr bool kVarlen = false;
+  static constexpr bool kTF32 = sizeof(T) == 4;
+  static constexpr int E = sizeof(T);
   static constexpr int D = D_;
   static constexpr int BN = BN_;
   static constexpr int NSLOT = NSLOT_;
   static constexpr int BM = 128;                 // query rows of a CTA tile = TMEM lanes
-  static constexpr int kPanelElems = 64;         // bf16 values per 128-byte swizzle row
+  static constexpr int kPanelElems = 128 / E;    // elements per 128-byte swizzle row
   static constexpr int kPanels = D / kPanelElems;
-  static constexpr int kKStep = 16;              // K extent of one kind::f16 MMA
+  static constexpr int kKStep = 32 / E;          // K extent of one MMA (16 bf16, 8 tf32)
   static constexpr uint32_t kQPanelBytes = BM * 128;
   static constexpr uint32_t kKVPanelBytes = BN * 128;
-  static constexpr uint32_t kVtPanelBytes = 0;
   static constexpr uint32_t kQBytes = BM * D * E;
   static constexpr uint32_t kKVBytes = BN * D * E;
-  // tensor-memory columns: S_0 | S_1 | O
+  // fp32: V^T made by warpgroup 1 (K-major B operand of P.V): panels of 32
+  // keys, each D rows of 128 bytes
+  static constexpr bool kTransV = kTF32;
+  static constexpr bool kVtInPlace = kTransV && D == BN;
+  static constexpr uint32_t kVtPanelBytes = D * 128;
+  static constexpr uint32_t kVtBytes = (kTransV && !kVtInPlace) ? D * BN * E : 0;
+  // tensor-memory columns: S_0 | S_1 | O_0 [| O_1]
+  static constexpr int kOBufs = (2 * BN + 2 * D <= 512) ? 2 : 1;
   __host__ __device__ static constexpr uint32_t col_s(uint32_t b) { return b * BN; }
-  static constexpr uint32_t kColO = 2 * BN;
+  __host__ __device__ static constexpr uint32_t col_o(uint32_t b) { return 2 * BN + b * D; }
   static constexpr uint32_t kTmemCols = 512;
-  // shared memory: Q, the K/V ring, barriers, row statistics
+  // shared memory: Q, the K/V ring, V^T (fp32, non-square tiles), barriers, row statistics
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = kQBytes;
-  static constexpr uint32_t kOffBar = kOffKV + NSLOT * kKVBytes;
-  static constexpr int kNumBars = 11 + 2 * NSLOT + 1;
+  static constexpr uint32_t kOffVt = kOffKV + NSLOT * kKVBytes;
+  static constexpr uint32_t kOffBar = kOffVt + kVtBytes;
+  static constexpr int kNumBars = 15 + 3 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMisc = kOffStats + BM * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
-  static constexpr uint32_t kIdescS = make_idesc(1u, 128, BN, 0, 0);
-  static constexpr uint32_t kIdescO = make_idesc(1u, 128, D, 0, 1);
+  static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
+  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, kTransV ? 0u : 1u);
   static constexpr int kThreads = 512;
   // Register split (setmaxnreg): 128 registers x 512 threads at launch; the
   // four warpgroups' shares add up to 4 x 128.  The softmax raises its share
   // (setmaxnreg.inc), the others lower theirs (setmaxnreg.dec only lowers).
   static constexpr uint32_t kRegSoftmax = 232;
-  static constexpr uint32_t kRegIdle = 56;
-  static constexpr uint32_t kRegEpilogue = 112;
+  static constexpr uint32_t kRegWg1 = kTransV ? 80 : 56;   // V transposer (fp32) or idle
+  static constexpr uint32_t kRegEpilogue = kTransV ? 88 : 112;
   static constexpr uint32_t kRegProducer = 112;
-  static_assert(kRegSoftmax + kRegIdle + kRegEpilogue + kRegProducer == 4 * 128, "register split");
+  static_assert(kRegSoftmax + kRegWg1 + kRegEpilogue + kRegProducer == 4 * 128, "register split");
   static_assert(kRegSoftmax >= 128 && kRegSoftmax <= 256 && kRegSoftmax % 8 == 0, "setmaxnreg.inc share");
-  static_assert(kRegIdle <= 128 && kRegEpilogue <= 128 && kRegProducer <= 128, "setmaxnreg.dec shares");
-  static_assert(kRegIdle >= 24 && kRegIdle % 8 == 0 && kRegEpilogue % 8 == 0 && kRegProducer % 8 == 0,
+  static_assert(kRegWg1 <= 128 && kRegEpilogue <= 128 && kRegProducer <= 128, "setmaxnreg.dec shares");
+  static_assert(kRegWg1 >= 24 && kRegWg1 % 8 == 0 && kRegEpilogue % 8 == 0 && kRegProducer % 8 == 0,
                 "setmaxnreg share granularity");
   static_assert(D % kPanelElems == 0 && D <= 256, "head dim: whole swizzle rows, at most 256 (MMA N)");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
-  static_assert(2 * BN + D <= 512, "tensor memory budget");
+  static_assert(!kTransV || (D % 32 == 0 && BN % 32 == 0), "transpose works on 32 x 32 blocks");
+  static_assert(2 * BN + kOBufs * D <= 512, "tensor memory budget");
+  static_assert(NSLOT <= 8, "ring slots (the load warp's per-slot bookkeeping)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -87,24 +111,32 @@ struct WideBars {
   uint64_t* s_full;    // [2] MMA -> softmax
   uint64_t* p_full;    // [2] softmax -> MMA (128 arrivals)
   uint64_t* pv_done;   // MMA -> softmax: one completion per P.V (lazy rescale)
-  uint64_t* o_full;    // MMA -> epilogue (last P.V of the tile done)
-  uint64_t* o_empty;   // epilogue -> MMA (128 arrivals)
+  uint64_t* o_full;    // [2] MMA -> epilogue (last P.V of a tile done), per O buffer
+  uint64_t* o_empty;   // [2] epilogue -> MMA (128 arrivals), per O buffer
   uint64_t* st_full;   // softmax -> epilogue (128 arrivals)
   uint64_t* st_empty;  // epilogue -> softmax (128 arrivals)
-  uint64_t* kv_full;   // [NSLOT]
+  uint64_t* vt_full;   // transposer -> MMA: one completion per V^T tile (fp32; 128 arrivals)
+  uint64_t* vt_empty;  // MMA -> transposer: the P.V that read the last V^T is done (fp32)
+  uint64_t* kv_full;   // [NSLOT] TMA -> MMA (fp32: V tiles only arrive here, no bytes)
   uint64_t* kv_empty;  // [NSLOT]
+  uint64_t* v_full;    // [NSLOT] TMA -> transposer: the bytes of V tiles (fp32)
   uint64_t* teardown;  // [1]
 };
 
 // Tile order as in fa_tc.cuh (head groups for K/V reuse in L2, the blocks of a
 // group's heads interleaved, the last -- longest under the causal mask --
-// first), with 128-row query blocks: n_qblk = ceil(N_q / 128).
+// first), with 128-row query blocks: n_qblk = ceil(N_q / 128).  Split-KV:
+// work unit u is split u % n_split of tile u / n_split; the tile's key tiles
+// are cut into min(n_split, #tiles) balanced ranges and the other splits are
+// empty (n_kv = 0).
 template <class C>
 __device__ __forceinline__ TileInfo wide_tile_info(const TcParams& p, int u) {
+  const int t = C::kSplit ? u / p.n_split : u;
+  const int split = C::kSplit ? u - t * p.n_split : 0;
   const int BH = p.B * p.H;
   const int per_group = p.head_group * p.n_qblk;
-  const int g = u / per_group;
-  const int r = u - g * per_group;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
   const int heads = min(p.head_group, BH - g * p.head_group);
   const int qi = r / heads;
   const int bh = g * p.head_group + (r - qi * heads);
@@ -117,37 +149,79 @@ __device__ __forceinline__ TileInfo wide_tile_info(const TcParams& p, int u) {
   ti.qrow0 = ti.krow0 = 0;
   ti.len_q = ti.len_k = 0;
   ti.coff = kNoCausal;
-  ti.split = 0;
-  ti.j0 = 0;
+  ti.split = split;
   int kv_end = p.N_k;
   if (p.causal != kNoCausal) kv_end = min(kv_end, min(ti.q0 + C::BM, p.N_q) + p.causal);
   const int n_tot = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
-  ti.n_kv = n_tot > 0 ? n_tot : 1;  // a block that sees no key takes one fully masked key tile
+  if constexpr (!C::kSplit) {
+    ti.j0 = 0;
+    ti.n_kv = n_tot > 0 ? n_tot : 1;  // a block that sees no key takes one fully masked key tile
+    return ti;
+  }
+  const int s_eff = min(p.n_split, n_tot);
+  if (split >= s_eff) {
+    ti.j0 = 0;
+    ti.n_kv = 0;
+  } else {
+    ti.j0 = split * n_tot / s_eff;
+    ti.n_kv = (split + 1) * n_tot / s_eff - ti.j0;
+  }
   return ti;
 }
 
+// Work units that take a pipeline phase (split-KV: units with keys).
+template <class C>
+__device__ __forceinline__ bool wide_counted(const TileInfo& ti) {
+  return C::kSplit ? ti.n_kv != 0 : true;
+}
+
 // ------------------------------------------------------------- load warp
+// fp32 inputs: a V tile's bytes complete on v_full[slot], which only the
+// transposer waits on -- every phase of it, in order -- and the load warp
+// arrives on kv_full[slot] without bytes, so that the phases of kv_full still
+// count every ring entry for the MMA warp's waits on K tiles.  (A waiter that
+// skipped phases could see a stale parity and take a K tile for a V tile.)
 template <class C>
 __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                const TcParams& p, uint8_t* smem, const WideBars& bars, const Watchdog& wd) {
   const uint64_t pol_q = l2_policy_evict_first();
   const uint64_t pol_kv = l2_policy_evict_last();
   uint32_t it = 0, q_armed = 0, tile_k = 0;
+  uint32_t withheld = ~0u;   // ring entry skipped by the test hook, if any
+  uint32_t v_loads[C::NSLOT] = {};  // fp32: V tiles issued per slot
+  uint32_t last_is_v = 0;    // fp32: bit s = the last entry issued into slot s was a V tile
   bool ok = true;
-  auto load_kv = [&](const CUtensorMap* map, int j, const TileInfo& ti) -> bool {
+  auto load_kv = [&](const CUtensorMap* map, int j, const TileInfo& ti, bool withhold, bool is_v) -> bool {
     const uint32_t slot = it % C::NSLOT;
     if (!mbar_wait(&bars.kv_empty[slot], ((it / C::NSLOT) & 1u) ^ 1u, wd, 0x81)) return false;
     ++it;
-    mbar_arrive_expect_tx(&bars.kv_full[slot], C::kKVBytes);
-    uint8_t* dst = smem + C::kOffKV + slot * C::kKVBytes;
+    if (withhold) {  // test hook: this tile never arrives
+      withheld = it - 1;
+      return true;
+    }
+    uint64_t* done = &bars.kv_full[slot];
+    if (C::kTransV) {
+      if (is_v) {
+        done = &bars.v_full[slot];
+        ++v_loads[slot];
+        last_is_v |= 1u << slot;
+      } else {
+        last_is_v &= ~(1u << slot);
+      }
+    }
+    mbar_arrive_expect_tx(done, C::kKVBytes);
 #pragma unroll
     for (int pn = 0; pn < C::kPanels; ++pn)
-      tma_load_4d(map, &bars.kv_full[slot], dst + pn * C::kKVPanelBytes, pn * C::kPanelElems, j * C::BN, ti.hk,
-                  ti.b, pol_kv);
+      tma_load_4d(map, done, smem + C::kOffKV + slot * C::kKVBytes + pn * C::kKVPanelBytes, pn * C::kPanelElems,
+                  (ti.j0 + j) * C::BN, ti.hk, ti.b, pol_kv);
+    if (C::kTransV && is_v) mbar_arrive(&bars.kv_full[slot]);
     return true;
   };
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++tile_k) {
+  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
+    if (!wide_counted<C>(ti)) continue;
+    // test hook (host-set flag): block 0 never delivers the second K tile of its first tile
+    const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
     if (!(ok = mbar_wait(&bars.q_empty[0], (tile_k & 1u) ^ 1u, wd, 0x80))) break;
     mbar_arrive_expect_tx(&bars.q_full[0], C::kQBytes);
 #pragma unroll
@@ -155,16 +229,144 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
       tma_load_4d(tmQ, &bars.q_full[0], smem + C::kOffQ + pn * C::kQPanelBytes, pn * C::kPanelElems, ti.q0, ti.h,
                   ti.b, pol_q);
     ++q_armed;
-    ok = load_kv(tmK, 0, ti) && (ti.n_kv < 2 || load_kv(tmK, 1, ti));
+    ++tile_k;
+    ok = load_kv(tmK, 0, ti, false, false) && (ti.n_kv < 2 || load_kv(tmK, 1, ti, inject, false));
     for (int j = 0; ok && j < ti.n_kv; ++j)
-      ok = load_kv(tmV, j, ti) && (j + 2 >= ti.n_kv || load_kv(tmK, j + 2, ti));
+      ok = load_kv(tmV, j, ti, false, true) && (j + 2 >= ti.n_kv || load_kv(tmK, j + 2, ti, false, false));
   }
   if (!ok) {
-    // let copies in flight land before the CTA's shared memory goes away
+    // let copies in flight land before the CTA's shared memory goes away (only
+    // the last entry of each slot can still be in flight)
     const uint64_t limit = 100000000ull;  // 100 ms
-    for (uint32_t i = it > C::NSLOT ? it - C::NSLOT : 0; i < it; ++i)
-      mbar_drain(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, limit);
+    for (uint32_t i = it > C::NSLOT ? it - C::NSLOT : 0; i < it; ++i) {
+      if (i == withheld) continue;
+      const uint32_t slot = i % C::NSLOT;
+      if (C::kTransV && ((last_is_v >> slot) & 1u))
+        mbar_drain(&bars.v_full[slot], (v_loads[slot] - 1) & 1u, limit);
+      else
+        mbar_drain(&bars.kv_full[slot], (i / C::NSLOT) & 1u, limit);
+    }
     if (q_armed) mbar_drain(&bars.q_full[0], (q_armed - 1) & 1u, limit);
+  }
+}
+
+// -------------------------------------------------------- V^T (fp32 inputs)
+// One V tile [BN keys][D] as TMA wrote it (D / 32 panels of BN rows x 128
+// bytes, 128-byte swizzle: the 16-byte chunk c of row k sits at chunk
+// position c ^ (k & 7)) becomes the K-major V^T [D][BN] (BN / 32 panels of D
+// rows x 128 bytes, same swizzle), at dst; dst == src when kInPlace (BN == D:
+// V^T then has exactly V's layout with the roles of keys and dims swapped).
+//
+// Work is split in 4 x 4 sub-blocks (keys 4a..4a+3, dims 4b..4b+3): a lane
+// reads the four 16-byte rows of its sub-block, transposes them in registers
+// and writes four 16-byte rows of V^T.  A quarter-warp (8 lanes, one 128-byte
+// wavefront of a 16-byte access) takes, in round t of a 32 x 32 block, the
+// sub-blocks (a, b) = ((i + t) mod 8, i) for its lanes i: the bank groups it
+// reads, b ^ ((4a + r) mod 8), and writes, a ^ ((4b + e) mod 8), are then
+// eight distinct values for every r and e, so no access has a bank conflict.
+// In place, a lane swaps sub-block (a, b) with (b, a): blocks (A, B) and
+// (B, A) of 32 x 32 are done together (A < B), and the diagonal blocks take
+// rounds 0 (sub-blocks on the diagonal, transposed alone) to 4 (half the
+// lanes), so that every pair is swapped exactly once.  128 threads.
+template <int BN, int D, bool kInPlace>
+__device__ __forceinline__ void transpose_v_tile(uint8_t* src, uint8_t* dst, int tid) {
+  const int quarter = tid >> 3;  // 16 quarter-warps
+  const int i = tid & 7;
+  // the 16-byte piece of key row k that holds dims 4b..4b+3
+  auto load4 = [&](int a, int b, float4 (&v)[4]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int k = 4 * a + r;
+      v[r] = *reinterpret_cast<const float4*>(src + (b >> 3) * (BN * 128) + k * 128 + (((b & 7) ^ (k & 7)) << 4));
+    }
+  };
+  // V^T rows 4b..4b+3 (dims), key chunk a: keys 4a..4a+3
+  auto store4 = [&](int a, int b, const float4 (&v)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = 4 * b + e;
+      const float4 w = e == 0 ? make_float4(v[0].x, v[1].x, v[2].x, v[3].x)
+                     : e == 1 ? make_float4(v[0].y, v[1].y, v[2].y, v[3].y)
+                     : e == 2 ? make_float4(v[0].z, v[1].z, v[2].z, v[3].z)
+                              : make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+      *reinterpret_cast<float4*>(dst + (a >> 3) * (D * 128) + n * 128 + (((a & 7) ^ (n & 7)) << 4)) = w;
+    }
+  };
+  if constexpr (!kInPlace) {
+    constexpr int kItems = (BN / 32) * (D / 32) * 8;
+#pragma unroll 1
+    for (int item = quarter; item < kItems; item += 16) {
+      const int sb = item >> 3, t = item & 7;
+      const int A = sb / (D / 32), B = sb % (D / 32);
+      const int a = 8 * A + ((i + t) & 7), b = 8 * B + i;
+      float4 v[4];
+      load4(a, b, v);
+      store4(a, b, v);
+    }
+  } else {
+    static_assert(BN == D, "in-place transpose needs a square tile");
+    constexpr int P = BN / 32;
+    constexpr int kOff = P * (P - 1) / 2 * 8;  // rounds of the off-diagonal block pairs
+    constexpr int kItems = kOff + P * 5;
+#pragma unroll 1
+    for (int item = quarter; item < kItems; item += 16) {
+      int A, B, t;
+      if (item < kOff) {
+        int pr = item >> 3;
+        t = item & 7;
+        A = 0;
+        while (pr >= P - 1 - A) {
+          pr -= P - 1 - A;
+          ++A;
+        }
+        B = A + 1 + pr;
+      } else {
+        A = B = (item - kOff) / 5;
+        t = (item - kOff) % 5;
+        if (t == 4 && i >= 4) continue;
+      }
+      const int a = 8 * A + ((i + t) & 7), b = 8 * B + i;
+      float4 v[4];
+      load4(a, b, v);
+      if (A == B && t == 0) {  // a sub-block on the diagonal: transposed alone
+        store4(a, b, v);
+      } else {
+        float4 w[4];
+        load4(b, a, w);
+        store4(a, b, v);  // (a, b)^T lands where (b, a) was
+        store4(b, a, w);
+      }
+    }
+  }
+}
+
+// Warpgroup 1 for fp32 inputs: transposes each V tile in the order the load
+// warp delivers them, once the P.V that read the previous V^T is done.  Every
+// thread publishes its own writes (proxy fence, then an arrival on vt_full,
+// which counts 128), so no warp ever waits for another one: a warp that gives
+// up on a wait cannot leave the others stuck.
+template <class C>
+__device__ void wide_transpose_role(const TcParams& p, uint8_t* smem, const WideBars& bars, const Watchdog& wd) {
+  const int tid = threadIdx.x & 127;
+  uint32_t it = 0, vcount = 0;
+  uint32_t v_seen[C::NSLOT] = {};  // V tiles taken per slot (phases of v_full[slot])
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    const TileInfo ti = wide_tile_info<C>(p, u);
+    if (!wide_counted<C>(ti)) continue;
+    it += ti.n_kv < 2 ? 1 : 2;  // K_0 [, K_1]
+    for (int j = 0; j < ti.n_kv; ++j, ++vcount) {
+      const uint32_t iv = it++;
+      if (j + 2 < ti.n_kv) ++it;  // K_{j+2} follows V_j
+      const uint32_t slot = iv % C::NSLOT;
+      if (!warp_wait(&bars.v_full[slot], v_seen[slot] & 1u, wd, 0x8b)) return;
+      ++v_seen[slot];
+      if (!warp_wait(&bars.vt_empty[0], (vcount & 1u) ^ 1u, wd, 0x8c)) return;
+      uint8_t* src = smem + C::kOffKV + slot * C::kKVBytes;
+      uint8_t* dst = C::kVtInPlace ? src : smem + C::kOffVt;
+      transpose_v_tile<C::BN, C::D, C::kVtInPlace>(src, dst, tid);
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+      mbar_arrive(&bars.vt_full[0]);
+    }
   }
 }
 
@@ -174,7 +376,9 @@ __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, c
                               const Watchdog& wd) {
   const uint32_t q_addr = smem_u32(smem + C::kOffQ);
   const uint32_t kv_base = smem_u32(smem + C::kOffKV);
+  const uint32_t vt_base = smem_u32(smem + C::kOffVt);
   uint32_t it = 0, tile_k = 0, g = 0;  // g: S tiles issued so far (all tiles of this CTA)
+  uint32_t vcount = 0;                 // V tiles consumed so far
   bool ok = true;
   auto kv_wait = [&](uint32_t i) -> bool {
     return warp_wait(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x82);
@@ -196,25 +400,38 @@ __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, c
     ++g;
     return true;
   };
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++tile_k) {
+  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
+    if (!wide_counted<C>(ti)) continue;
     const int n = ti.n_kv;
     const uint32_t g0 = g;  // S index of key tile 0 of this tile
+    const uint32_t ob = tile_k % C::kOBufs;          // O buffer of this tile
+    const uint32_t o_par = (tile_k / C::kOBufs) & 1u;
     if (!(ok = warp_wait(&bars.q_full[0], tile_k & 1u, wd, 0x83))) break;
+    ++tile_k;
     if (!(ok = qk(n == 1))) break;
     if (n > 1 && !(ok = qk(n == 2))) break;
-    for (int j = 0; ok && j < n; ++j) {
+    for (int j = 0; ok && j < n; ++j, ++vcount) {
       const uint32_t gj = g0 + j;
       const uint32_t iv = it++;
       if (!(ok = warp_wait(&bars.p_full[gj & 1u], (gj >> 1) & 1u, wd, 0x84))) break;
-      if (j == 0 && !(ok = warp_wait(&bars.o_empty[0], (tile_k & 1u) ^ 1u, wd, 0x85))) break;
-      if (!(ok = kv_wait(iv))) break;
+      if (j == 0 && !(ok = warp_wait(&bars.o_empty[ob], o_par ^ 1u, wd, 0x85))) break;
+      if constexpr (C::kTransV)
+        ok = warp_wait(&bars.vt_full[0], vcount & 1u, wd, 0x86);
+      else
+        ok = kv_wait(iv);
+      if (!ok) break;
+      const uint32_t v_addr = (C::kTransV && !C::kVtInPlace) ? vt_base : slot_addr(iv);
       tc_fence_after();
       if (elect_one()) {
-        issue_pv<C>(tmem + C::kColO, tmem + C::col_s(gj & 1u), slot_addr(iv), j > 0);
-        tc_commit(&bars.kv_empty[iv % C::NSLOT]);
+        // the ring slot of V_j: once V^T sits in its own buffer the slot is
+        // free now (the transposer's reads are done); else after the P.V
+        if (C::kTransV && !C::kVtInPlace) mbar_arrive(&bars.kv_empty[iv % C::NSLOT]);
+        issue_pv<C>(tmem + C::col_o(ob), tmem + C::col_s(gj & 1u), v_addr, j > 0);
+        if (C::kTransV) tc_commit(&bars.vt_empty[0]);
+        if (!C::kTransV || C::kVtInPlace) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
         tc_commit(&bars.pv_done[0]);
-        if (j == n - 1) tc_commit(&bars.o_full[0]);
+        if (j == n - 1) tc_commit(&bars.o_full[ob]);
       }
       __syncwarp();
       if (j + 2 < n) ok = qk(j + 2 == n - 1);
@@ -236,19 +453,20 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t tO = tmem + lane_base + C::kColO;
   const float sc = p.scale_log2;
   uint32_t gs = 0, tile_k = 0;  // gs: key tiles processed so far (= S index)
 
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++tile_k) {
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
+    if (!wide_counted<C>(ti)) continue;
+    const uint32_t tO = tmem + lane_base + C::col_o(tile_k % C::kOBufs);
     const int q = ti.q0 + row;
     const int vis_end = p.causal != kNoCausal ? min(p.N_k, q + 1 + p.causal) : p.N_k;  // keys < vis_end are visible
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < ti.n_kv; ++j, ++gs) {
       const uint32_t b = gs & 1u;
       const uint32_t tS = tmem + lane_base + C::col_s(b);
-      if (!warp_wait(&bars.s_full[b], (gs >> 1) & 1u, wd, 0x86)) return;
+      if (!warp_wait(&bars.s_full[b], (gs >> 1) & 1u, wd, 0x87)) return;
       tc_fence_after();
       uint32_t s[C::BN];
 #pragma unroll
@@ -257,7 +475,7 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
 #pragma unroll
       for (int c = 32; c < C::BN; c += 32) reg_fence32(s + c);
 
-      const int lim = vis_end - j * C::BN;  // columns c < lim are visible
+      const int lim = vis_end - (ti.j0 + j) * C::BN;  // columns c < lim are visible
       const bool need_mask = __any_sync(0xffffffffu, lim < C::BN);
       constexpr int kAcc = 8;
       float acc[kAcc];
@@ -300,7 +518,7 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
         // O holds sum_{i<j-1} P_i V_i plus the P(j-1).V still in flight: wait
         // for it (completion number gs - 1 of pv_done; P.V(j) needs P(j), which
         // is not written yet, so pv_done is at most one completion ahead).
-        if (!warp_wait(&bars.pv_done[0], (gs - 1) & 1u, wd, 0x87)) return;
+        if (!warp_wait(&bars.pv_done[0], (gs - 1) & 1u, wd, 0x88)) return;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < C::D; c += 32) {
@@ -329,14 +547,25 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
             if (c >= lim) v0 = 0.f;
             if (c + 1 >= lim) v1 = 0.f;
           }
+          if constexpr (C::kTF32) {  // l sums exactly the P that P.V uses
+            v0 = to_tf32(v0);
+            v1 = to_tf32(v1);
+          }
           e[k] = v0;
           e[k + 1] = v1;
           sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
         }
-        uint32_t pw[16];
+        if constexpr (C::kTF32) {
+          uint32_t pw[32];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
-        tmem_st16(tS + c0 / 2, pw);
+          for (int k = 0; k < 32; ++k) pw[k] = __float_as_uint(e[k]);
+          tmem_st32(tS + c0, pw);
+        } else {
+          uint32_t pw[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
+          tmem_st16(tS + c0 / 2, pw);
+        }
       }
 #pragma unroll
       for (int w = kAcc / 4; w > 0; w /= 2)
@@ -348,8 +577,9 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
       mbar_arrive(&bars.p_full[b]);
     }
     // row statistics for the epilogue: 1/l and LSE (natural log); l = 0 only
-    // for a row that sees no key (then O = 0 and LSE = -inf)
-    if (!warp_wait(&bars.st_empty[0], (tile_k & 1u) ^ 1u, wd, 0x88)) return;
+    // for a row that sees no key of the unit (then O = 0 and LSE = -inf)
+    if (!warp_wait(&bars.st_empty[0], (tile_k & 1u) ^ 1u, wd, 0x89)) return;
+    ++tile_k;
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     stats[row] = make_float2(inv_l, (m_run + __log2f(l_run)) * kLn2);
     mbar_arrive(&bars.st_full[0]);
@@ -364,26 +594,42 @@ __device__ void wide_epilogue_role(const TcParams& p, uint32_t tmem, const WideB
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
-  const uint32_t tO = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColO;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   uint32_t tile_k = 0;
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++tile_k) {
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
-    if (!warp_wait(&bars.o_full[0], tile_k & 1u, wd, 0x89)) return;
-    if (!warp_wait(&bars.st_full[0], tile_k & 1u, wd, 0x8a)) return;
+    if (!wide_counted<C>(ti)) continue;
+    const uint32_t ob = tile_k % C::kOBufs;
+    if (!warp_wait(&bars.o_full[ob], (tile_k / C::kOBufs) & 1u, wd, 0x8a)) return;
+    if (!warp_wait(&bars.st_full[0], tile_k & 1u, wd, 0x8d)) return;
+    ++tile_k;
     tc_fence_after();
     const float2 st = stats[row];
     mbar_arrive(&bars.st_empty[0]);
+    const uint32_t tO = tmem + lane_base + C::col_o(ob);
     const int q = ti.q0 + row;
     const bool valid = q < p.N_q;
     T* orow = reinterpret_cast<T*>(p.O) + ti.b * p.o_stride[0] + ti.h * p.o_stride[1] +
               static_cast<long long>(q) * p.o_stride[2];
-    const int dv = p.dv;  // columns of O to store (<= D)
+    // split-KV: this unit's normalised partial O (fp32) and LSE go to the
+    // workspace; the combine kernel merges the splits into O and LSE
+    const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
+    const int dv = C::kSplit ? C::D : p.dv;  // columns of O to store (<= D)
 #pragma unroll 1
     for (int c = 0; c < dv; c += 32) {
       uint32_t o[32];
       tmem_ld32(tO + c, o);
       tmem_ld_wait32(o);
-      if (valid) {
+      if (!valid) continue;
+      if constexpr (C::kSplit || C::kTF32) {
+        float4* dst = C::kSplit ? reinterpret_cast<float4*>(p.ws_o + wrow * C::D + c)
+                                : reinterpret_cast<float4*>(reinterpret_cast<float*>(orow) + c);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (c + 4 * k < dv)
+            dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
+                                 __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
+      } else {
         uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -398,8 +644,10 @@ __device__ void wide_epilogue_role(const TcParams& p, uint32_t tmem, const WideB
       }
     }
     tc_fence_before();
-    mbar_arrive(&bars.o_empty[0]);
-    if (valid && p.LSE)
+    mbar_arrive(&bars.o_empty[ob]);
+    if (valid && C::kSplit)
+      p.ws_lse[wrow] = st.y;
+    else if (valid && p.LSE)
       p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
   }
 }
@@ -419,12 +667,15 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   bars.p_full = bar + 4;
   bars.pv_done = bar + 6;
   bars.o_full = bar + 7;
-  bars.o_empty = bar + 8;
-  bars.st_full = bar + 9;
-  bars.st_empty = bar + 10;
-  bars.kv_full = bar + 11;
-  bars.kv_empty = bar + 11 + C::NSLOT;
-  bars.teardown = bar + 11 + 2 * C::NSLOT;
+  bars.o_empty = bar + 9;
+  bars.st_full = bar + 11;
+  bars.st_empty = bar + 12;
+  bars.vt_full = bar + 13;
+  bars.vt_empty = bar + 14;
+  bars.kv_full = bar + 15;
+  bars.kv_empty = bar + 15 + C::NSLOT;
+  bars.v_full = bar + 15 + 2 * C::NSLOT;
+  bars.teardown = bar + 15 + 3 * C::NSLOT;
   float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -437,15 +688,18 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.p_full[b], 128);
+      mbar_init(&bars.o_full[b], 1);
+      mbar_init(&bars.o_empty[b], 128);
     }
     mbar_init(&bars.pv_done[0], 1);
-    mbar_init(&bars.o_full[0], 1);
-    mbar_init(&bars.o_empty[0], 128);
     mbar_init(&bars.st_full[0], 128);
     mbar_init(&bars.st_empty[0], 128);
+    mbar_init(&bars.vt_full[0], 128);
+    mbar_init(&bars.vt_empty[0], 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
     }
     mbar_init(&bars.teardown[0], 1);
     *abort_flag = 0;
@@ -475,7 +729,8 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     setmaxnreg_dec<C::kRegEpilogue>();
     wide_epilogue_role<C>(p, tmem, bars, stats, wd);
   } else if (wg == 1) {
-    setmaxnreg_dec<C::kRegIdle>();
+    setmaxnreg_dec<C::kRegWg1>();
+    if constexpr (C::kTransV) wide_transpose_role<C>(p, smem, bars, wd);
   } else {
     setmaxnreg_inc<C::kRegSoftmax>();
     wide_softmax_role<C>(p, tmem, bars, stats, wd);

@@ -34,6 +34,13 @@
 //    lane mapping under which no two lanes of a quarter-warp touch the same
 //    bank group (transpose_v_tile).  For bf16, V is used in place as an
 //    MN-major operand and warpgroup 1 has no role;
+//  * fp32 inputs: Q lives in tensor memory, as the A operand of a TS-form
+//    Q.K^T, so that the tensor core reads only K from shared memory (Q re-read
+//    for every key tile would take a third of the shared-memory bandwidth that
+//    the tf32 tile needs).  Its TMA copy goes through the K/V ring like a K
+//    tile, and the epilogue warpgroup moves it into tensor memory (row per
+//    thread), once the previous tile's last Q.K^T is done; the slot it frees
+//    deepens the ring to three tiles of 64 KB;
 //  * split-KV instantiations (SPLIT): work unit u is the key range u mod s of
 //    tile u / s, and writes a normalised partial O and its LSE to the caller's
 //    workspace (merged by fa_combine_kernel), as in fa_tc.cuh;
@@ -68,17 +75,20 @@ struct TcWideCfg {
   static constexpr bool kVtInPlace = kTransV && D == BN;
   static constexpr uint32_t kVtPanelBytes = D * 128;
   static constexpr uint32_t kVtBytes = (kTransV && !kVtInPlace) ? D * BN * E : 0;
-  // tensor-memory columns: S_0 | S_1 | O_0 [| O_1]
-  static constexpr int kOBufs = (2 * BN + 2 * D <= 512) ? 2 : 1;
+  // fp32: Q in tensor memory, its tiles delivered through the ring
+  static constexpr bool kQTmem = kTF32;
+  // tensor-memory columns: S_0 | S_1 | O_0 [| O_1] [| Q]
+  static constexpr int kOBufs = kQTmem ? 1 : ((2 * BN + 2 * D <= 512) ? 2 : 1);
   __host__ __device__ static constexpr uint32_t col_s(uint32_t b) { return b * BN; }
   __host__ __device__ static constexpr uint32_t col_o(uint32_t b) { return 2 * BN + b * D; }
+  static constexpr uint32_t kColQ = 2 * BN + kOBufs * D;
   static constexpr uint32_t kTmemCols = 512;
-  // shared memory: Q, the K/V ring, V^T (fp32, non-square tiles), barriers, row statistics
+  // shared memory: Q (bf16), the K/V ring, V^T (fp32, non-square tiles), barriers, row statistics
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffKV = kQBytes;
+  static constexpr uint32_t kOffKV = kQTmem ? 0 : kQBytes;
   static constexpr uint32_t kOffVt = kOffKV + NSLOT * kKVBytes;
   static constexpr uint32_t kOffBar = kOffVt + kVtBytes;
-  static constexpr int kNumBars = 15 + 3 * NSLOT + 1;
+  static constexpr int kNumBars = 15 + 4 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMisc = kOffStats + BM * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
@@ -89,9 +99,9 @@ struct TcWideCfg {
   // four warpgroups' shares add up to 4 x 128.  The softmax raises its share
   // (setmaxnreg.inc), the others lower theirs (setmaxnreg.dec only lowers).
   static constexpr uint32_t kRegSoftmax = 232;
-  static constexpr uint32_t kRegWg1 = kTransV ? 80 : 56;   // V transposer (fp32) or idle
-  static constexpr uint32_t kRegEpilogue = kTransV ? 88 : 112;
-  static constexpr uint32_t kRegProducer = 112;
+  static constexpr uint32_t kRegWg1 = kTransV ? 96 : 56;   // V transposer (fp32) or idle
+  static constexpr uint32_t kRegEpilogue = kTransV ? 80 : 112;
+  static constexpr uint32_t kRegProducer = kTransV ? 104 : 112;
   static_assert(kRegSoftmax + kRegWg1 + kRegEpilogue + kRegProducer == 4 * 128, "register split");
   static_assert(kRegSoftmax >= 128 && kRegSoftmax <= 256 && kRegSoftmax % 8 == 0, "setmaxnreg.inc share");
   static_assert(kRegWg1 <= 128 && kRegEpilogue <= 128 && kRegProducer <= 128, "setmaxnreg.dec shares");
@@ -100,14 +110,16 @@ struct TcWideCfg {
   static_assert(D % kPanelElems == 0 && D <= 256, "head dim: whole swizzle rows, at most 256 (MMA N)");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
   static_assert(!kTransV || (D % 32 == 0 && BN % 32 == 0), "transpose works on 32 x 32 blocks");
-  static_assert(2 * BN + kOBufs * D <= 512, "tensor memory budget");
+  static_assert(2 * BN + kOBufs * D + (kQTmem ? D : 0) <= 512, "tensor memory budget");
+  static_assert(!kQTmem || (BM == BN && kQBytes == kKVBytes), "Q tiles travel in ring slots");
   static_assert(NSLOT <= 8, "ring slots (the load warp's per-slot bookkeeping)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct WideBars {
-  uint64_t* q_full;    // TMA -> MMA
-  uint64_t* q_empty;   // MMA -> TMA (last S of the tile done)
+  uint64_t* q_full;    // TMA -> MMA (fp32: -> the epilogue warpgroup, which moves Q to TMEM)
+  uint64_t* q_empty;   // MMA -> TMA (last S of the tile done; fp32: -> epilogue, TMEM Q free)
+  uint64_t* q_ready;   // fp32: epilogue -> MMA, Q is in tensor memory (128 arrivals)
   uint64_t* s_full;    // [2] MMA -> softmax
   uint64_t* p_full;    // [2] softmax -> MMA (128 arrivals)
   uint64_t* pv_done;   // MMA -> softmax: one completion per P.V (lazy rescale)
@@ -115,8 +127,9 @@ struct WideBars {
   uint64_t* o_empty;   // [2] epilogue -> MMA (128 arrivals), per O buffer
   uint64_t* st_full;   // softmax -> epilogue (128 arrivals)
   uint64_t* st_empty;  // epilogue -> softmax (128 arrivals)
-  uint64_t* vt_full;   // transposer -> MMA: one completion per V^T tile (fp32; 128 arrivals)
-  uint64_t* vt_empty;  // MMA -> transposer: the P.V that read the last V^T is done (fp32)
+  uint64_t* vt_full;   // [NSLOT] transposer -> MMA: V^T ready (fp32; 128 arrivals); per ring
+                       // slot when V^T is made in place, else only [0] (the V^T buffer)
+  uint64_t* vt_empty;  // MMA -> transposer: the P.V that read the V^T buffer is done (fp32, not in place)
   uint64_t* kv_full;   // [NSLOT] TMA -> MMA (fp32: V tiles only arrive here, no bytes)
   uint64_t* kv_empty;  // [NSLOT]
   uint64_t* v_full;    // [NSLOT] TMA -> transposer: the bytes of V tiles (fp32)
@@ -190,6 +203,7 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
   uint32_t withheld = ~0u;   // ring entry skipped by the test hook, if any
   uint32_t v_loads[C::NSLOT] = {};  // fp32: V tiles issued per slot
   uint32_t last_is_v = 0;    // fp32: bit s = the last entry issued into slot s was a V tile
+  uint32_t last_is_q = 0;    // fp32: bit s = ... a Q tile
   bool ok = true;
   auto load_kv = [&](const CUtensorMap* map, int j, const TileInfo& ti, bool withhold, bool is_v) -> bool {
     const uint32_t slot = it % C::NSLOT;
@@ -201,6 +215,7 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
     }
     uint64_t* done = &bars.kv_full[slot];
     if (C::kTransV) {
+      last_is_q &= ~(1u << slot);
       if (is_v) {
         done = &bars.v_full[slot];
         ++v_loads[slot];
@@ -222,12 +237,27 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
     if (!wide_counted<C>(ti)) continue;
     // test hook (host-set flag): block 0 never delivers the second K tile of its first tile
     const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
-    if (!(ok = mbar_wait(&bars.q_empty[0], (tile_k & 1u) ^ 1u, wd, 0x80))) break;
-    mbar_arrive_expect_tx(&bars.q_full[0], C::kQBytes);
+    if constexpr (C::kQTmem) {
+      // Q into the next ring slot; its bytes complete on q_full, kv_full[slot] gets a plain arrival
+      const uint32_t slot = it % C::NSLOT;
+      if (!(ok = mbar_wait(&bars.kv_empty[slot], ((it / C::NSLOT) & 1u) ^ 1u, wd, 0x80))) break;
+      ++it;
+      last_is_q |= 1u << slot;
+      last_is_v &= ~(1u << slot);
+      mbar_arrive_expect_tx(&bars.q_full[0], C::kQBytes);
 #pragma unroll
-    for (int pn = 0; pn < C::kPanels; ++pn)
-      tma_load_4d(tmQ, &bars.q_full[0], smem + C::kOffQ + pn * C::kQPanelBytes, pn * C::kPanelElems, ti.q0, ti.h,
-                  ti.b, pol_q);
+      for (int pn = 0; pn < C::kPanels; ++pn)
+        tma_load_4d(tmQ, &bars.q_full[0], smem + C::kOffKV + slot * C::kKVBytes + pn * C::kQPanelBytes,
+                    pn * C::kPanelElems, ti.q0, ti.h, ti.b, pol_q);
+      mbar_arrive(&bars.kv_full[slot]);
+    } else {
+      if (!(ok = mbar_wait(&bars.q_empty[0], (tile_k & 1u) ^ 1u, wd, 0x80))) break;
+      mbar_arrive_expect_tx(&bars.q_full[0], C::kQBytes);
+#pragma unroll
+      for (int pn = 0; pn < C::kPanels; ++pn)
+        tma_load_4d(tmQ, &bars.q_full[0], smem + C::kOffQ + pn * C::kQPanelBytes, pn * C::kPanelElems, ti.q0, ti.h,
+                    ti.b, pol_q);
+    }
     ++q_armed;
     ++tile_k;
     ok = load_kv(tmK, 0, ti, false, false) && (ti.n_kv < 2 || load_kv(tmK, 1, ti, inject, false));
@@ -243,7 +273,7 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
       const uint32_t slot = i % C::NSLOT;
       if (C::kTransV && ((last_is_v >> slot) & 1u))
         mbar_drain(&bars.v_full[slot], (v_loads[slot] - 1) & 1u, limit);
-      else
+      else if (!(C::kQTmem && ((last_is_q >> slot) & 1u)))
         mbar_drain(&bars.kv_full[slot], (i / C::NSLOT) & 1u, limit);
     }
     if (q_armed) mbar_drain(&bars.q_full[0], (q_armed - 1) & 1u, limit);
@@ -267,10 +297,12 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
 // In place, a lane swaps sub-block (a, b) with (b, a): blocks (A, B) and
 // (B, A) of 32 x 32 are done together (A < B), and the diagonal blocks take
 // rounds 0 (sub-blocks on the diagonal, transposed alone) to 4 (half the
-// lanes), so that every pair is swapped exactly once.  128 threads.
-template <int BN, int D, bool kInPlace>
+// lanes), so that every pair is swapped exactly once.  kThreads threads (a
+// multiple of 8) share the work.
+template <int BN, int D, bool kInPlace, int kThreads>
 __device__ __forceinline__ void transpose_v_tile(uint8_t* src, uint8_t* dst, int tid) {
-  const int quarter = tid >> 3;  // 16 quarter-warps
+  constexpr int kQuarters = kThreads / 8;
+  const int quarter = tid >> 3;
   const int i = tid & 7;
   // the 16-byte piece of key row k that holds dims 4b..4b+3
   auto load4 = [&](int a, int b, float4 (&v)[4]) {
@@ -292,24 +324,37 @@ __device__ __forceinline__ void transpose_v_tile(uint8_t* src, uint8_t* dst, int
       *reinterpret_cast<float4*>(dst + (a >> 3) * (D * 128) + n * 128 + (((a & 7) ^ (n & 7)) << 4)) = w;
     }
   };
+  // two work items in flight per lane (item and item + kQuarters): all their
+  // loads are issued before any store, so the shared-memory latency of one
+  // item hides behind the other's
   if constexpr (!kInPlace) {
     constexpr int kItems = (BN / 32) * (D / 32) * 8;
-#pragma unroll 1
-    for (int item = quarter; item < kItems; item += 16) {
+    auto decode = [&](int item, int& a, int& b) -> bool {
+      if (item >= kItems) return false;
       const int sb = item >> 3, t = item & 7;
-      const int A = sb / (D / 32), B = sb % (D / 32);
-      const int a = 8 * A + ((i + t) & 7), b = 8 * B + i;
-      float4 v[4];
-      load4(a, b, v);
-      store4(a, b, v);
+      a = 8 * (sb / (D / 32)) + ((i + t) & 7);
+      b = 8 * (sb % (D / 32)) + i;
+      return true;
+    };
+#pragma unroll 1
+    for (int item = quarter; item < kItems; item += 2 * kQuarters) {
+      int a0 = 0, b0 = 0, a1 = 0, b1 = 0;
+      const bool k0 = decode(item, a0, b0), k1 = decode(item + kQuarters, a1, b1);
+      float4 v0[4], v1[4];
+      if (k0) load4(a0, b0, v0);
+      if (k1) load4(a1, b1, v1);
+      if (k0) store4(a0, b0, v0);
+      if (k1) store4(a1, b1, v1);
     }
   } else {
     static_assert(BN == D, "in-place transpose needs a square tile");
     constexpr int P = BN / 32;
     constexpr int kOff = P * (P - 1) / 2 * 8;  // rounds of the off-diagonal block pairs
     constexpr int kItems = kOff + P * 5;
-#pragma unroll 1
-    for (int item = quarter; item < kItems; item += 16) {
+    // 0: no work for this lane, 1: a sub-block on the diagonal (transposed
+    // alone), 2: a pair (a, b) <-> (b, a)
+    auto decode = [&](int item, int& a, int& b) -> int {
+      if (item >= kItems) return 0;
       int A, B, t;
       if (item < kOff) {
         int pr = item >> 3;
@@ -323,62 +368,89 @@ __device__ __forceinline__ void transpose_v_tile(uint8_t* src, uint8_t* dst, int
       } else {
         A = B = (item - kOff) / 5;
         t = (item - kOff) % 5;
-        if (t == 4 && i >= 4) continue;
+        if (t == 4 && i >= 4) return 0;
       }
-      const int a = 8 * A + ((i + t) & 7), b = 8 * B + i;
-      float4 v[4];
-      load4(a, b, v);
-      if (A == B && t == 0) {  // a sub-block on the diagonal: transposed alone
-        store4(a, b, v);
-      } else {
-        float4 w[4];
-        load4(b, a, w);
-        store4(a, b, v);  // (a, b)^T lands where (b, a) was
-        store4(b, a, w);
-      }
+      a = 8 * A + ((i + t) & 7);
+      b = 8 * B + i;
+      return (A == B && t == 0) ? 1 : 2;
+    };
+#pragma unroll 1
+    for (int item = quarter; item < kItems; item += 2 * kQuarters) {
+      int a0 = 0, b0 = 0, a1 = 0, b1 = 0;
+      const int k0 = decode(item, a0, b0), k1 = decode(item + kQuarters, a1, b1);
+      float4 v0[4], w0[4], v1[4], w1[4];
+      if (k0) load4(a0, b0, v0);
+      if (k0 == 2) load4(b0, a0, w0);
+      if (k1) load4(a1, b1, v1);
+      if (k1 == 2) load4(b1, a1, w1);
+      if (k0) store4(a0, b0, v0);  // (a, b)^T lands where (b, a) was
+      if (k0 == 2) store4(b0, a0, w0);
+      if (k1) store4(a1, b1, v1);
+      if (k1 == 2) store4(b1, a1, w1);
     }
   }
 }
 
-// Warpgroup 1 for fp32 inputs: transposes each V tile in the order the load
-// warp delivers them, once the P.V that read the previous V^T is done.  Every
-// thread publishes its own writes (proxy fence, then an arrival on vt_full,
-// which counts 128), so no warp ever waits for another one: a warp that gives
-// up on a wait cannot leave the others stuck.
+// The V^T makers (fp32 inputs): warpgroup 1.  (Six warps -- adding the two
+// idle warps of the producer warpgroup -- transpose a tile faster on their
+// own, but slow the softmax warps that share their schedulers by more.)
+constexpr int kTransThreads = 128;
+
+// The V^T makers: transpose each V tile in the order the load
+// warp delivers them -- in its ring slot as soon as it lands (vt_full of that
+// slot), or into the V^T buffer once the P.V that read the previous V^T is
+// done.  Every thread publishes its own writes (proxy fence, then an arrival
+// on vt_full, which counts kTransThreads), so no warp ever waits for another one: a
+// warp that gives up on a wait cannot leave the others stuck.
 template <class C>
-__device__ void wide_transpose_role(const TcParams& p, uint8_t* smem, const WideBars& bars, const Watchdog& wd) {
-  const int tid = threadIdx.x & 127;
+__device__ void wide_transpose_role(const TcParams& p, uint8_t* smem, const WideBars& bars, const Watchdog& wd,
+                                    int tid) {
   uint32_t it = 0, vcount = 0;
   uint32_t v_seen[C::NSLOT] = {};  // V tiles taken per slot (phases of v_full[slot])
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
     if (!wide_counted<C>(ti)) continue;
-    it += ti.n_kv < 2 ? 1 : 2;  // K_0 [, K_1]
+    it += (C::kQTmem ? 1 : 0) + (ti.n_kv < 2 ? 1 : 2);  // [Q,] K_0 [, K_1]
     for (int j = 0; j < ti.n_kv; ++j, ++vcount) {
       const uint32_t iv = it++;
       if (j + 2 < ti.n_kv) ++it;  // K_{j+2} follows V_j
       const uint32_t slot = iv % C::NSLOT;
       if (!warp_wait(&bars.v_full[slot], v_seen[slot] & 1u, wd, 0x8b)) return;
       ++v_seen[slot];
-      if (!warp_wait(&bars.vt_empty[0], (vcount & 1u) ^ 1u, wd, 0x8c)) return;
+      if (!C::kVtInPlace && !warp_wait(&bars.vt_empty[0], (vcount & 1u) ^ 1u, wd, 0x8c)) return;
       uint8_t* src = smem + C::kOffKV + slot * C::kKVBytes;
       uint8_t* dst = C::kVtInPlace ? src : smem + C::kOffVt;
-      transpose_v_tile<C::BN, C::D, C::kVtInPlace>(src, dst, tid);
+      transpose_v_tile<C::BN, C::D, C::kVtInPlace, kTransThreads>(src, dst, tid);
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-      mbar_arrive(&bars.vt_full[0]);
+      mbar_arrive(&bars.vt_full[C::kVtInPlace ? slot : 0]);
     }
   }
 }
 
 // -------------------------------------------------------------- MMA warp
+// S = Q K^T with Q in tensor memory (TS form, fp32 inputs): A = Q, K columns
+// of 32-bit tf32 from tmem_q (one MMA takes 8 of them); B = the K tile,
+// K-major in shared memory as in issue_qk.
+template <class C>
+__device__ __forceinline__ void issue_qk_ts(uint32_t tmem_s, uint32_t tmem_q, uint32_t k_addr) {
+  const uint64_t b0 = sdesc_sw128<16, 1024>(k_addr);
+#pragma unroll
+  for (int kk = 0; kk < C::D / C::kKStep; ++kk) {
+    const uint32_t byte = kk * 32;
+    const uint32_t b_off = ((byte / 128) * C::kKVPanelBytes + byte % 128) >> 4;
+    mma_ts<C::kTF32>(tmem_s, tmem_q + kk * 8, b0 + b_off, C::kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
 template <class C>
 __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const WideBars& bars,
                               const Watchdog& wd) {
-  const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+  const uint32_t q_addr = smem_u32(smem + C::kOffQ);  // (bf16: Q in shared memory)
   const uint32_t kv_base = smem_u32(smem + C::kOffKV);
   const uint32_t vt_base = smem_u32(smem + C::kOffVt);
   uint32_t it = 0, tile_k = 0, g = 0;  // g: S tiles issued so far (all tiles of this CTA)
   uint32_t vcount = 0;                 // V tiles consumed so far
+  uint32_t vt_seen[C::NSLOT] = {};     // fp32, V^T in place: V^T tiles taken per slot
   bool ok = true;
   auto kv_wait = [&](uint32_t i) -> bool {
     return warp_wait(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x82);
@@ -391,7 +463,10 @@ __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, c
     if (!kv_wait(ik)) return false;
     tc_fence_after();
     if (elect_one()) {
-      issue_qk<C>(tmem + C::col_s(g & 1u), opaque(q_addr), slot_addr(ik));
+      if constexpr (C::kQTmem)
+        issue_qk_ts<C>(tmem + C::col_s(g & 1u), tmem + C::kColQ, slot_addr(ik));
+      else
+        issue_qk<C>(tmem + C::col_s(g & 1u), opaque(q_addr), slot_addr(ik));
       tc_commit(&bars.s_full[g & 1u]);
       tc_commit(&bars.kv_empty[ik % C::NSLOT]);
       if (last_of_tile) tc_commit(&bars.q_empty[0]);
@@ -407,7 +482,15 @@ __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, c
     const uint32_t g0 = g;  // S index of key tile 0 of this tile
     const uint32_t ob = tile_k % C::kOBufs;          // O buffer of this tile
     const uint32_t o_par = (tile_k / C::kOBufs) & 1u;
-    if (!(ok = warp_wait(&bars.q_full[0], tile_k & 1u, wd, 0x83))) break;
+    if constexpr (C::kQTmem) {
+      // Q is in tensor memory: its ring slot (read by the epilogue's copy) is free
+      const uint32_t iq = it++;
+      if (!(ok = warp_wait(&bars.q_ready[0], tile_k & 1u, wd, 0x83))) break;
+      if (elect_one()) mbar_arrive(&bars.kv_empty[iq % C::NSLOT]);
+      __syncwarp();
+    } else {
+      if (!(ok = warp_wait(&bars.q_full[0], tile_k & 1u, wd, 0x83))) break;
+    }
     ++tile_k;
     if (!(ok = qk(n == 1))) break;
     if (n > 1 && !(ok = qk(n == 2))) break;
@@ -416,7 +499,9 @@ __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, c
       const uint32_t iv = it++;
       if (!(ok = warp_wait(&bars.p_full[gj & 1u], (gj >> 1) & 1u, wd, 0x84))) break;
       if (j == 0 && !(ok = warp_wait(&bars.o_empty[ob], o_par ^ 1u, wd, 0x85))) break;
-      if constexpr (C::kTransV)
+      if constexpr (C::kTransV && C::kVtInPlace)
+        ok = warp_wait(&bars.vt_full[iv % C::NSLOT], vt_seen[iv % C::NSLOT]++ & 1u, wd, 0x86);
+      else if constexpr (C::kTransV)
         ok = warp_wait(&bars.vt_full[0], vcount & 1u, wd, 0x86);
       else
         ok = kv_wait(iv);
@@ -428,7 +513,7 @@ __device__ void wide_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, c
         // free now (the transposer's reads are done); else after the P.V
         if (C::kTransV && !C::kVtInPlace) mbar_arrive(&bars.kv_empty[iv % C::NSLOT]);
         issue_pv<C>(tmem + C::col_o(ob), tmem + C::col_s(gj & 1u), v_addr, j > 0);
-        if (C::kTransV) tc_commit(&bars.vt_empty[0]);
+        if (C::kTransV && !C::kVtInPlace) tc_commit(&bars.vt_empty[0]);
         if (!C::kTransV || C::kVtInPlace) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
         tc_commit(&bars.pv_done[0]);
         if (j == n - 1) tc_commit(&bars.o_full[ob]);
@@ -547,9 +632,13 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
             if (c >= lim) v0 = 0.f;
             if (c + 1 >= lim) v1 = 0.f;
           }
-          if constexpr (C::kTF32) {  // l sums exactly the P that P.V uses
-            v0 = to_tf32(v0);
-            v1 = to_tf32(v1);
+          if constexpr (C::kTF32) {
+            // P to tf32 by dropping the 13 low mantissa bits (one integer op,
+            // instead of a conversion on the special-function pipe, which ex2
+            // already keeps busy): l then sums exactly the P that P.V uses, so
+            // the common shrink of the weights cancels in O / l
+            v0 = __uint_as_float(__float_as_uint(v0) & 0xFFFFE000u);
+            v1 = __uint_as_float(__float_as_uint(v1) & 0xFFFFE000u);
           }
           e[k] = v0;
           e[k + 1] = v1;
@@ -588,21 +677,18 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
 
 // ------------------------------------------------------- epilogue warpgroup
 template <class C>
-__device__ void wide_epilogue_role(const TcParams& p, uint32_t tmem, const WideBars& bars, const float2* stats,
-                                   const Watchdog& wd) {
+__device__ void wide_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const WideBars& bars,
+                                   const float2* stats, const Watchdog& wd) {
   using T = typename C::Elem;
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  uint32_t tile_k = 0;
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-    const TileInfo ti = wide_tile_info<C>(p, u);
-    if (!wide_counted<C>(ti)) continue;
-    const uint32_t ob = tile_k % C::kOBufs;
-    if (!warp_wait(&bars.o_full[ob], (tile_k / C::kOBufs) & 1u, wd, 0x8a)) return;
-    if (!warp_wait(&bars.st_full[0], tile_k & 1u, wd, 0x8d)) return;
-    ++tile_k;
+  // O / l of tile number k (this CTA's k-th unit with keys), and its LSE
+  auto store_tile = [&](const TileInfo& ti, uint32_t k) -> bool {
+    const uint32_t ob = k % C::kOBufs;
+    if (!warp_wait(&bars.o_full[ob], (k / C::kOBufs) & 1u, wd, 0x8a)) return false;
+    if (!warp_wait(&bars.st_full[0], k & 1u, wd, 0x8d)) return false;
     tc_fence_after();
     const float2 st = stats[row];
     mbar_arrive(&bars.st_empty[0]);
@@ -649,7 +735,51 @@ __device__ void wide_epilogue_role(const TcParams& p, uint32_t tmem, const WideB
       p.ws_lse[wrow] = st.y;
     else if (valid && p.LSE)
       p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
+    return true;
+  };
+  uint32_t tile_k = 0, it = 0;
+  TileInfo prev{};
+  bool have_prev = false;
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    const TileInfo ti = wide_tile_info<C>(p, u);
+    if (!wide_counted<C>(ti)) continue;
+    if constexpr (C::kQTmem) {
+      // this tile's Q: ring slot -> tensor memory, once its bytes have landed
+      // and the previous tile's last Q.K^T no longer reads tensor-memory Q;
+      // then the previous tile's output (which completes later)
+      const uint32_t slot = it % C::NSLOT;
+      it += 1 + 2 * ti.n_kv;  // Q, then n K and n V tiles
+      if (!warp_wait(&bars.q_full[0], tile_k & 1u, wd, 0x8e)) return;
+      if (!warp_wait(&bars.q_empty[0], (tile_k & 1u) ^ 1u, wd, 0x8f)) return;
+      tc_fence_after();
+      const uint8_t* qs = smem + C::kOffKV + slot * C::kKVBytes;
+      const uint32_t tQ = tmem + lane_base + C::kColQ;
+#pragma unroll 1
+      for (int pn = 0; pn < C::kPanels; ++pn) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qs + pn * C::kQPanelBytes + row * 128 + ((c ^ (row & 7)) << 4));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        tmem_st32(tQ + pn * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.q_ready[0]);
+      if (have_prev && !store_tile(prev, tile_k - 1)) return;
+      prev = ti;
+      have_prev = true;
+      ++tile_k;
+    } else {
+      if (!store_tile(ti, tile_k)) return;
+      ++tile_k;
+    }
   }
+  if (C::kQTmem && have_prev) store_tile(prev, tile_k - 1);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -670,12 +800,13 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   bars.o_empty = bar + 9;
   bars.st_full = bar + 11;
   bars.st_empty = bar + 12;
-  bars.vt_full = bar + 13;
-  bars.vt_empty = bar + 14;
+  bars.vt_empty = bar + 13;
+  bars.q_ready = bar + 14;
   bars.kv_full = bar + 15;
   bars.kv_empty = bar + 15 + C::NSLOT;
   bars.v_full = bar + 15 + 2 * C::NSLOT;
-  bars.teardown = bar + 15 + 3 * C::NSLOT;
+  bars.vt_full = bar + 15 + 3 * C::NSLOT;
+  bars.teardown = bar + 15 + 4 * C::NSLOT;
   float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -694,12 +825,13 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     mbar_init(&bars.pv_done[0], 1);
     mbar_init(&bars.st_full[0], 128);
     mbar_init(&bars.st_empty[0], 128);
-    mbar_init(&bars.vt_full[0], 128);
     mbar_init(&bars.vt_empty[0], 1);
+    mbar_init(&bars.q_ready[0], 128);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
       mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.vt_full[s], kTransThreads);
     }
     mbar_init(&bars.teardown[0], 1);
     *abort_flag = 0;
@@ -727,10 +859,10 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     if (warp == 13) wide_mma_role<C>(p, smem, tmem, bars, wd);
   } else if (wg == 2) {
     setmaxnreg_dec<C::kRegEpilogue>();
-    wide_epilogue_role<C>(p, tmem, bars, stats, wd);
+    wide_epilogue_role<C>(p, smem, tmem, bars, stats, wd);
   } else if (wg == 1) {
     setmaxnreg_dec<C::kRegWg1>();
-    if constexpr (C::kTransV) wide_transpose_role<C>(p, smem, bars, wd);
+    if constexpr (C::kTransV) wide_transpose_role<C>(p, smem, bars, wd, threadIdx.x - 128);
   } else {
     setmaxnreg_inc<C::kRegSoftmax>();
     wide_softmax_role<C>(p, tmem, bars, stats, wd);

@@ -688,6 +688,7 @@ fa_status_t fa_bwd_dv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int6
   }
   p.err = ds->err;
   p.timeout_ns = g_timeout_ns.load();
+  p.debug_flags = g_debug_flags.load();
   p.d_qk = (int)d;
   p.d_v = (int)d_v;
   BwdPreParams& pre = L.pre;

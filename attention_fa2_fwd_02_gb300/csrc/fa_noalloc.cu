@@ -30,7 +30,8 @@ std::mutex g_scratch_mu;
 std::atomic<void*> g_scratch_ptr[kMaxDevices];  // device address per ordinal, once looked up
 
 // Device address of the scratch on the current device.  The first call per
-// device looks it up with that device current and caches it.
+// device looks it up with that device current and caches it (for the life of
+// the process: cudaDeviceReset while the library is loaded is not supported).
 fa_status_t scratch_on_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -57,6 +57,9 @@ def _(q, k, v, o, lse, do, scale, is_causal):
 def _setup_context(ctx, inputs, output):
     q, k, v, scale, is_causal = inputs
     o, lse = output
+    # the backward below gives the gradients of O only: a gradient reaching
+    # LSE would be dropped, so autograd is told that LSE has none
+    ctx.mark_non_differentiable(lse)
     ctx.save_for_backward(q, k, v, o, lse)
     ctx.scale, ctx.is_causal = scale, is_causal
 

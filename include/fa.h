@@ -212,6 +212,15 @@ fa_status_t fa_fwd_splitkv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t N_q, 
  *               wrong results.  Calls issued in order on one stream are safe.
  *   Contents    every scratch element the merge step reads is first written
  *               by the same call, so nothing needs clearing between calls.
+ *   Residency   the buffer is part of the library's device image.  Under
+ *               lazy module loading (the CUDA default) a device holds it
+ *               from the first call on that device until the process exits;
+ *               under eager loading (CUDA_MODULE_LOADING=EAGER) every device
+ *               on which the process creates a context holds it from then
+ *               on, whether or not this entry point is ever called.
+ *   Device reset  the buffer's address is looked up once per device and kept
+ *               (as is the library's error word): calling cudaDeviceReset
+ *               while this library is loaded is not supported.
  */
 #define FA_SPLITKV_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
 

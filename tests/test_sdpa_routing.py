@@ -95,3 +95,17 @@ def test_sdpa_inside_torch_compile():
     fa.check()
     for a, b in ((q1.grad, q2.grad), (k1.grad, k2.grad), (v1.grad, v2.grad)):
         assert torch.equal(a, b)
+
+
+@gpu
+def test_custom_op_lse_has_no_gradient():
+    """The forward custom op returns LSE too, but its backward gives the
+    gradients of O only: LSE is marked non-differentiable, so a loss built on
+    it cannot silently lose a gradient term."""
+    _need_gpu()
+    q, k, v = (x.cuda().requires_grad_(True) for x in qkv((1, 2, 128, 64), (1, 2, 128, 64), 1331, torch.bfloat16))
+    o, lse = torch.ops.fa_gb300.fwd(q, k, v, 0.125, False)
+    fa.check()
+    assert o.requires_grad and not lse.requires_grad
+    with pytest.raises(RuntimeError):
+        lse.sum().backward()

@@ -352,13 +352,13 @@ cudaError_t launch_small_typed(const SmallParams& P, DevState& ds, cudaStream_t 
     bool& ready = ds.small_attr[sizeof(T) == 4 ? 1 : 0][D == 16 ? 0 : 1];
     if (!ready) {
       cudaError_t e =
-          cudaFuncSetAttribute(fa_small_fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+          cudaFuncSetAttribute(fa_small_fwd_kernel<T, D, kSmallSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       ready = true;
     }
   }
-  const long long blocks = (P.n_items + 3) / 4;
-  fa_small_fwd_kernel<T, D><<<(unsigned)blocks, 128, smem, stream>>>(P);
+  // one CTA per work item (32 query rows of one (problem, b, h))
+  fa_small_fwd_kernel<T, D, kSmallSplit><<<(unsigned)P.n_items, 32 * kSmallSplit, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
@@ -399,7 +399,7 @@ fa_status_t launch_small(fa_dtype_t dtype, int d, const std::vector<const fa_pro
     items += pb.B * pb.H * s.n_qblk;
   }
   P.n_items = items;
-  if ((items + 3) / 4 >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query blocks in one launch");
+  if (items >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many query blocks in one launch");
   cudaError_t e;
   if (dtype == FA_FP32)
     e = d == 16 ? launch_small_typed<float, 16>(P, ds, stream) : launch_small_typed<float, 32>(P, ds, stream);

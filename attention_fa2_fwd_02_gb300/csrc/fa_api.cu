@@ -20,6 +20,7 @@
 #include "fa_launch.h"
 #include "fa_axial_block.cuh"
 #include "fa_small.cuh"
+#include "fa_small_mma.cuh"
 
 namespace fa {
 // Raised (atomicOr) by any kernel of this library whose bounded wait expires.
@@ -347,21 +348,31 @@ bool row_aligned16(const fa_tensor_t& t, long long E) {
   return true;
 }
 
+// fp32: warp-level tf32 tiles with a three-term split (fa_small_mma.cuh), one
+// warp per work item, 4 per CTA; bf16: the CUDA-core kernel (fa_small.cuh),
+// one CTA per work item.
 template <typename T, int D>
 cudaError_t launch_small_typed(const SmallParams& P, DevState& ds, cudaStream_t stream) {
-  constexpr int smem = small_smem_bytes<T, D>();
+  constexpr bool kMma = sizeof(T) == 4;
+  constexpr int smem = kMma ? small_mma_smem_bytes<D>() : small_smem_bytes<T, D>();
   {  // once per device, so that captured launches make no attribute call
     std::lock_guard<std::mutex> lk(g_mu);
     bool& ready = ds.small_attr[sizeof(T) == 4 ? 1 : 0][D == 16 ? 0 : 1];
     if (!ready) {
-      cudaError_t e =
-          cudaFuncSetAttribute(fa_small_fwd_kernel<T, D, kSmallSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaError_t e;
+      if constexpr (kMma)
+        e = cudaFuncSetAttribute(fa_small_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      else
+        e = cudaFuncSetAttribute(fa_small_fwd_kernel<T, D, kSmallSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem);
       if (e != cudaSuccess) return e;
       ready = true;
     }
   }
-  // one CTA per work item (32 query rows of one (problem, b, h))
-  fa_small_fwd_kernel<T, D, kSmallSplit><<<(unsigned)P.n_items, 32 * kSmallSplit, smem, stream>>>(P);
+  if constexpr (kMma)
+    fa_small_mma_kernel<D><<<(unsigned)((P.n_items + 3) / 4), 128, smem, stream>>>(P);
+  else
+    fa_small_fwd_kernel<T, D, kSmallSplit><<<(unsigned)P.n_items, 32 * kSmallSplit, smem, stream>>>(P);
   return cudaGetLastError();
 }
 

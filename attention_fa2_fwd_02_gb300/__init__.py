@@ -121,6 +121,12 @@ def lib() -> ctypes.CDLL:
             L.fa_axial_block_fwd.restype = ctypes.c_int
             L.fa_axial_block_fwd.argtypes = [ctypes.c_int64] * 5 + [ctypes.c_void_p, P(AxialWeights),
                                                                    P(AxialWeights), ctypes.c_void_p, ctypes.c_void_p]
+            L.fa_fwd_ws_bytes.restype = ctypes.c_size_t
+            L.fa_fwd_ws_bytes.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 6
+            L.fa_fwd_ws.restype = ctypes.c_int
+            L.fa_fwd_ws.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 6 + [P(FaTensor)] * 3 + \
+                [ctypes.c_float, ctypes.c_int, P(FaTensor), ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p,
+                 ctypes.c_size_t, ctypes.c_void_p]
             L.fa_fwd_gqa.restype = ctypes.c_int
             L.fa_fwd_gqa.argtypes = [ctypes.c_int] + [ctypes.c_int64] * 6 + [P(FaTensor)] * 3 + \
                 [ctypes.c_float, ctypes.c_int, P(FaTensor), ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p]
@@ -247,9 +253,11 @@ def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None =
     Asynchronous on the current (or given) stream.  Returns (O, LSE); LSE is
     None when ``with_lse`` is False and no ``lse`` buffer is passed.
     ``split_kv``: key-range splits (None = the library's choice for this
-    device; 1 = never split).  A split run needs scratch memory: ``workspace``
-    (a CUDA uint8 tensor of at least the required bytes) or, if None, one
-    allocated here from PyTorch's allocator.
+    device; 1 = never split).  A split run needs scratch memory, and so does
+    an fp32 run whose V tiles are each read by several query tiles (V^T is
+    written there once, fa_fwd_ws): ``workspace`` (a CUDA uint8 tensor of at
+    least the required bytes) or, if None, one allocated here from PyTorch's
+    allocator.
     """
     pb, out, lse = _problem(Q, K, V, scale, is_causal, out, lse, with_lse)
     L = lib()
@@ -260,25 +268,35 @@ def fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None =
         if pb.d in (64, 128) and pb.H_kv == pb.H and pb.Dv == pb.d:  # (split-KV: K/V with the query heads, Dv = d)
             n_split = (L.fa_fwd_splitkv_choose(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d, pb.is_causal)
                        if split_kv is None else int(split_kv))
-        if pb.Dv != pb.d:  # V with a head dim of its own: the one-problem grouped entry
-            st = L.fa_fwd_grouped(code, 1, ctypes.byref(pb), _stream_ptr(Q.device, stream))
-        elif n_split == 1:
-            st = L.fa_fwd_gqa(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
-                          ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
-                          pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
-                          _stream_ptr(Q.device, stream))
-        else:
-            need = L.fa_fwd_splitkv_workspace_bytes(pb.B, pb.H, pb.N_q, pb.d, n_split)
+        def scratch(need):
+            nonlocal workspace
             if workspace is None:
                 workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
             if workspace.device != Q.device or workspace.numel() * workspace.element_size() < need:
                 raise ValueError(f"workspace must be a CUDA buffer of >= {need} bytes on Q's device")
+            return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+        if pb.Dv != pb.d:  # V with a head dim of its own: the one-problem grouped entry
+            st = L.fa_fwd_grouped(code, 1, ctypes.byref(pb), _stream_ptr(Q.device, stream))
+        elif n_split == 1:
+            need = L.fa_fwd_ws_bytes(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d)
+            if need > 0:  # fp32: V^T written once into the workspace
+                ws, ws_bytes = scratch(need)
+                st = L.fa_fwd_ws(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
+                                 ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                                 pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
+                                 ws, ws_bytes, _stream_ptr(Q.device, stream))
+            else:
+                st = L.fa_fwd_gqa(code, pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d,
+                                  ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
+                                  pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
+                                  _stream_ptr(Q.device, stream))
+        else:
+            ws, ws_bytes = scratch(L.fa_fwd_splitkv_workspace_bytes(pb.B, pb.H, pb.N_q, pb.d, n_split))
             st = L.fa_fwd_splitkv(code, pb.B, pb.H, pb.N_q, pb.N_k, pb.d,
                                   ctypes.byref(pb.Q), ctypes.byref(pb.K), ctypes.byref(pb.V),
                                   pb.scale, pb.is_causal, ctypes.byref(pb.O), pb.LSE, lse_stride,
-                                  n_split, ctypes.c_void_p(workspace.data_ptr()),
-                                  workspace.numel() * workspace.element_size(),
-                                  _stream_ptr(Q.device, stream))
+                                  n_split, ws, ws_bytes, _stream_ptr(Q.device, stream))
     _raise_on(st)
     return out, lse
 

@@ -19,7 +19,8 @@ OUT_DIR = PKG / "_build"
 LIB = OUT_DIR / "libfa.so"
 SOURCES = ["fa_api.cu", "fa_tc_bf16.cu", "fa_tc_bf16_split.cu",
            "fa_noalloc.cu", "fa_bwd.cu",
-           "fa_tc_bf16_varlen.cu", "fa_tc_wide.cu", "fa_tc_wide_fp32.cu"]
+           "fa_tc_bf16_varlen.cu", "fa_tc_wide.cu", "fa_tc_wide_fp32.cu",
+           "fa_tc_wide_fp32_vt.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

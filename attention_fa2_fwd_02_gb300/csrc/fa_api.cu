@@ -21,6 +21,7 @@
 #include "fa_axial_block.cuh"
 #include "fa_small.cuh"
 #include "fa_small_mma.cuh"
+#include "fa_vt.cuh"
 
 namespace fa {
 // Raised (atomicOr) by any kernel of this library whose bounded wait expires.
@@ -207,8 +208,42 @@ SplitWs split_ws_layout(void* ws, long long B, long long H, long long N_q, long 
   return w;
 }
 
+// V^T workspace of the fp32 tensor-core path (fa_vt.cuh): [B * H_kv][Dv][ldk]
+// fp32, ldk = N_k rounded up to 32.
+long long vt_ldk(long long N_k) { return (N_k + 31) / 32 * 32; }
+size_t vt_ws_bytes(const fa_problem_t& pb) {
+  return static_cast<size_t>(pb.B) * kv_heads(pb) * v_dim(pb) * vt_ldk(pb.N_k) * 4;
+}
+// A problem takes the V^T pass when it runs on the tf32 tensor cores and each
+// V tile is read by at least two query tiles (query blocks x the query heads
+// of a K/V head): the pass then saves at least one in-kernel transpose per
+// V tile.
+bool wants_vt(fa_dtype_t dtype, const fa_problem_t& pb, Path path) {
+  if (dtype != FA_FP32 || path != Path::kTensorCore) return false;
+  const long long uses = (pb.N_q + kWideQueryTile - 1) / kWideQueryTile * (pb.H / kv_heads(pb));
+  return uses >= 2;
+}
+
+fa_status_t make_vt_map(CUtensorMap* map, const float* vt, const fa_problem_t& pb, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const long long ldk = vt_ldk(pb.N_k), dv = v_dim(pb);
+  cuuint64_t dims[4] = {(cuuint64_t)pb.N_k, (cuuint64_t)dv, (cuuint64_t)kv_heads(pb), (cuuint64_t)pb.B};
+  cuuint64_t strides[3] = {(cuuint64_t)(ldk * 4), (cuuint64_t)(dv * ldk * 4), (cuuint64_t)(kv_heads(pb) * dv * ldk * 4)};
+  cuuint32_t box[4] = {32, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_TFLOAT32, 4, const_cast<float*>(vt), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the V^T workspace (CUresult " +
+                                        std::to_string((int)r) + ")");
+  return FA_OK;
+}
+
+// vt: the V^T workspace (fp32, unsplit) or null (V tiles transposed in the kernel).
 fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const DevState& ds, cudaStream_t stream,
-                               int n_split = 1, SplitWs ws = SplitWs{}) {
+                               int n_split = 1, SplitWs ws = SplitWs{}, float* vt = nullptr) {
   const bool fp32 = dtype == FA_FP32;
   const int dv = static_cast<int>(v_dim(pb));
   const int d = tc_tile_dim(pb.d, dv);  // the kernel's tile width
@@ -223,7 +258,12 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   fa_status_t st;
   if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, pb.d, 128, "Q")) != FA_OK) return st;
   if ((st = make_map(&L.tmK, pb.K, fp32, pb.B, kv_heads(pb), pb.N_k, pb.d, bn, "K")) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, kv_heads(pb), pb.N_k, dv, bn, "V")) != FA_OK) return st;
+  if (vt) {
+    if (!fp32 || n_split > 1) return fail(FA_ERR_UNSUPPORTED, "the V^T pass serves the unsplit fp32 path");
+    if ((st = make_vt_map(&L.tmV, vt, pb, d)) != FA_OK) return st;
+  } else if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, kv_heads(pb), pb.N_k, dv, bn, "V")) != FA_OK) {
+    return st;
+  }
   TcParams& p = L.p;
   p.B = (int)pb.B;
   p.H = (int)pb.H;
@@ -263,7 +303,23 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   L.device = ds.device;
   L.stream = stream;
   cudaError_t e;
-  if (fp32 && n_split > 1) {
+  if (vt) {
+    VtParams v{};
+    v.V = static_cast<const float*>(pb.V.ptr);
+    v.s0 = pb.V.stride[0];
+    v.s1 = pb.V.stride[1];
+    v.s2 = pb.V.stride[2];
+    v.Vt = vt;
+    v.H_kv = (int)kv_heads(pb);
+    v.N_k = (int)pb.N_k;
+    v.dv = dv;
+    v.ldk = (int)vt_ldk(pb.N_k);
+    v.n_kblk = (int)((pb.N_k + kVtKeys - 1) / kVtKeys);
+    fa_vt_kernel<<<(unsigned)(pb.B * kv_heads(pb) * v.n_kblk), 256, 0, stream>>>(v);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("V^T kernel launch", e));
+    L.after_vt = true;
+    e = d == 128 ? launch_tc_wide_fp32_d128_vt(L) : launch_tc_wide_fp32_d64_vt(L);
+  } else if (fp32 && n_split > 1) {
     e = d == 128 ? launch_tc_wide_fp32_d128_split(L) : launch_tc_wide_fp32_d64_split(L);
   } else if (fp32) {
     e = d == 128 ? launch_tc_wide_fp32_d128(L) : launch_tc_wide_fp32_d64(L);
@@ -531,6 +587,61 @@ fa_status_t fa_fwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
 
 fa_status_t fa_fwd_grouped(fa_dtype_t dtype, int n, const fa_problem_t* problems, void* stream) {
   return run_problems(dtype, n, problems, stream);
+}
+
+size_t fa_fwd_ws_bytes(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d) {
+  if (dtype != FA_FP32 || B <= 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || N_q <= 0 || N_k <= 0 || d <= 0 ||
+      d > kVtMaxDim || d == 16 || d == 32 || d % 4 != 0 || N_k >= (1ll << 31) || N_q >= (1ll << 31))
+    return 0;
+  fa_problem_t pb{};
+  pb.B = B;
+  pb.H = H;
+  pb.H_kv = H_kv;
+  pb.N_q = N_q;
+  pb.N_k = N_k;
+  pb.d = d;
+  if (!wants_vt(dtype, pb, Path::kTensorCore)) return 0;
+  return vt_ws_bytes(pb);
+}
+
+fa_status_t fa_fwd_ws(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                      const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale, int is_causal,
+                      const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARG, "Q, K, V and O must not be NULL");
+  if (LSE && !lse_stride) return fail(FA_ERR_INVALID_ARG, "lse_stride must not be NULL when LSE is given");
+  if (H_kv <= 0) return fail(FA_ERR_INVALID_ARG, "problem 0: H_kv must divide H");
+  fa_problem_t pb{};
+  pb.B = B;
+  pb.H = H;
+  pb.H_kv = H_kv;
+  pb.N_q = N_q;
+  pb.N_k = N_k;
+  pb.d = d;
+  pb.Q = *Q;
+  pb.K = *K;
+  pb.V = *V;
+  pb.O = *O;
+  pb.LSE = LSE;
+  for (int i = 0; i < 3; ++i) pb.lse_stride[i] = LSE ? lse_stride[i] : 0;
+  pb.scale = scale;
+  pb.is_causal = is_causal;
+  Path path;
+  fa_status_t st = validate(dtype, pb, 0, &path);
+  if (st != FA_OK) return st;
+  if (!wants_vt(dtype, pb, path)) return run_problems(dtype, 1, &pb, stream);  // no workspace needed
+  if (B * H_kv * ((N_k + kVtKeys - 1) / kVtKeys) >= (1ll << 31)) return fail(FA_ERR_UNSUPPORTED, "too many V^T blocks");
+  if (!workspace) return fail(FA_ERR_INVALID_ARG, "this problem needs a workspace (fa_fwd_ws_bytes > 0)");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(FA_ERR_INVALID_ARG, "the workspace must be 256-byte aligned");
+  const size_t need = vt_ws_bytes(pb);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace too small: " + std::to_string(workspace_bytes) + " < " +
+                                        std::to_string(need) + " bytes");
+  DevState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  return launch_tensor_core(dtype, pb, *ds, static_cast<cudaStream_t>(stream), 1, SplitWs{},
+                            static_cast<float*>(workspace));
 }
 
 size_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d, int n_split) {
@@ -921,6 +1032,6 @@ void fa_debug_set(uint64_t timeout_ns, int debug_flags) {
   g_debug_flags.store(debug_flags);
 }
 
-int fa_version(void) { return 104; }
+int fa_version(void) { return 105; }
 
 }  // extern "C"

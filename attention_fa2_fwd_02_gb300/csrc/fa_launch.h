@@ -22,6 +22,7 @@ struct TcLaunch {
   int grid;
   int device;  // current device ordinal (per-device one-time setup)
   cudaStream_t stream;
+  bool after_vt = false;  // launched behind fa_vt_kernel: programmatic dependent launch
 };
 
 // Kernel variants: (element type, head dim).  Each returns the CUDA error of
@@ -43,6 +44,9 @@ cudaError_t launch_tc_wide_fp32_d128(const TcLaunch& L);
 cudaError_t launch_tc_wide_fp32_d64(const TcLaunch& L);
 cudaError_t launch_tc_wide_fp32_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_wide_fp32_d64_split(const TcLaunch& L);
+// fp32 with V^T in global memory (tmV is then the map of V^T, fa_vt.cuh)
+cudaError_t launch_tc_wide_fp32_d128_vt(const TcLaunch& L);
+cudaError_t launch_tc_wide_fp32_d64_vt(const TcLaunch& L);
 constexpr int kWideQueryTile = 128;
 constexpr int kWideKeyTile = 128;
 

@@ -115,6 +115,17 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the kernel ahead of it on
+// the stream has finished; griddep_wait blocks the calling thread until that
+// kernel has completed and its writes are visible (a no-op for a normal
+// launch), and griddep_launch_dependents lets the dependent kernel start
+// before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

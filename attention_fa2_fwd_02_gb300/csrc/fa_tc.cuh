@@ -103,8 +103,8 @@ struct TcCfg {
   __host__ __device__ static constexpr uint32_t col_o(int s) { return 2 * BN + (s ? D : 0); }
   static constexpr uint32_t kTmemCols = 512;
   // V is used in place as an MN-major B operand (bf16 only: fp32 inputs run
-  // on the single-stage kernel of fa_tc_wide.cuh, which transposes V)
-  static constexpr bool kTransV = false;
+  // on the single-stage kernel of fa_tc_wide.cuh, which takes V^T)
+  static constexpr bool kVKMajor = false;
   // shared memory
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQBytes;
@@ -341,7 +341,7 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint3
 template <class C>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
                                          bool accumulate) {
-  if constexpr (C::kTransV) {
+  if constexpr (C::kVKMajor) {
     // tf32: V^T is [D][BN] with keys contiguous, a K-major B operand like K in
     // Q.K^T, in panels of 32 keys (kVtPanelBytes apart); one MMA takes 8 keys
     const uint64_t b0 = sdesc_sw128<16, 1024>(v_addr);

@@ -37,8 +37,23 @@ static cudaError_t launch_tc_wide(const TcLaunch& L) {
     if (e != cudaSuccess) return e;
     ready[L.device].store(true, std::memory_order_release);
   }
-  fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
-  return cudaGetLastError();
+  if (!L.after_vt) {
+    fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+    return cudaGetLastError();
+  }
+  // behind the V^T pass: start early (barriers, tensor memory, Q and K
+  // copies); the load warp waits for the pass before its first V^T copy
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_tc_wide_kernel<C>, L.tmQ, L.tmK, L.tmV, L.p);
 }
 
 // Geometry of the instantiated configurations (the host side sizes its TMA

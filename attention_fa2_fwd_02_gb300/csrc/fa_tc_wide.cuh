@@ -28,19 +28,25 @@
 //    which the MMA warp consumes them;
 //  * fp32 inputs: tf32-typed tensor maps round Q, K and V to tf32 during the
 //    copy.  The tensor core takes tf32 operands K-major only, so V (keys x
-//    dims, dims contiguous) must become V^T (dims x keys, keys contiguous):
-//    warpgroup 1 transposes each V tile in shared memory -- in its ring slot
-//    when the tile is square (D = BN), else into a buffer of its own -- with a
-//    lane mapping under which no two lanes of a quarter-warp touch the same
-//    bank group (transpose_v_tile).  For bf16, V is used in place as an
-//    MN-major operand and warpgroup 1 has no role;
-//  * fp32 inputs: Q lives in tensor memory, as the A operand of a TS-form
-//    Q.K^T, so that the tensor core reads only K from shared memory (Q re-read
-//    for every key tile would take a third of the shared-memory bandwidth that
-//    the tf32 tile needs).  Its TMA copy goes through the K/V ring like a K
-//    tile, and the epilogue warpgroup moves it into tensor memory (row per
-//    thread), once the previous tile's last Q.K^T is done; the slot it frees
-//    deepens the ring to three tiles of 64 KB;
+//    dims, dims contiguous) must become V^T (dims x keys, keys contiguous).
+//    Two ways:
+//    - VT (fa_vt_kernel has written V^T to global memory, once per call):
+//      the load warp copies V^T tiles like K tiles (BN / 32 panels of 32
+//      keys, each D rows of 128 bytes) and the kernel is the bf16 one with
+//      tf32 arithmetic -- Q in shared memory, two O buffers;
+//    - otherwise warpgroup 1 transposes each V tile in shared memory -- in
+//      its ring slot when the tile is square (D = BN), else into a buffer of
+//      its own -- with a lane mapping under which no two lanes of a
+//      quarter-warp touch the same bank group (transpose_v_tile), and Q
+//      lives in tensor memory, as the A operand of a TS-form Q.K^T, so that
+//      the tensor core reads only K from shared memory (the transposer
+//      already takes much of the shared-memory bandwidth).  Q's TMA copy
+//      goes through the K/V ring like a K tile, and the epilogue warpgroup
+//      moves it into tensor memory (row per thread), once the previous
+//      tile's last Q.K^T is done; the slot it frees deepens the ring to three
+//      tiles of 64 KB.
+//    For bf16, V is used in place as an MN-major operand and warpgroup 1 has
+//    no role;
 //  * split-KV instantiations (SPLIT): work unit u is the key range u mod s of
 //    tile u / s, and writes a normalised partial O and its LSE to the caller's
 //    workspace (merged by fa_combine_kernel), as in fa_tc.cuh;
@@ -51,7 +57,7 @@
 
 namespace fa {
 
-template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false>
+template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false, bool VT_ = false>
 struct TcWideCfg {
   using Elem = T;
   static constexpr bool kSplit = SPLIT_;
@@ -69,14 +75,16 @@ struct TcWideCfg {
   static constexpr uint32_t kKVPanelBytes = BN * 128;
   static constexpr uint32_t kQBytes = BM * D * E;
   static constexpr uint32_t kKVBytes = BN * D * E;
-  // fp32: V^T made by warpgroup 1 (K-major B operand of P.V): panels of 32
-  // keys, each D rows of 128 bytes
-  static constexpr bool kTransV = kTF32;
+  // fp32: the B operand of P.V is V^T (K-major): panels of 32 keys, each D
+  // rows of 128 bytes, copied from global memory (VT) or made by warpgroup 1
+  static constexpr bool kVKMajor = kTF32;
+  static constexpr bool kVtGlobal = VT_;
+  static constexpr bool kTransV = kTF32 && !VT_;
   static constexpr bool kVtInPlace = kTransV && D == BN;
   static constexpr uint32_t kVtPanelBytes = D * 128;
   static constexpr uint32_t kVtBytes = (kTransV && !kVtInPlace) ? D * BN * E : 0;
-  // fp32: Q in tensor memory, its tiles delivered through the ring
-  static constexpr bool kQTmem = kTF32;
+  // fp32 with the transposer: Q in tensor memory, its tiles delivered through the ring
+  static constexpr bool kQTmem = kTransV;
   // tensor-memory columns: S_0 | S_1 | O_0 [| O_1] [| Q]
   static constexpr int kOBufs = kQTmem ? 1 : ((2 * BN + 2 * D <= 512) ? 2 : 1);
   __host__ __device__ static constexpr uint32_t col_s(uint32_t b) { return b * BN; }
@@ -93,7 +101,7 @@ struct TcWideCfg {
   static constexpr uint32_t kOffMisc = kOffStats + BM * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
-  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, kTransV ? 0u : 1u);
+  static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, kVKMajor ? 0u : 1u);
   static constexpr int kThreads = 512;
   // Register split (setmaxnreg): 128 registers x 512 threads at launch; the
   // four warpgroups' shares add up to 4 x 128.  The softmax raises its share
@@ -110,6 +118,7 @@ struct TcWideCfg {
   static_assert(D % kPanelElems == 0 && D <= 256, "head dim: whole swizzle rows, at most 256 (MMA N)");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
   static_assert(!kTransV || (D % 32 == 0 && BN % 32 == 0), "transpose works on 32 x 32 blocks");
+  static_assert(!VT_ || (kTF32 && BN % 32 == 0), "V^T from global memory: fp32, whole 32-key panels");
   static_assert(2 * BN + kOBufs * D + (kQTmem ? D : 0) <= 512, "tensor memory budget");
   static_assert(!kQTmem || (BM == BN && kQBytes == kKVBytes), "Q tiles travel in ring slots");
   static_assert(NSLOT <= 8, "ring slots (the load warp's per-slot bookkeeping)");
@@ -201,6 +210,7 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
   const uint64_t pol_kv = l2_policy_evict_last();
   uint32_t it = 0, q_armed = 0, tile_k = 0;
   uint32_t withheld = ~0u;   // ring entry skipped by the test hook, if any
+  bool vt_ready = false;     // V^T from global memory: the V^T pass has completed
   uint32_t v_loads[C::NSLOT] = {};  // fp32: V tiles issued per slot
   uint32_t last_is_v = 0;    // fp32: bit s = the last entry issued into slot s was a V tile
   uint32_t last_is_q = 0;    // fp32: bit s = ... a Q tile
@@ -225,10 +235,23 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
       }
     }
     mbar_arrive_expect_tx(done, C::kKVBytes);
+    uint8_t* dst = smem + C::kOffKV + slot * C::kKVBytes;
+    if (C::kVtGlobal && is_v) {
+      if (!vt_ready) {  // V^T is written by the kernel ahead of this one on the stream
+        griddep_wait();
+        vt_ready = true;
+      }
+      // V^T [B][H_kv][Dv][keys]: BN / 32 panels of 32 keys x D rows (rows past
+      // Dv and keys past N_k read as zeros)
 #pragma unroll
-    for (int pn = 0; pn < C::kPanels; ++pn)
-      tma_load_4d(map, done, smem + C::kOffKV + slot * C::kKVBytes + pn * C::kKVPanelBytes, pn * C::kPanelElems,
-                  (ti.j0 + j) * C::BN, ti.hk, ti.b, pol_kv);
+      for (int pn = 0; pn < C::BN / 32; ++pn)
+        tma_load_4d(map, done, dst + pn * C::kVtPanelBytes, (ti.j0 + j) * C::BN + pn * 32, 0, ti.hk, ti.b, pol_kv);
+    } else {
+#pragma unroll
+      for (int pn = 0; pn < C::kPanels; ++pn)
+        tma_load_4d(map, done, dst + pn * C::kKVPanelBytes, pn * C::kPanelElems, (ti.j0 + j) * C::BN, ti.hk, ti.b,
+                    pol_kv);
+    }
     if (C::kTransV && is_v) mbar_arrive(&bars.kv_full[slot]);
     return true;
   };

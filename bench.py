@@ -715,6 +715,7 @@ def main():
         flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
 
     n_split = 1  # key-range splits the library picks for this problem
+    vt_bytes = 0  # fp32: bytes of the V^T workspace (the step is then the V^T pass + the attention kernel)
     if bwd:
         # forward outputs (not timed), then the backward as the step
         Od, Ld = fa.fwd(Qd, Kd, Vd, scale=w.scale, is_causal=w.causal, split_kv=1)
@@ -742,6 +743,11 @@ def main():
         if n_split > 1:  # the split path's scratch, allocated once outside the timed region
             ws = torch.empty(fa.lib().fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.N_q, w.d, n_split),
                              dtype=torch.uint8, device=dev)
+        vt_bytes = 0
+        if n_split == 1 and w.v_dim == w.d:  # fp32: V^T written once per call into this scratch
+            vt_bytes = fa.lib().fa_fwd_ws_bytes(code, w.B, w.H, w.kv_heads, w.N_q, w.N_k, w.d)
+            if vt_bytes > 0:
+                ws = torch.empty(vt_bytes, dtype=torch.uint8, device=dev)
 
         def make_step(Qx, Kx, Vx, Ox=None, Lx=None):
             Ox = torch.empty((*Qx.shape[:-1], Vx.shape[-1]), dtype=Qx.dtype, device=dev) if Ox is None else Ox
@@ -894,6 +900,8 @@ def main():
                 "frac": achieved / peak, "traffic": traffic, "peak_source": note}
         if n_split > 1:  # the events bracket both launches of a split step
             roof["timed"] = f"split-KV attention kernel (n_split={n_split}) + merge kernel"
+        if vt_bytes > 0:  # ... and both launches of an fp32 step with the V^T pass
+            roof["timed"] = "V^T pass (fa_vt_kernel) + tf32 attention kernel"
         tile = 256 if max(w.d, w.v_dim) > 128 else (128 if max(w.d, w.v_dim) > 64 else 64)
         if not axial and not bwd and (w.d != tile or w.v_dim != tile) and w.d not in (16, 32):
             roof["tile_columns"] = (f"d={w.d}, Dv={w.v_dim} run on {tile}-column tiles: the tensor work is "
@@ -1007,6 +1015,8 @@ def main():
         cfg["parallelism"] = f"replicas x{world} (independent problems per GPU)"
         cfg["cuda_graph"] = use_graph
         cfg["split_kv"] = n_split
+        if vt_bytes > 0:
+            cfg["v_transpose"] = f"V^T pass into a {vt_bytes / 2**20:.1f} MB workspace, then K-major V^T tiles"
         if args.api == "sdpa":
             cfg["api"] = "torch.nn.functional.scaled_dot_product_attention routed to this library"
         if bwd:
@@ -1019,8 +1029,10 @@ def main():
             "data": "synthetic (seeded i.i.d. N(0,1))", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             # one kernel per step, plus the merge kernel when the keys are split
+            # or the V^T pass before it (fp32)
             # (a backward step is three launches: preprocess, kernel, dQ conversion)
-            "gpu_launches": steps * (3 if bwd else (2 if n_split > 1 else 1)), "kernel_ms": kernel_ms,
+            "gpu_launches": steps * (3 if bwd else (2 if (n_split > 1 or vt_bytes > 0) else 1)),
+            "kernel_ms": kernel_ms,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -109,6 +109,41 @@ fa_status_t fa_fwd_gqa(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int
                        int64_t d, const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
                        int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3], void* stream);
 
+/*
+ * fa_fwd_ws -- fa_fwd_gqa with a caller-owned workspace, which the fp32
+ * tensor-core path uses to hold V transposed ("Blackwell Attention Example",
+ * section "Attention Kernel Implementation": O accumulates P.V tile by tile).
+ *
+ * Why: with fp32 inputs both contractions run on the tf32 tensor cores, which
+ * take their operands only with the reduction index contiguous; for P.V that
+ * index is the key, and V [B, H_kv, N_k, d] has the head dims contiguous.
+ * fa_fwd transposes every V tile in shared memory, once per query tile that
+ * reads it.  fa_fwd_ws first writes V^T once into `workspace` (one pass that
+ * reads and writes V's bytes), and the attention kernel then loads V^T tiles
+ * the way it loads K tiles -- faster whenever a V tile is read by two or more
+ * query tiles.  The results equal fa_fwd's up to the order of fp32 additions.
+ *
+ *   workspace        device memory of at least fa_fwd_ws_bytes(dtype, B, H,
+ *                    H_kv, N_q, N_k, d) bytes, 256-byte aligned, owned by the
+ *                    caller; its contents are scratch (V^T, fp32
+ *                    [B * H_kv][d][N_k rounded up to 32]).  Calls that may
+ *                    overlap on the device need separate workspaces.
+ *   workspace_bytes  its size; less than required is FA_ERR_INVALID_ARG.
+ *   other arguments  as fa_fwd_gqa.
+ *
+ * fa_fwd_ws_bytes is 0 where no workspace is used: bf16 inputs, the
+ * small-head path (d = 16, 32), and fp32 problems whose V tiles are each read
+ * by a single query tile (ceil(N_q / 128) * H / H_kv == 1); fa_fwd_ws is then
+ * fa_fwd_gqa and `workspace` may be NULL.  It is also 0 for arguments that
+ * fa_fwd_gqa rejects.
+ */
+size_t fa_fwd_ws_bytes(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d);
+
+fa_status_t fa_fwd_ws(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_k, int64_t d,
+                      const fa_tensor_t* Q, const fa_tensor_t* K, const fa_tensor_t* V, float scale,
+                      int is_causal, const fa_tensor_t* O, float* LSE, const int64_t lse_stride[3],
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* One problem of a grouped call: the arguments of fa_fwd_gqa, by value.
  * H_kv = 0 means H_kv = H (K and V have the query heads).
  * Dv: head dim of V and O when it differs from d ("Blackwell Attention

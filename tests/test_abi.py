@@ -47,7 +47,7 @@ def test_library_is_built_for_sm103a():
 def test_status_strings(L):
     assert L.fa_status_string(0) == b"ok"
     assert L.fa_status_string(4) == b"device wait timed out"
-    assert L.fa_version() == 104
+    assert L.fa_version() == 105
 
 
 def _t(ptr, strides):
@@ -262,3 +262,39 @@ def test_problem_value_dim_validation(L):
     assert L.fa_fwd_grouped(fa.FA_BF16, 1, ctypes.byref(pb), None) == fa.FA_ERR_UNSUPPORTED
     pb.Dv = 136
     assert L.fa_fwd_grouped(fa.FA_FP32, 1, ctypes.byref(pb), None) == fa.FA_ERR_UNSUPPORTED  # fp32 stops at 128
+
+
+def _fwd_ws(L, dtype=fa.FA_FP32, B=1, H=2, H_kv=2, Nq=256, Nk=300, d=128, ws=0x100000, ws_bytes=1 << 30):
+    sq, sk = (H * Nq * d, Nq * d, d, 1), (H_kv * Nk * d, Nk * d, d, 1)
+    Q, O = _t(0x10000, sq), _t(0x40000, sq)
+    K, V = _t(0x20000, sk), _t(0x30000, sk)
+    ls = (ctypes.c_int64 * 3)(H * Nq, Nq, 1)
+    return L.fa_fwd_ws(dtype, B, H, H_kv, Nq, Nk, d, ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V),
+                       0.1, 0, ctypes.byref(O), None, ls, ws, ws_bytes, None)
+
+
+def test_fwd_ws_bytes(L):
+    # fp32 V^T: B * H_kv rows of d, each N_k rounded up to 32 keys, fp32
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 2, 4, 2, 256, 300, 128) == 2 * 2 * 128 * 320 * 4
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 1, 1, 1, 129, 64, 96) == 96 * 64 * 4
+    # a V tile read by one query tile only (one query block, one query head per K/V head): none
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 3, 2, 2, 128, 4096, 128) == 0
+    # ... but two query heads per K/V head read each V tile twice
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 1, 2, 1, 128, 64, 64) == 64 * 64 * 4
+    # bf16, the small-head path and rejected arguments: none
+    assert L.fa_fwd_ws_bytes(fa.FA_BF16, 2, 4, 2, 256, 300, 128) == 0
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 1, 1, 1, 4096, 4096, 16) == 0
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 1, 4, 3, 256, 256, 128) == 0   # H_kv does not divide H
+    assert L.fa_fwd_ws_bytes(fa.FA_FP32, 1, 1, 1, 256, 256, 136) == 0   # above the fp32 tile
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),             # needed, not given
+    (dict(ws=0x100040), fa.FA_ERR_INVALID_ARG),      # not 256-byte aligned
+    (dict(ws_bytes=128 * 320 * 4 * 2 - 1), fa.FA_ERR_INVALID_ARG),  # one byte short
+    (dict(d=102), fa.FA_ERR_UNSUPPORTED),            # usual validation first (408-byte rows)
+    (dict(H_kv=3), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_ws_host_validation(L, kw, status):
+    assert _fwd_ws(L, **kw) == status
+    assert L.fa_last_error() != b""

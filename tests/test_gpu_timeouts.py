@@ -7,11 +7,13 @@ context is correct against the oracle.  No GPU fault, trap or hang is
 involved: a wait that gives up only returns.
 
 Kernels covered: the two-stage forward (bf16; plain, split-KV and packed
-variable-length instantiations), the single-stage forward (bf16 d = 256,
-fp32 d = 128 and 64, fp32 split-KV) and the backward.
+variable-length instantiations), the single-stage forward (bf16 d = 256;
+fp32 d = 128 and 64 both with V^T from the workspace and with the in-kernel
+V transpose; fp32 split-KV) and the backward.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import numpy as np
@@ -58,28 +60,49 @@ def _close(O, L, O_ref, L_ref, dtype, what):
     assert eo <= to and el <= tl, f"{what}: max|dO|={eo:.3e} max|dLSE|={el:.3e}"
 
 
-# (name, dtype, N_q, N_k, d, causal, split): every case gives block 0 a first
-# work unit with at least two key tiles, so the withheld second K tile is awaited
+def _fwd_no_workspace(Q, K, V, scale, causal, out, lse):
+    """fa_fwd_gqa straight through the C ABI: for fp32, the in-kernel V
+    transpose (the binding would pass a workspace and take the V^T pass)."""
+    pb, out, lse = fa._problem(Q, K, V, scale, causal, out, lse, True)
+    st = fa.lib().fa_fwd_gqa(fa._dtype_code(Q), pb.B, pb.H, pb.H_kv, pb.N_q, pb.N_k, pb.d, ctypes.byref(pb.Q),
+                             ctypes.byref(pb.K), ctypes.byref(pb.V), pb.scale, pb.is_causal, ctypes.byref(pb.O),
+                             pb.LSE, (ctypes.c_int64 * 3)(*pb.lse_stride), fa._stream_ptr(Q.device))
+    fa._raise_on(st)
+
+
+# (name, dtype, N_q, N_k, d, causal, split, workspace): every case gives block
+# 0 a first work unit with at least two key tiles, so the withheld second K
+# tile is awaited.  workspace=False calls fa_fwd_gqa (fp32: in-kernel V
+# transpose); True goes through the binding (fp32: the V^T pass).
 FWD_CASES = [
-    ("two_stage_bf16_d128_split", torch.bfloat16, 256, 2048, 128, False, 2),
-    ("two_stage_bf16_d64_causal", torch.bfloat16, 384, 384, 64, True, 1),
-    ("single_stage_bf16_d256", torch.bfloat16, 256, 512, 256, False, 1),
-    ("single_stage_fp32_d128", torch.float32, 256, 512, 128, False, 1),
-    ("single_stage_fp32_d64_causal", torch.float32, 300, 300, 64, True, 1),
-    ("single_stage_fp32_d128_split", torch.float32, 128, 2048, 128, False, 2),
+    ("two_stage_bf16_d128_split", torch.bfloat16, 256, 2048, 128, False, 2, True),
+    ("two_stage_bf16_d64_causal", torch.bfloat16, 384, 384, 64, True, 1, True),
+    ("single_stage_bf16_d256", torch.bfloat16, 256, 512, 256, False, 1, True),
+    ("single_stage_fp32_vt_d128", torch.float32, 256, 512, 128, False, 1, True),
+    ("single_stage_fp32_vt_d64_causal", torch.float32, 300, 300, 64, True, 1, True),
+    ("single_stage_fp32_d128", torch.float32, 256, 512, 128, False, 1, False),
+    ("single_stage_fp32_d64_causal", torch.float32, 300, 300, 64, True, 1, False),
+    ("single_stage_fp32_d128_split", torch.float32, 128, 2048, 128, False, 2, True),
 ]
 
 
 @pytest.mark.parametrize("case", FWD_CASES, ids=[c[0] for c in FWD_CASES])
 def test_forward_withheld_tile_times_out_then_runs_correctly(oracle_mod, case):
-    name, dtype, nq, nk, d, causal, split = case
+    name, dtype, nq, nk, d, causal, split, workspace = case
     Q, K, V = qkv((1, 2, nq, d), (1, 2, nk, d), 91 + d + nk, dtype)
     Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
     scale = 1 / math.sqrt(d)
-    _times_out(lambda: fa.fwd(Qd, Kd, Vd, scale=scale, is_causal=causal, split_kv=split))
+
+    def run(out=None, lse=None):
+        if workspace:
+            fa.fwd(Qd, Kd, Vd, scale=scale, is_causal=causal, split_kv=split, out=out, lse=lse)
+        else:
+            _fwd_no_workspace(Qd, Kd, Vd, scale, causal, out, lse)
+
+    _times_out(run)
     O = torch.full(Qd.shape, float("nan"), dtype=dtype, device="cuda")
     L = torch.full(Qd.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
-    fa.fwd(Qd, Kd, Vd, scale=scale, is_causal=causal, split_kv=split, out=O, lse=L)
+    run(O, L)
     fa.check()
     O_ref, L_ref = oracle_mod.attention(Q, K, V, scale, causal)
     _close(O, L, O_ref, L_ref, dtype, name)

@@ -163,9 +163,27 @@ struct TileInfo {
 // the causal work is handed out longest-first.  Work unit u is split
 // u % n_split of tile u / n_split: the tile's key tiles are cut into
 // min(n_split, #tiles) balanced ranges; the remaining splits are empty.
+// Causal schedules (tiles of unequal length, longest first): the work units
+// of one round -- one per CTA of the persistent grid -- are dealt in
+// alternating directions.  In round k, CTA c takes unit k*G + c for even k and
+// k*G + (r - 1 - c) for odd k (r = units in that round), so a CTA that took one
+// of the longest tiles of a round takes one of the shortest of the next.  A
+// permutation of [0, n_units); every role applies it to the same u.
+__device__ __forceinline__ int snake_unit(int u, int n_units) {
+  const int G = gridDim.x;
+  const int k = u / G;
+  if ((k & 1) == 0) return u;
+  const int base = k * G;
+  const int r = min(G, n_units - base);
+  return base + r - 1 - (u - base);
+}
+
 template <class C>
 __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   constexpr int BN = C::BN;
+  // (not for packed batches: their blocks are ordered by sequence, and the
+  // alternating rounds measured 5 % slower there)
+  if (!C::kVarlen && p.causal != kNoCausal) u = snake_unit(u, p.n_units);
   if constexpr (C::kVarlen) {
     // virtual tiles in the order of the batched tiles: groups of head_group
     // (b, h) pairs (sized on the host so that their K/V stay in L2), inside a

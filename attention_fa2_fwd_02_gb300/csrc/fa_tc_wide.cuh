@@ -153,6 +153,7 @@ struct WideBars {
 // empty (n_kv = 0).
 template <class C>
 __device__ __forceinline__ TileInfo wide_tile_info(const TcParams& p, int u) {
+  if (p.causal != kNoCausal) u = snake_unit(u, p.n_units);
   const int t = C::kSplit ? u / p.n_split : u;
   const int split = C::kSplit ? u - t * p.n_split : 0;
   const int BH = p.B * p.H;

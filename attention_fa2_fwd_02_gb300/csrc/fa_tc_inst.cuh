@@ -38,7 +38,7 @@ static cudaError_t launch_tc_wide(const TcLaunch& L) {
     ready[L.device].store(true, std::memory_order_release);
   }
   if (!L.after_vt) {
-    fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+    fa_tc_wide_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmO, L.p);
     return cudaGetLastError();
   }
   // behind the V^T pass: start early (barriers, tensor memory, Q and K
@@ -53,7 +53,7 @@ static cudaError_t launch_tc_wide(const TcLaunch& L) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_tc_wide_kernel<C>, L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaLaunchKernelEx(&cfg, fa_tc_wide_kernel<C>, L.tmQ, L.tmK, L.tmV, L.tmO, L.p);
 }
 
 // Geometry of the instantiated configurations (the host side sizes its TMA

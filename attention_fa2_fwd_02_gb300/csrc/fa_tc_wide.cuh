@@ -47,6 +47,12 @@
 //      tiles of 64 KB.
 //    For bf16, V is used in place as an MN-major operand and warpgroup 1 has
 //    no role;
+//  * the epilogue writes O with TMA stores: each of its warps converts one
+//    128-byte column chunk of its 32 rows into a swizzled 4 KB shared-memory
+//    buffer (two per warp, so the next chunk is written while the last one's
+//    store still reads) and one lane issues the store.  Row-per-thread global
+//    stores put 32 rows 512 bytes apart into every store instruction, and
+//    their load on the memory pipeline slowed the next tile's softmax;
 //  * split-KV instantiations (SPLIT): work unit u is the key range u mod s of
 //    tile u / s, and writes a normalised partial O and its LSE to the caller's
 //    workspace (merged by fa_combine_kernel), as in fa_tc.cuh;
@@ -95,7 +101,12 @@ struct TcWideCfg {
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = kQTmem ? 0 : kQBytes;
   static constexpr uint32_t kOffVt = kOffKV + NSLOT * kKVBytes;
-  static constexpr uint32_t kOffBar = kOffVt + kVtBytes;
+  // O leaves through shared memory and TMA stores (unsplit): per epilogue warp
+  // two 4 KB buffers, each 32 rows x one 128-byte column chunk
+  static constexpr bool kTmaStore = !SPLIT_;
+  static constexpr uint32_t kStageBytes = kTmaStore ? 4 * 2 * 32 * 128 : 0;
+  static constexpr uint32_t kOffStage = kOffVt + kVtBytes;
+  static constexpr uint32_t kOffBar = kOffStage + kStageBytes;
   static constexpr int kNumBars = 15 + 4 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMisc = kOffStats + BM * 8;
@@ -701,13 +712,15 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
 
 // ------------------------------------------------------- epilogue warpgroup
 template <class C>
-__device__ void wide_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tmem, const WideBars& bars,
-                                   const float2* stats, const Watchdog& wd) {
+__device__ void wide_epilogue_role(const CUtensorMap* tmO, const TcParams& p, uint8_t* smem, uint32_t tmem,
+                                   const WideBars& bars, const float2* stats, const Watchdog& wd) {
   using T = typename C::Elem;
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  uint8_t* stage = smem + C::kOffStage + wq * (2 * 32 * 128);  // this warp's two store buffers
+  uint32_t n_st = 0;                                           // chunks this warp has stored
   // O / l of tile number k (this CTA's k-th unit with keys), and its LSE
   auto store_tile = [&](const TileInfo& ti, uint32_t k) -> bool {
     const uint32_t ob = k % C::kOBufs;
@@ -725,6 +738,52 @@ __device__ void wide_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tm
     // workspace; the combine kernel merges the splits into O and LSE
     const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
     const int dv = C::kSplit ? C::D : p.dv;  // columns of O to store (<= D)
+    if constexpr (C::kTmaStore) {
+      // rows ti.q0 + 32 wq .. + 31 (TMA drops rows past N_q and columns past Dv)
+      const bool any_row = ti.q0 + wq * 32 < p.N_q;
+#pragma unroll 1
+      for (int c = 0; c < dv; c += C::kPanelElems) {
+        uint32_t w[32];  // this row's 128 bytes of the chunk
+        if constexpr (C::kTF32) {
+          tmem_ld32(tO + c, w);
+          tmem_ld_wait32(w);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * st.x);
+        } else {
+          uint32_t o[64];
+          tmem_ld32(tO + c, o);
+          tmem_ld32(tO + c + 32, o + 32);
+          tmem_ld_wait32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * st.x, __uint_as_float(o[2 * i + 1]) * st.x);
+        }
+        if (!any_row) continue;
+        uint8_t* buf = stage + (n_st & 1u) * (32 * 128);
+        if (n_st >= 2) {  // the store that last read this buffer
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+        }
+        // row `lane` of the buffer, 16-byte chunk i at position i ^ (row mod 8)
+        // (the 128-byte swizzle of the tensor map)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(tmO, buf, c, ti.q0 + wq * 32, ti.h, ti.b);
+          bulk_commit();
+        }
+        ++n_st;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.o_empty[ob]);
+      if (valid && p.LSE)
+        p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
+      return true;
+    }
 #pragma unroll 1
     for (int c = 0; c < dv; c += 32) {
       uint32_t o[32];
@@ -764,6 +823,7 @@ __device__ void wide_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tm
   uint32_t tile_k = 0, it = 0;
   TileInfo prev{};
   bool have_prev = false;
+  auto run = [&]() {
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
     if (!wide_counted<C>(ti)) continue;
@@ -804,13 +864,22 @@ __device__ void wide_epilogue_role(const TcParams& p, uint8_t* smem, uint32_t tm
     }
   }
   if (C::kQTmem && have_prev) store_tile(prev, tile_k - 1);
+  };
+  run();
+  // the O stores must have read their buffers (and landed) before the CTA's
+  // shared memory goes away, on every exit path
+  if constexpr (C::kTmaStore) {
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
 }
 
 // ------------------------------------------------------------------ kernel
 template <class C>
 __global__ void __launch_bounds__(512, 1)
 fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ TcParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -865,6 +934,7 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
+    if (C::kTmaStore) prefetch_tensormap(&tmO);
   }
   if (warp == 13) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -883,7 +953,7 @@ fa_tc_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     if (warp == 13) wide_mma_role<C>(p, smem, tmem, bars, wd);
   } else if (wg == 2) {
     setmaxnreg_dec<C::kRegEpilogue>();
-    wide_epilogue_role<C>(p, smem, tmem, bars, stats, wd);
+    wide_epilogue_role<C>(&tmO, p, smem, tmem, bars, stats, wd);
   } else if (wg == 1) {
     setmaxnreg_dec<C::kRegWg1>();
     if constexpr (C::kTransV) wide_transpose_role<C>(p, smem, bars, wd, threadIdx.x - 128);

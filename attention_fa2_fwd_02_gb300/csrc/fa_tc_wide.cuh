@@ -778,14 +778,9 @@ __device__ void wide_epilogue_role(const CUtensorMap* tmO, const TcParams& p, ui
         }
         ++n_st;
       }
-      tc_fence_before();
-      mbar_arrive(&bars.o_empty[ob]);
-      if (valid && p.LSE)
-        p.LSE[ti.b * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(q) * p.lse_stride[2]] = st.y;
-      return true;
     }
 #pragma unroll 1
-    for (int c = 0; c < dv; c += 32) {
+    for (int c = 0; !C::kTmaStore && c < dv; c += 32) {
       uint32_t o[32];
       tmem_ld32(tO + c, o);
       tmem_ld_wait32(o);

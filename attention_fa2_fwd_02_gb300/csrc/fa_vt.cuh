@@ -47,9 +47,7 @@ constexpr int kVtKeys = 64;     // keys per CTA
 // c .. c + 3 with c = 32 s + 4 (l mod 8), all eight of a thread's loads
 // issued before any is used; the stores into the row-major tile (row stride
 // kVtMaxDim + 1 = 1 mod 32 words) then fall on bank key + c + i, distinct
-// over the warp.  Stores: a warp writes 32 keys of one V^T row (one 128-byte
-// line) per instruction, lane = key, reading tile[key][c] -- bank key + c,
-// again distinct.
+// over the warp.
 __global__ void __launch_bounds__(256) fa_vt_kernel(const VtParams p) {
   __shared__ float tile[kVtKeys][kVtMaxDim + 1];
   // the attention kernel behind this one may start now: it waits for this
@@ -88,12 +86,24 @@ __global__ void __launch_bounds__(256) fa_vt_kernel(const VtParams p) {
     }
   }
   __syncthreads();
+  // stores: a warp instruction writes four V^T rows x 32 keys (four 128-byte
+  // lines), lane l taking row c0 + l / 8 and keys 4 (l mod 8) .. + 3 of a
+  // 32-key half; its four shared-memory reads tile[k + i][c] fall on bank
+  // k + i + c, distinct over the warp for each i
   float* dst = p.Vt + static_cast<long long>(bh) * p.dv * p.ldk + k0;
+  const int kq = 4 * (lane & 7);
+#pragma unroll 1
+  for (int c0 = 4 * warp; c0 < p.dv; c0 += 32) {
+    const int c = c0 + (lane >> 3);
 #pragma unroll
-  for (int half = 0; half < kVtKeys / 32; ++half) {
-    const int key = half * 32 + lane;
-    if (k0 + key < p.N_k)
-      for (int c = warp; c < p.dv; c += 8) dst[static_cast<long long>(c) * p.ldk + key] = tile[key][c];
+    for (int half = 0; half < kVtKeys / 32; ++half) {
+      const int k = half * 32 + kq;
+      if (c < p.dv && k0 + k < p.N_k) {
+        const float4 w = make_float4(tile[k][c], tile[k + 1][c], tile[k + 2][c], tile[k + 3][c]);
+        // keys past N_k (at most 3, inside the 32-key padding of ldk) are written too
+        *reinterpret_cast<float4*>(dst + static_cast<long long>(c) * p.ldk + k) = w;
+      }
+    }
   }
 }
 

@@ -45,9 +45,16 @@ constexpr int kVtKeys = 64;     // keys per CTA
 // through shared memory.  Loads: a warp instruction reads 4 key rows x 32
 // values (four 128-byte segments), lane l taking key 4g + l / 8 and values
 // c .. c + 3 with c = 32 s + 4 (l mod 8), all eight of a thread's loads
-// issued before any is used; the stores into the row-major tile (row stride
+// issued before any is used (streaming loads: V is read once); the stores into the row-major tile (row stride
 // kVtMaxDim + 1 = 1 mod 32 words) then fall on bank key + c + i, distinct
 // over the warp.
+// A 16-byte store that asks L2 to keep the line (evict-last policy).
+__device__ __forceinline__ void st_evict_last(float4* dst, const float4& v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(256) fa_vt_kernel(const VtParams p) {
   __shared__ float tile[kVtKeys][kVtMaxDim + 1];
   // the attention kernel behind this one may start now: it waits for this
@@ -71,7 +78,7 @@ __global__ void __launch_bounds__(256) fa_vt_kernel(const VtParams p) {
     const int c = (u / kGroups) * 32 + 4 * (lane & 7);
     v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (u / kGroups < segs && k0 + key < p.N_k && c < p.dv)
-      v[t] = *reinterpret_cast<const float4*>(src + static_cast<long long>(k0 + key) * p.s2 + c);
+      v[t] = __ldcs(reinterpret_cast<const float4*>(src + static_cast<long long>(k0 + key) * p.s2 + c));
   }
 #pragma unroll
   for (int t = 0; t < kItems; ++t) {
@@ -92,6 +99,7 @@ __global__ void __launch_bounds__(256) fa_vt_kernel(const VtParams p) {
   // k + i + c, distinct over the warp for each i
   float* dst = p.Vt + static_cast<long long>(bh) * p.dv * p.ldk + k0;
   const int kq = 4 * (lane & 7);
+  const uint64_t pol = l2_policy_evict_last();  // V^T is read again by every query tile of its head
 #pragma unroll 1
   for (int c0 = 4 * warp; c0 < p.dv; c0 += 32) {
     const int c = c0 + (lane >> 3);
@@ -101,7 +109,7 @@ __global__ void __launch_bounds__(256) fa_vt_kernel(const VtParams p) {
       if (c < p.dv && k0 + k < p.N_k) {
         const float4 w = make_float4(tile[k][c], tile[k + 1][c], tile[k + 2][c], tile[k + 3][c]);
         // keys past N_k (at most 3, inside the 32-key padding of ldk) are written too
-        *reinterpret_cast<float4*>(dst + static_cast<long long>(c) * p.ldk + k) = w;
+        st_evict_last(reinterpret_cast<float4*>(dst + static_cast<long long>(c) * p.ldk + k), w, pol);
       }
     }
   }

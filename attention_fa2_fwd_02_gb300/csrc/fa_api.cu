@@ -252,8 +252,9 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   // the single-stage kernel (fa_tc_wide.cuh): bf16 tiles of 256 columns and
   // every fp32 problem (split or not)
   const bool wide = d == 256 || fp32;
-  const int bn = wide ? kWideKeyTile : tc_key_tile(fp32, d);
-  const int bm = wide ? kWideQueryTile : 256;  // query rows of a CTA tile
+  const int stages = tc_stages(fp32, d, pb.is_causal != 0, n_split > 1);  // (two-stage kernel)
+  const int bn = wide ? kWideKeyTile : tc_key_tile(stages);
+  const int bm = wide ? kWideQueryTile : tc_tile_rows(stages);  // query rows of a CTA tile
   TcLaunch L;
   fa_status_t st;
   if ((st = make_map(&L.tmQ, pb.Q, fp32, pb.B, pb.H, pb.N_q, pb.d, 128, "Q")) != FA_OK) return st;
@@ -333,7 +334,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   } else if (n_split > 1) {
     e = d == 128 ? launch_tc_bf16_d128_split(L) : launch_tc_bf16_d64_split(L);
   } else {
-    e = d == 128 ? launch_tc_bf16_d128(L) : launch_tc_bf16_d64(L);
+    e = d == 128 ? launch_tc_bf16_d128(L) : (stages == 3 ? launch_tc_bf16_d64(L) : launch_tc_bf16_d64_causal(L));
   }
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, cuda_msg("tensor-core kernel launch", e));
   if (n_split > 1) {
@@ -381,8 +382,10 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
 int choose_split(bool fp32, long long B, long long H, long long N_q, long long N_k, long long d, int causal,
                  int sm_count) {
   if (fp32 || causal || (d != 64 && d != 128) || sm_count <= 0) return 1;
-  const long long bn = tc_key_tile(fp32, (int)d);
-  const long long tiles = B * H * ((N_q + 255) / 256);
+  const int stages = tc_stages(fp32, (int)d, false, true);
+  const long long bn = tc_key_tile(stages);
+  const long long bm = tc_tile_rows(stages);
+  const long long tiles = B * H * ((N_q + bm - 1) / bm);
   const long long n_kv = (N_k + bn - 1) / bn;
   auto cost = [&](long long s) {
     const long long waves = (tiles * s + sm_count - 1) / sm_count;

@@ -30,7 +30,8 @@ struct TcLaunch {
 // the launch (cudaSuccess when it was queued).  Two-stage kernel (fa_tc.cuh),
 // bf16, 256-row CTA tiles:
 cudaError_t launch_tc_bf16_d128(const TcLaunch& L);
-cudaError_t launch_tc_bf16_d64(const TcLaunch& L);
+cudaError_t launch_tc_bf16_d64(const TcLaunch& L);         // three stages
+cudaError_t launch_tc_bf16_d64_causal(const TcLaunch& L);  // two stages
 // split-KV variants (L.p.n_split > 1, L.p.ws_o / ws_lse set)
 cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L);
 cudaError_t launch_tc_bf16_d64_split(const TcLaunch& L);
@@ -69,10 +70,21 @@ cudaError_t launch_bwd_bf16(const BwdLaunch& L);
 // (for entry points defined outside fa_api.cu).
 fa_status_t report_error(fa_status_t st, const std::string& msg);
 
-// Tile geometry shared with the instantiations in fa_tc_*.cu: key-tile width
-// (128 keys for every instantiation) and TMA box width (one 128-byte swizzle
-// row: 64 bf16 or 32 fp32 values).
-constexpr int tc_key_tile(bool, int) { return 128; }
+// Tile geometry shared with the instantiations in fa_tc_*.cu (the batched,
+// not packed, two-stage kernel):
+//  * query stages of a CTA tile: three for bf16 tiles of 64 columns when the
+//    problem is not causal or is split (3 x (96 S + 64 O) tensor-memory
+//    columns; measured +5..8 % on the d = 64 shapes, but -3 % causal, where
+//    the larger diagonal block masks more work), else two;
+//  * key-tile width: 96 keys with three stages, else 128;
+//  * query rows of a CTA tile: 128 per stage;
+//  * TMA box width: one 128-byte swizzle row, 64 bf16 or 32 fp32 values.
+// (Packed batches keep two stages, 128-key tiles and 256-row virtual tiles.)
+constexpr int tc_stages(bool fp32, int d, bool causal, bool split) {
+  return (!fp32 && d <= 64 && (split || !causal)) ? 3 : 2;
+}
+constexpr int tc_key_tile(int stages) { return stages == 3 ? 96 : 128; }
+constexpr int tc_tile_rows(int stages) { return 128 * stages; }
 constexpr int tc_box_inner(bool fp32) { return fp32 ? 32 : 64; }
 
 }  // namespace fa

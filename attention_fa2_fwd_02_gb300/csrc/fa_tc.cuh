@@ -48,7 +48,7 @@ struct TcParams {
   int causal;             // kNoCausal: no mask; else key j is visible to row i iff j <= i + causal
                           // (0: top-left alignment, N_k - N_q: bottom-right)
   float scale_log2;       // scale * log2(e)
-  int n_qblk;             // ceil(N_q / 256)
+  int n_qblk;             // ceil(N_q / tile rows): 256 (two-stage kernel), 384 (three stages), 128 (single-stage)
   int n_tiles;            // B * H * n_qblk
   union {
     int n_split;          // split-KV instantiations: key-range splits per tile
@@ -75,9 +75,14 @@ struct TcParams {
   int debug_flags;
 };
 
-template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false, bool VARLEN_ = false>
+template <typename T, int D_, int BN_, int NSLOT_, bool SPLIT_ = false, bool VARLEN_ = false, int NST_ = 2>
 struct TcCfg {
   using Elem = T;
+  // query stages of 128 rows per CTA tile, one softmax warpgroup each.  With
+  // three (d = 64: 3 x (96 S + 64 O) tensor-memory columns), warpgroup 2 is a
+  // softmax group too and every softmax group writes its own rows of O.
+  static constexpr int NST = NST_;
+  static constexpr bool kOwnEpilogue = NST > 2;
   // variable-length instantiation: B packed sequences (offsets cu_q, cu_k;
   // N_q, N_k = the packed totals), tiles over B x H x ceil(max_len_q / 256)
   static constexpr bool kVarlen = VARLEN_;
@@ -98,50 +103,53 @@ struct TcCfg {
   static constexpr uint32_t kKVPanelBytes = BN * 128;
   static constexpr uint32_t kQBytes = BM * D * E;
   static constexpr uint32_t kKVBytes = BN * D * E;
-  // tensor-memory columns: S0 | S1 | O0 | O1   (P_s overwrites S_s)
-  __host__ __device__ static constexpr uint32_t col_s(int s) { return s ? BN : 0; }
-  __host__ __device__ static constexpr uint32_t col_o(int s) { return 2 * BN + (s ? D : 0); }
+  static constexpr int kTileRows = NST * BM;       // query rows of a CTA tile
+  // tensor-memory columns: S_0 .. S_{NST-1} | O_0 .. O_{NST-1}   (P_s overwrites S_s)
+  __host__ __device__ static constexpr uint32_t col_s(int s) { return s * BN; }
+  __host__ __device__ static constexpr uint32_t col_o(int s) { return NST * BN + s * D; }
   static constexpr uint32_t kTmemCols = 512;
   // V is used in place as an MN-major B operand (bf16 only: fp32 inputs run
   // on the single-stage kernel of fa_tc_wide.cuh, which takes V^T)
   static constexpr bool kVKMajor = false;
   // shared memory
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffKV = 2 * kQBytes;
+  static constexpr uint32_t kOffKV = NST * kQBytes;
   static constexpr uint32_t kOffBar = kOffKV + NSLOT * kKVBytes;
-  static constexpr int kNumBars = 16 + 2 * NSLOT + 1;
+  static constexpr int kNumBars = 8 * NST + 2 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kOffMisc = kOffStats + 2 * BM * 8;
+  static constexpr uint32_t kOffMisc = kOffStats + NST * BM * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
   static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, 1);
   static constexpr int kThreads = 512;
   // Register split (setmaxnreg) of the 4 warpgroups; 128 registers x 512
   // threads at launch, so the shares must add up to 4 x 128.
-  static constexpr uint32_t kRegSoftmax = 184;
-  static constexpr uint32_t kRegEpilogue = 64;
+  static constexpr uint32_t kRegSoftmax = NST == 2 ? 184 : 144;
+  static constexpr uint32_t kRegEpilogue = NST == 2 ? 64 : 0;   // (three stages: no epilogue group)
   static constexpr uint32_t kRegProducer = 80;  // load warp + MMA warp
-  static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 4 * 128, "register split");
+  static_assert(NST * kRegSoftmax + kRegEpilogue + kRegProducer == 4 * 128, "register split");
+  static_assert(NST == 2 || NST == 3, "two or three query stages");
   static_assert(kRegSoftmax >= 128 && kRegEpilogue <= 128 && kRegProducer <= 128,
                 "setmaxnreg.inc raises, setmaxnreg.dec lowers");
 
   static_assert(!kTF32, "fp32 inputs run on the single-stage kernel (fa_tc_wide.cuh)");
   static_assert(D % kPanelElems == 0, "head dim must fill whole swizzle rows");
   static_assert(BN % 32 == 0 && BN <= 256, "key tile");
-  static_assert(2 * BN + 2 * D <= 512, "tensor memory budget");
+  static_assert(NST * (BN + D) <= 512, "tensor memory budget");
+  static_assert(!(kVarlen && NST != 2), "packed batches: 256-row virtual tiles");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(!(kSplit && kVarlen), "split-KV and varlen are separate instantiations");
 };
 
-struct Bars {
-  uint64_t* q_full;     // [2] TMA -> MMA
-  uint64_t* q_empty;    // [2] MMA -> TMA
-  uint64_t* s_full;     // [2] MMA -> softmax
-  uint64_t* p_full;     // [2] softmax -> MMA  (128 arrivals)
-  uint64_t* o_full;     // [2] MMA -> epilogue (last P.V of a tile done)
-  uint64_t* o_empty;    // [2] epilogue -> MMA (128 arrivals)
-  uint64_t* st_full;    // [2] softmax -> epilogue: row stats written (128 arrivals)
-  uint64_t* st_empty;   // [2] epilogue -> softmax (128 arrivals)
+struct Bars {            // [NST]: one per query stage
+  uint64_t* q_full;     // [NST] TMA -> MMA
+  uint64_t* q_empty;    // [NST] MMA -> TMA
+  uint64_t* s_full;     // [NST] MMA -> softmax
+  uint64_t* p_full;     // [NST] softmax -> MMA  (128 arrivals)
+  uint64_t* o_full;     // [NST] MMA -> epilogue (last P.V of a tile done)
+  uint64_t* o_empty;    // [NST] epilogue -> MMA (128 arrivals)
+  uint64_t* st_full;    // [NST] softmax -> epilogue: row stats written (128 arrivals; two stages)
+  uint64_t* st_empty;   // [NST] epilogue -> softmax (128 arrivals; two stages)
   uint64_t* kv_full;    // [NSLOT]
   uint64_t* kv_empty;   // [NSLOT]
   uint64_t* teardown;   // [1]
@@ -201,7 +209,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
     ti.b = bh / p.H;
     ti.h = bh - ti.b * p.H;
     ti.hk = ti.h / p.kv_group;
-    ti.q0 = (causal ? (p.n_qblk - 1 - qi) : qi) * 256;
+    ti.q0 = (causal ? (p.n_qblk - 1 - qi) : qi) * C::kTileRows;
     ti.qrow0 = p.cu_q[ti.b];
     ti.krow0 = p.cu_k[ti.b];
     ti.len_q = p.cu_q[ti.b + 1] - ti.qrow0;
@@ -214,7 +222,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
       return ti;
     }
     int kv_end = ti.len_k;
-    if (causal) kv_end = min(kv_end, min(ti.q0 + 256, ti.len_q) + ti.coff);
+    if (causal) kv_end = min(kv_end, min(ti.q0 + C::kTileRows, ti.len_q) + ti.coff);
     const int n_tot = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
     ti.n_kv = n_tot > 0 ? n_tot : 1;  // rows that see no key take one masked tile
     return ti;
@@ -233,11 +241,11 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   ti.b = bh / p.H;
   ti.h = bh - ti.b * p.H;
   ti.hk = ti.h / p.kv_group;
-  ti.q0 = qb * 256;
+  ti.q0 = qb * C::kTileRows;
   ti.qrow0 = ti.krow0 = 0;
   ti.split = split;
   int kv_end = p.N_k;
-  if (p.causal != kNoCausal) kv_end = min(kv_end, min(ti.q0 + 256, p.N_q) + p.causal);
+  if (p.causal != kNoCausal) kv_end = min(kv_end, min(ti.q0 + C::kTileRows, p.N_q) + p.causal);
   // (bottom-right alignment with N_q > N_k: a tile may see no key at all)
   const int n_tot = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
   if constexpr (!C::kSplit) {
@@ -274,7 +282,7 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
   const uint64_t pol_kv = l2_policy_evict_last();
   uint32_t it = 0;          // ring entries handed out so far
   uint32_t withheld = ~0u;  // ring entry skipped by the test hook, if any
-  uint32_t q_armed0 = 0, q_armed1 = 0;
+  uint32_t q_armed[C::NST] = {};  // Q copies issued per stage
   bool ok = true;
   uint32_t tile_k = 0;
 
@@ -286,7 +294,7 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     for (int pn = 0; pn < C::kPanels; ++pn)
       tma_load_4d(tmQ, &bars.q_full[stage], dst + pn * C::kQPanelBytes, pn * C::kPanelElems,
                   ti.qrow0 + ti.q0 + stage * C::BM, ti.h, C::kVarlen ? 0 : ti.b, pol_q);
-    if (stage == 0) ++q_armed0; else ++q_armed1;
+    ++q_armed[stage];
     return true;
   };
   auto load_kv = [&](const CUtensorMap* map, int j, const TileInfo& ti, bool withhold) -> bool {
@@ -312,8 +320,11 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
     const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
-    ok = load_q(0, ti) && load_kv(tmK, 0, ti, false) && load_q(1, ti) &&
-         load_kv(tmV, 0, ti, false);
+    // Q_0, K_0 (the first S needs both), the other stages' Q, then V_0
+    ok = load_q(0, ti) && load_kv(tmK, 0, ti, false);
+#pragma unroll
+    for (int st = 1; st < C::NST; ++st) ok = ok && load_q(st, ti);
+    ok = ok && load_kv(tmV, 0, ti, false);
     for (int j = 1; ok && j < ti.n_kv; ++j)
       ok = load_kv(tmK, j, ti, inject && j == 1) && load_kv(tmV, j, ti, false);
   }
@@ -323,8 +334,9 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     const uint64_t limit = 100000000ull;  // 100 ms
     for (uint32_t i = it > C::NSLOT ? it - C::NSLOT : 0; i < it; ++i)
       if (i != withheld) mbar_drain(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, limit);
-    if (q_armed0) mbar_drain(&bars.q_full[0], (q_armed0 - 1) & 1u, limit);
-    if (q_armed1) mbar_drain(&bars.q_full[1], (q_armed1 - 1) & 1u, limit);
+#pragma unroll
+    for (int st = 0; st < C::NST; ++st)
+      if (q_armed[st]) mbar_drain(&bars.q_full[st], (q_armed[st] - 1) & 1u, limit);
   }
 }
 
@@ -390,7 +402,7 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
   const uint32_t q_addr0 = smem_u32(smem + C::kOffQ);
   const uint32_t kv_base = smem_u32(smem + C::kOffKV);
   uint32_t it = 0, tile_k = 0;
-  uint32_t p_par[2] = {0, 0};
+  uint32_t p_par[C::NST] = {};
   bool ok = true;
   auto kv_wait = [&](uint32_t i) -> bool {
     return warp_wait(&bars.kv_full[i % C::NSLOT], (i / C::NSLOT) & 1u, wd, 0x20);
@@ -404,16 +416,16 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     if (!counted) continue;
     const uint32_t par_k = tile_k & 1u;
     const int n = ti.n_kv;
-    // S_s(0) = Q_s K_0^T for both stages
+    // S_s(0) = Q_s K_0^T for every stage
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      if (!(ok = warp_wait(&bars.q_full[s], par_k, wd, 0x21 + s) && (s == 1 || kv_wait(it)))) break;
+    for (int s = 0; s < C::NST; ++s) {
+      if (!(ok = warp_wait(&bars.q_full[s], par_k, wd, 0x21 + s) && (s > 0 || kv_wait(it)))) break;
       tc_fence_after();
       if (elect_one()) {
         issue_qk<C>(tmem + C::col_s(s), q_addr0 + s * C::kQBytes, slot_addr(it));
         tc_commit(&bars.s_full[s]);
         if (n == 1) tc_commit(&bars.q_empty[s]);
-        if (s == 1) tc_commit(&bars.kv_empty[it % C::NSLOT]);
+        if (s == C::NST - 1) tc_commit(&bars.kv_empty[it % C::NSLOT]);
       }
       __syncwarp();
     }
@@ -427,21 +439,21 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
       const uint32_t v_addr = slot_addr(iv);
       const uint32_t k_addr = slot_addr(ik);
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        if (!(ok = warp_wait(&bars.p_full[s], p_par[s], wd, 0x23 + s))) break;
+      for (int s = 0; s < C::NST; ++s) {
+        if (!(ok = warp_wait(&bars.p_full[s], p_par[s], wd, 0x24 + s))) break;
         p_par[s] ^= 1u;
-        if (j == 1 && !(ok = warp_wait(&bars.o_empty[s], par_k ^ 1u, wd, 0x25 + s))) break;
+        if (j == 1 && !(ok = warp_wait(&bars.o_empty[s], par_k ^ 1u, wd, 0x27 + s))) break;
         tc_fence_after();
         if (elect_one()) {
           issue_pv<C>(tmem + C::col_o(s), tmem + C::col_s(s), v_addr, j > 1);
-          if (s == 1) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
+          if (s == C::NST - 1) tc_commit(&bars.kv_empty[iv % C::NSLOT]);
           if (last) {
             tc_commit(&bars.o_full[s]);
           } else {
             issue_qk<C>(tmem + C::col_s(s), q_addr0 + s * C::kQBytes, k_addr);
             tc_commit(&bars.s_full[s]);
             if (j == n - 1) tc_commit(&bars.q_empty[s]);
-            if (s == 1) tc_commit(&bars.kv_empty[ik % C::NSLOT]);
+            if (s == C::NST - 1) tc_commit(&bars.kv_empty[ik % C::NSLOT]);
           }
         }
         __syncwarp();
@@ -456,6 +468,61 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
     __syncwarp();
     mbar_drain(&bars.teardown[0], 0, 100000000ull);
   }
+}
+
+// ------------------------------------------------------- epilogue
+// Rows of stage s of tile ti, row `row` of this thread (TMEM lane): O / l
+// (O_s read from tensor memory, st.x = 1/l) and the LSE (st.y), then O_s is
+// handed back to the MMA warp (o_empty).
+template <class C>
+__device__ __forceinline__ void store_stage(const TcParams& p, const TileInfo& ti, int s, float2 st,
+                                            uint32_t tmem, uint32_t lane_base, int row, const Bars& bars) {
+  using T = typename C::Elem;
+  const int q = ti.q0 + s * C::BM + row;
+  // varlen: rows of this sequence only, stored at their packed index (the
+  // bound on the packed total also keeps bad offsets from writing out of range)
+  const int qo = ti.qrow0 + q;
+  const bool valid = C::kVarlen ? (q < ti.len_q && qo < p.N_q && ti.qrow0 >= 0) : q < p.N_q;
+  const int ob = C::kVarlen ? 0 : ti.b;
+  T* orow = reinterpret_cast<T*>(p.O) + ob * p.o_stride[0] + ti.h * p.o_stride[1] +
+            static_cast<long long>(qo) * p.o_stride[2];
+  // split-KV: this unit's normalised partial O (fp32) and LSE go to the
+  // workspace; the combine kernel merges the splits into O and LSE
+  constexpr bool partial = C::kSplit;
+  const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
+  const uint32_t tO = tmem + lane_base + C::col_o(s);
+  const int dv = C::kSplit ? C::D : p.dv;  // columns of O to store
+#pragma unroll 1
+  for (int c = 0; c < dv; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(tO + c, o);
+    tmem_ld_wait32(o);
+    if (partial && valid) {
+      float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * C::D + c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
+                             __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
+    } else if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (c + 8 * k >= dv) break;
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * st.x, __uint_as_float(o[8 * k + 1]) * st.x);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * st.x, __uint_as_float(o[8 * k + 3]) * st.x);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * st.x, __uint_as_float(o[8 * k + 5]) * st.x);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * st.x, __uint_as_float(o[8 * k + 7]) * st.x);
+        dst[k] = w;
+      }
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&bars.o_empty[s]);
+  if (partial && valid)
+    p.ws_lse[wrow] = st.y;
+  else if (valid && p.LSE)
+    p.LSE[ob * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(qo) * p.lse_stride[2]] = st.y;
 }
 
 // --------------------------------------------------------- softmax warpgroups
@@ -590,21 +657,30 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
       tc_fence_before();
       mbar_arrive(&bars.p_full[stage]);
     }
-    // hand the row statistics to the epilogue: 1/l and LSE (natural log)
-    if (!warp_wait(&bars.st_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x32 + stage)) return;
-    // (l_run = 0 only for a row that sees no key of the unit -- a split-KV
-    // unit, or bottom-right causal with N_q > N_k: then O = 0 and LSE = -inf)
+    // the row statistics: 1/l and LSE (natural log); l_run = 0 only for a row
+    // that sees no key of the unit -- a split-KV unit, or bottom-right causal
+    // with N_q > N_k: then O = 0 and LSE = -inf
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    stats[stage * C::BM + row] = make_float2(inv_l, (m_run + __log2f(l_run)) * kLn2);
-    mbar_arrive(&bars.st_full[stage]);
+    const float2 st = make_float2(inv_l, (m_run + __log2f(l_run)) * kLn2);
+    if constexpr (C::kOwnEpilogue) {
+      // three stages: this group writes its own rows once the last P.V is done
+      if (!warp_wait(&bars.o_full[stage], tile_k & 1u, wd, 0x40 + stage)) return;
+      tc_fence_after();
+      store_stage<C>(p, ti, stage, st, tmem, lane_base, row, bars);
+    } else {
+      // two stages: hand them to the epilogue warpgroup
+      if (!warp_wait(&bars.st_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x34 + stage)) return;
+      stats[stage * C::BM + row] = st;
+      mbar_arrive(&bars.st_full[stage]);
+    }
   }
 }
 
-// ------------------------------------------------------- epilogue warpgroup
+// The epilogue warpgroup (two stages): the row statistics come from the
+// softmax groups through shared memory.
 template <class C>
 __device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& bars,
                                  const float2* stats, const Watchdog& wd) {
-  using T = typename C::Elem;
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
@@ -616,57 +692,13 @@ __device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& b
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
 #pragma unroll 1
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NST; ++s) {
       if (!warp_wait(&bars.o_full[s], tile_k & 1u, wd, 0x40 + s)) return;
-      if (!warp_wait(&bars.st_full[s], tile_k & 1u, wd, 0x42 + s)) return;
+      if (!warp_wait(&bars.st_full[s], tile_k & 1u, wd, 0x43 + s)) return;
       tc_fence_after();
       const float2 st = stats[s * C::BM + row];
       mbar_arrive(&bars.st_empty[s]);
-      const int q = ti.q0 + s * C::BM + row;
-      // varlen: rows of this sequence only, stored at their packed index (the
-      // bound on the packed total also keeps bad offsets from writing out of range)
-      const int qo = ti.qrow0 + q;
-      const bool valid = C::kVarlen ? (q < ti.len_q && qo < p.N_q && ti.qrow0 >= 0) : q < p.N_q;
-      const int ob = C::kVarlen ? 0 : ti.b;
-      T* orow = reinterpret_cast<T*>(p.O) + ob * p.o_stride[0] + ti.h * p.o_stride[1] +
-                static_cast<long long>(qo) * p.o_stride[2];
-      // split-KV: this unit's normalised partial O (fp32) and LSE go to the
-      // workspace; the combine kernel merges the splits into O and LSE
-      constexpr bool partial = C::kSplit;
-      const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
-      const uint32_t tO = tmem + lane_base + C::col_o(s);
-      const int dv = C::kSplit ? C::D : p.dv;  // columns of O to store
-#pragma unroll 1
-      for (int c = 0; c < dv; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c, o);
-        tmem_ld_wait32(o);
-        if (partial && valid) {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * C::D + c);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(o[4 * k]) * st.x, __uint_as_float(o[4 * k + 1]) * st.x,
-                                 __uint_as_float(o[4 * k + 2]) * st.x, __uint_as_float(o[4 * k + 3]) * st.x);
-        } else if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (c + 8 * k >= dv) break;
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * st.x, __uint_as_float(o[8 * k + 1]) * st.x);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * st.x, __uint_as_float(o[8 * k + 3]) * st.x);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * st.x, __uint_as_float(o[8 * k + 5]) * st.x);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * st.x, __uint_as_float(o[8 * k + 7]) * st.x);
-            dst[k] = w;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bars.o_empty[s]);
-      if (partial && valid)
-        p.ws_lse[wrow] = st.y;
-      else if (valid && p.LSE)
-        p.LSE[ob * p.lse_stride[0] + ti.h * p.lse_stride[1] + static_cast<long long>(qo) * p.lse_stride[2]] = st.y;
+      store_stage<C>(p, ti, s, st, tmem, lane_base, row, bars);
     }
   }
 }
@@ -680,17 +712,18 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   Bars bars;
-  bars.q_full = bar + 0;
-  bars.q_empty = bar + 2;
-  bars.s_full = bar + 4;
-  bars.p_full = bar + 6;
-  bars.o_full = bar + 8;
-  bars.o_empty = bar + 10;
-  bars.st_full = bar + 12;
-  bars.st_empty = bar + 14;
-  bars.kv_full = bar + 16;
-  bars.kv_empty = bar + 16 + C::NSLOT;
-  bars.teardown = bar + 16 + 2 * C::NSLOT;
+  constexpr int S = C::NST;
+  bars.q_full = bar + 0 * S;
+  bars.q_empty = bar + 1 * S;
+  bars.s_full = bar + 2 * S;
+  bars.p_full = bar + 3 * S;
+  bars.o_full = bar + 4 * S;
+  bars.o_empty = bar + 5 * S;
+  bars.st_full = bar + 6 * S;
+  bars.st_empty = bar + 7 * S;
+  bars.kv_full = bar + 8 * S;
+  bars.kv_empty = bar + 8 * S + C::NSLOT;
+  bars.teardown = bar + 8 * S + 2 * C::NSLOT;
   float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -698,7 +731,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
@@ -736,9 +769,11 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     setmaxnreg_dec<C::kRegProducer>();
     if (warp == 12 && lane == 0) tc_load_role<C>(&tmQ, &tmK, &tmV, p, smem, bars, wd);
     if (warp == 13) tc_mma_role<C>(p, smem, tmem, bars, wd);
-  } else if (wg == 2) {
-    setmaxnreg_dec<C::kRegEpilogue>();
-    tc_epilogue_role<C>(p, tmem, bars, stats, wd);
+  } else if (wg == 2 && !C::kOwnEpilogue) {
+    if constexpr (!C::kOwnEpilogue) {
+      setmaxnreg_dec<C::kRegEpilogue>();
+      tc_epilogue_role<C>(p, tmem, bars, stats, wd);
+    }
   } else {
     setmaxnreg_inc<C::kRegSoftmax>();
     tc_softmax_role<C>(p, wg, tmem, bars, stats, wd);

@@ -8,7 +8,7 @@
 namespace fa {
 
 using CfgBf16D128Split = TcCfg<__nv_bfloat16, 128, 128, 4, true>;
-using CfgBf16D64Split = TcCfg<__nv_bfloat16, 64, 128, 6, true>;
+using CfgBf16D64Split = TcCfg<__nv_bfloat16, 64, 96, 10, true, false, 3>;
 static_assert(tc_geometry_ok<CfgBf16D128Split, false>() && tc_geometry_ok<CfgBf16D64Split, false>(), "geometry");
 
 cudaError_t launch_tc_bf16_d128_split(const TcLaunch& L) { return launch_tc<CfgBf16D128Split>(L); }

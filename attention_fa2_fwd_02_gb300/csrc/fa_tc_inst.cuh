@@ -60,7 +60,8 @@ static cudaError_t launch_tc_wide(const TcLaunch& L) {
 // boxes from tc_key_tile / tc_box_inner).
 template <class C, bool FP32>
 constexpr bool tc_geometry_ok() {
-  return C::BN == tc_key_tile(FP32, C::D) && C::kPanelElems == tc_box_inner(FP32);
+  return C::BN == tc_key_tile(C::NST) && C::kTileRows == tc_tile_rows(C::NST) &&
+         C::kPanelElems == tc_box_inner(FP32);
 }
 
 }  // namespace fa

@@ -130,6 +130,10 @@ WORKLOADS = {
     "large_d96_nc": _w("large_d96_nc", 4, 32, 8192, 8192, 96, torch.bfloat16, False, seed=10),
     "large_d96_causal": _w("large_d96_causal", 4, 32, 8192, 8192, 96, torch.bfloat16, True, seed=10),
     "large_dv64_nc": _w("large_dv64_nc", 4, 32, 8192, 8192, 128, torch.bfloat16, False, seed=11, Dv=64),
+    # head dim 64 at the large shape ("Blackwell Attention Example", main():
+    # (4, 32, 8192, 64) bf16)
+    "large_d64_nc": _w("large_d64_nc", 4, 32, 8192, 8192, 64, torch.bfloat16, False, seed=14),
+    "large_d64_causal": _w("large_d64_causal", 4, 32, 8192, 8192, 64, torch.bfloat16, True, seed=14),
     # head dim 256 (the single-stage kernel for head dims above 128)
     "large_d256_nc": _w("large_d256_nc", 4, 32, 8192, 8192, 256, torch.bfloat16, False, seed=12),
     "large_d256_causal": _w("large_d256_causal", 4, 32, 8192, 8192, 256, torch.bfloat16, True, seed=12),

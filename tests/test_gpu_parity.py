@@ -240,7 +240,8 @@ def sampled_rows(w, n_random=192, seed=7):
     return out
 
 
-@pytest.mark.parametrize("name", ["large_nc", "large_causal", "cross_long_nc", "long_causal"])
+@pytest.mark.parametrize("name", ["large_nc", "large_causal", "cross_long_nc", "long_causal", "large_d64_nc",
+                                  "large_d64_causal"])
 def test_config_large_sampled(oracle_mod, name):
     """Full-size configurations in the launch configuration the benchmark times,
     checked on sampled rows against the oracle, plus properties on every row."""

@@ -24,7 +24,7 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L) {
   fa_bwd_pre_kernel<__nv_bfloat16, D><<<(unsigned)((pre_rows + 7) / 8), 256, 0, L.stream>>>(L.pre);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmdO, L.p);
+  fa_bwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmdO, L.p, L.tmDq);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long post_rows = static_cast<long long>(L.post.B) * L.post.H * L.post.N_q;
   fa_bwd_post_kernel<__nv_bfloat16, D><<<(unsigned)((post_rows + 7) / 8), 256, 0, L.stream>>>(L.post);

@@ -82,7 +82,13 @@ struct BwdCfg {
   static constexpr uint32_t kOffdO = kOffQ + NST * kQTileBytes;    // [NST]
   static constexpr uint32_t kOffdS = kOffdO + NST * kQTileBytes;   // dS^T [keys][queries]
   static constexpr uint32_t kOffVec = kOffdS + BN * BM * 2;        // [NST] -lse2[BM], delta[BM]
-  static constexpr uint32_t kOffBar = kOffVec + NST * 2 * BM * 4;
+  // d = 128 (dQ^T, lanes = head dims): the epilogue hands each step's dQ to
+  // the TMA engine as fp32 reduce-adds; per epilogue warp two 8 KB buffers of
+  // BM queries x its 32 head dims
+  static constexpr bool kDqTma = kDqT;
+  static constexpr uint32_t kDqStageBytes = BM * 32 * 4;
+  static constexpr uint32_t kOffDqStage = (kOffVec + NST * 2 * BM * 4 + 1023) / 1024 * 1024;
+  static constexpr uint32_t kOffBar = kOffDqStage + (kDqTma ? 4 * 2 * kDqStageBytes : 0);
   static constexpr int kNumBars = 11 + 2 * NST;  // + teardown
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
@@ -506,12 +512,16 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
 }
 
 template <class C>
-__device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBars& bars, const Watchdog& wd) {
+__device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, uint8_t* smem, uint32_t tmem,
+                                  const BwdBars& bars, const Watchdog& wd) {
   const int wq = (threadIdx.x / 32) & 3;
   const int lane = threadIdx.x & 31;
   const int r = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  uint8_t* dq_stage = smem + C::kOffDqStage + wq * 2 * C::kDqStageBytes;  // this warp's two buffers
+  uint32_t n_red = 0;                                                     // reductions issued
   uint32_t ku = 0, gs = 0;
+  auto run = [&]() {
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const BwdUnit w = bwd_unit<C>(p, u);
     const int key = w.j * C::BN + r;
@@ -541,7 +551,28 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
       reg_fence32(v + 32);
       tc_fence_before();
       mbar_arrive(&bars.dq_empty[qb]);  // the values are in registers now
-      if constexpr (C::kDqT) {
+      if constexpr (C::kDqTma) {
+        // lane r = head-dim index, columns = the step's 64 queries: the warp's
+        // 64 x 32 block goes through its shared-memory buffer (row = query,
+        // 32 consecutive head dims: every store instruction covers one
+        // 128-byte row) and one lane adds it into the accumulator with a TMA
+        // reduction
+        float* buf = reinterpret_cast<float*>(dq_stage + (n_red & 1u) * C::kDqStageBytes);
+        if (n_red >= 2) {  // the reduction that last read this buffer
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) buf[c * 32 + lane] = __uint_as_float(v[c]);
+        fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(tmDq, buf, wq * 32, q0, static_cast<int>(t.bh));
+          bulk_commit();
+        }
+        ++n_red;
+        (void)acc;
+      } else if constexpr (C::kDqT) {
         // lane r = head-dim index, columns = the step's 64 queries: a warp's
         // reductions hit 32 consecutive floats of one query row
 #pragma unroll
@@ -585,13 +616,22 @@ __device__ void bwd_epilogue_role(const BwdParams& p, uint32_t tmem, const BwdBa
     mbar_arrive(&bars.dkv_empty[0]);
     ++ku;
   }
+  };
+  run();
+  // the reductions must have read their buffers (and landed) before the
+  // CTA's shared memory goes away and before the dQ conversion reads the
+  // accumulator, on every exit path
+  if constexpr (C::kDqTma) {
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
 }
 
 template <class C>
 __global__ void __launch_bounds__(512, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-              const __grid_constant__ BwdParams p) {
+              const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tmDq) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -635,6 +675,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmdO);
+    if (C::kDqTma) prefetch_tensormap(&tmDq);
   }
   if (warp == 13) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -654,7 +695,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     bwd_compute_role<C>(p, smem, tmem, bars, wd, warp / 4);
   } else if (warp < 12) {
     setmaxnreg_dec<kRegEpilogue>();
-    bwd_epilogue_role<C>(p, tmem, bars, wd);
+    bwd_epilogue_role<C>(&tmDq, p, smem, tmem, bars, wd);
   } else {
     setmaxnreg_dec<kRegProducer>();
     if (warp == 12) {

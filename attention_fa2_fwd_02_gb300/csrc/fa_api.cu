@@ -519,17 +519,18 @@ fa_status_t run_problems(fa_dtype_t dtype, int n, const fa_problem_t* problems, 
 }
 
 // The backward's fp32 dQ accumulator [BH][N_qp][D] as a 3-D tensor map for
-// TMA reductions: boxes of 32 head dims x 64 query rows, no swizzle.
+// TMA reductions: boxes of 32 head dims x 64 query rows, unswizzled (D = 128),
+// or 32 head dims x 32 query rows, 128-byte swizzle (D = 64).
 fa_status_t make_dq_map(CUtensorMap* map, float* acc, long long BH, long long N_qp, long long D) {
   auto enc = encode_fn();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N_qp, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)(D * 4), (cuuint64_t)(N_qp * D * 4)};
-  cuuint32_t box[3] = {32, 64, 1};
+  cuuint32_t box[3] = {32, D == 128 ? 64u : 32u, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, acc, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, D == 128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(FA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the dQ accumulator (CUresult " +
                                         std::to_string((int)r) + ")");
@@ -806,7 +807,7 @@ fa_status_t fa_bwd_dv(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, int6
   if ((st = make_map(&L.tmK, *K, false, B, H_kv, N_k, (int)d, 128, "K")) != FA_OK) return st;
   if ((st = make_map(&L.tmV, *V, false, B, H_kv, N_k, (int)d_v, 128, "V")) != FA_OK) return st;
   const int N_qp = (int)((N_q + 127) / 128 * 128);  // workspace row pitch
-  if (D == 128 && (st = make_dq_map(&L.tmDq, ws.dq_acc, B * H, N_qp, D)) != FA_OK) return st;
+  if ((st = make_dq_map(&L.tmDq, ws.dq_acc, B * H, N_qp, D)) != FA_OK) return st;
   BwdParams& p = L.p;
   p.B = (int)B;
   p.H = (int)H;

@@ -19,8 +19,11 @@
 //    compute warpgroups (each a half of the query columns), then
 //    dV += P^T dO_i and dK += dS^T Q_i (A in tensor memory) and the step's dQ
 //    contribution from dS^T staged in shared memory; dQ goes to one of two
-//    tensor-memory buffers, so that its read-out (fp32 reductions into the
-//    accumulator) overlaps the following steps;
+//    tensor-memory buffers, so that its read-out overlaps the following
+//    steps: the epilogue warps stage it in shared memory and add it into the
+//    fp32 accumulator with TMA reductions (cp.reduce.async.bulk.tensor), one
+//    per warp and 8 KB block -- per-element global reductions cost 6 % (d =
+//    128) and 27 % (d = 64) of the whole backward;
 //  * fa_bwd_post_kernel: dQ = scale * accumulator in the output dtype.
 //
 // The dQ product: d = 128 uses 64-row query steps and computes dQ_i^T =
@@ -82,13 +85,16 @@ struct BwdCfg {
   static constexpr uint32_t kOffdO = kOffQ + NST * kQTileBytes;    // [NST]
   static constexpr uint32_t kOffdS = kOffdO + NST * kQTileBytes;   // dS^T [keys][queries]
   static constexpr uint32_t kOffVec = kOffdS + BN * BM * 2;        // [NST] -lse2[BM], delta[BM]
-  // d = 128 (dQ^T, lanes = head dims): the epilogue hands each step's dQ to
-  // the TMA engine as fp32 reduce-adds; per epilogue warp two 8 KB buffers of
-  // BM queries x its 32 head dims
-  static constexpr bool kDqTma = kDqT;
-  static constexpr uint32_t kDqStageBytes = BM * 32 * 4;
+  // The epilogue hands each step's dQ to the TMA engine as fp32 reduce-adds,
+  // through two 8 KB buffers per epilogue warp: d = 128 (dQ^T, lanes = head
+  // dims) 64 queries x the warp's 32 head dims, unswizzled; d = 64 (lanes =
+  // queries) the warp's 32 queries x 64 head dims, as two 128-byte-swizzled
+  // 32 x 32 halves
+  static constexpr uint32_t kDqStageBytes = 8192;
+  static_assert(BM * 32 * 4 == kDqStageBytes || !kDqT, "d = 128 buffer: BM queries x 32 head dims");
+  static_assert(32 * D * 4 == kDqStageBytes || kDqT, "d = 64 buffer: 32 queries x 64 head dims");
   static constexpr uint32_t kOffDqStage = (kOffVec + NST * 2 * BM * 4 + 1023) / 1024 * 1024;
-  static constexpr uint32_t kOffBar = kOffDqStage + (kDqTma ? 4 * 2 * kDqStageBytes : 0);
+  static constexpr uint32_t kOffBar = kOffDqStage + 4 * 2 * kDqStageBytes;
   static constexpr int kNumBars = 11 + 2 * NST;  // + teardown
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
@@ -169,11 +175,6 @@ __device__ __forceinline__ BwdStep bwd_step(const BwdParams& p, const BwdUnit& w
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-               ::"l"(dst), "f"(__uint_as_float(a)), "f"(__uint_as_float(b)), "f"(__uint_as_float(c)),
-                 "f"(__uint_as_float(d)) : "memory");
 }
 
 // ------------------------------------------------------------- pre / post
@@ -266,9 +267,6 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
-}
-__device__ __forceinline__ void red_add_f32(float* dst, uint32_t v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(__uint_as_float(v)) : "memory");
 }
 
 template <class C>
@@ -539,7 +537,6 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
     }
     for (int s = 0; s < w.n_steps; ++s, ++gs) {
       const BwdStep t = bwd_step(p, w, s);
-      float* acc = p.dq_acc + t.bh * p.N_qp * C::D;
       const uint32_t qb = gs & 1u;
       const int q0 = t.i * C::BM;
       if (!bwd_warp_wait(&bars.dq_full[qb], (gs >> 1) & 1u, wd, 0x68)) return;
@@ -551,7 +548,32 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
       reg_fence32(v + 32);
       tc_fence_before();
       mbar_arrive(&bars.dq_empty[qb]);  // the values are in registers now
-      if constexpr (C::kDqTma) {
+      if constexpr (!C::kDqT) {
+        // lane r = query row of the step, columns = the 64 head dims: the
+        // warp's 32 x 64 block in two 32 x 32 halves, each row a 128-byte
+        // swizzle row (16-byte chunk i at i ^ (row mod 8): conflict-free
+        // quarter-warps), and one lane adds them with two TMA reductions
+        uint8_t* buf = dq_stage + (n_red & 1u) * C::kDqStageBytes;
+        if (n_red >= 2) {  // the reductions that last read this buffer
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(buf + h * 4096 + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(v[32 * h + 4 * i]), __uint_as_float(v[32 * h + 4 * i + 1]),
+                            __uint_as_float(v[32 * h + 4 * i + 2]), __uint_as_float(v[32 * h + 4 * i + 3]));
+        fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(tmDq, buf, 0, q0 + wq * 32, static_cast<int>(t.bh));
+          tma_reduce_add_3d(tmDq, buf + 4096, 32, q0 + wq * 32, static_cast<int>(t.bh));
+          bulk_commit();
+        }
+        ++n_red;
+      } else {
         // lane r = head-dim index, columns = the step's 64 queries: the warp's
         // 64 x 32 block goes through its shared-memory buffer (row = query,
         // 32 consecutive head dims: every store instruction covers one
@@ -571,17 +593,6 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
           bulk_commit();
         }
         ++n_red;
-        (void)acc;
-      } else if constexpr (C::kDqT) {
-        // lane r = head-dim index, columns = the step's 64 queries: a warp's
-        // reductions hit 32 consecutive floats of one query row
-#pragma unroll
-        for (int c = 0; c < 64; ++c) red_add_f32(acc + static_cast<long long>(q0 + c) * C::D + r, v[c]);
-      } else {
-        // lane r = query row of the step, columns = the 64 head-dim values
-        float* dst = acc + static_cast<long long>(q0 + r) * C::D;
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) red_add_v4(dst + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
       }
     }
     if (!bwd_warp_wait(&bars.dkv_full[0], ku & 1u, wd, 0x69)) return;
@@ -621,10 +632,8 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
   // the reductions must have read their buffers (and landed) before the
   // CTA's shared memory goes away and before the dQ conversion reads the
   // accumulator, on every exit path
-  if constexpr (C::kDqTma) {
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
-  }
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
 }
 
 template <class C>
@@ -675,7 +684,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmdO);
-    if (C::kDqTma) prefetch_tensormap(&tmDq);
+    prefetch_tensormap(&tmDq);
   }
   if (warp == 13) {
     tmem_alloc(tmem_slot, C::kTmemCols);

@@ -56,7 +56,7 @@ constexpr int kWideKeyTile = 128;
 // conversion on one stream.  bf16 only; d = 64 or 128.
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO;
-  CUtensorMap tmDq;  // the fp32 dQ accumulator [B*H][N_qp][d] (TMA reductions, head dim 128)
+  CUtensorMap tmDq;  // the fp32 dQ accumulator [B*H][N_qp][d] (TMA reductions)
   BwdParams p;
   BwdPreParams pre;
   BwdPostParams post;

@@ -24,8 +24,10 @@
 #include "fa_vt.cuh"
 
 namespace fa {
-// Raised (atomicOr) by any kernel of this library whose bounded wait expires.
-__device__ unsigned int g_err_word;
+// [0]: raised (atomicOr) by any kernel of this library whose bounded wait
+// expires.  [1 + 2 s], [2 + 2 s]: the work-unit counters of packed-batch
+// launches (scheduler slot s: units taken, CTAs done; zero between launches).
+__device__ unsigned int g_err_word[1 + 2 * kSchedSlots];
 }  // namespace fa
 
 namespace {
@@ -45,6 +47,7 @@ std::string cuda_msg(const char* what, cudaError_t e) {
 
 std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
 std::atomic<int> g_debug_flags{0};
+std::atomic<unsigned int> g_sched_next{0};  // next scheduler slot of a packed-batch launch
 
 struct DevState {
   bool ready = false;
@@ -931,9 +934,11 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   p.causal = is_causal == 0 ? kNoCausal : (is_causal == 2 ? kVarlenBottomRight : 0);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.n_qblk = (int)n_qblk;
-  p.n_tiles = (int)(B * H * n_qblk);
   p.dv = dv;
-  p.n_units = p.n_tiles;
+  p.n_units = (int)(B * H * n_qblk);
+  // this launch's work-unit counters: slots taken round robin, so that up to
+  // kSchedSlots packed-batch launches may be in flight at once
+  p.sched_slot = static_cast<int>(g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
   // Heads per schedule group, as for the batched tiles: keep the K/V of a

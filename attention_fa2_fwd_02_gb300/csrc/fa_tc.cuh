@@ -42,6 +42,14 @@ constexpr int kNoCausal = 0x7fffffff;
 // packed variable-length batches: bottom-right alignment per sequence (its
 // offset len_k - len_q differs between sequences)
 constexpr int kVarlenBottomRight = 0x7ffffffe;
+// Packed batches hand out their work units at run time: each launch owns a
+// pair of counters next to the device error word (units taken, CTAs done),
+// picked round robin among kSchedSlots, and the load warp passes the units
+// it takes to the other roles through a kSchedDepth-deep queue in shared
+// memory.  The last CTA to finish zeroes its pair for the next launch.
+constexpr int kSchedSlots = 64;
+constexpr int kSchedDepth = 4;
+constexpr int kSchedConsumers = 13;  // arrivals that free a queue entry: MMA warp, 2 x 4 softmax warps, 4 epilogue warps
 
 struct TcParams {
   int B, H, N_q, N_k;
@@ -49,7 +57,10 @@ struct TcParams {
                           // (0: top-left alignment, N_k - N_q: bottom-right)
   float scale_log2;       // scale * log2(e)
   int n_qblk;             // ceil(N_q / tile rows): 256 (two-stage kernel), 384 (three stages), 128 (single-stage)
-  int n_tiles;            // B * H * n_qblk
+  union {
+    int n_tiles;          // B * H * n_qblk (host bookkeeping; no kernel reads it)
+    int sched_slot;       // varlen: this launch's scheduler counters, err[1 + 2 slot] and err[2 + 2 slot]
+  };
   union {
     int n_split;          // split-KV instantiations: key-range splits per tile
     int dv;               // the others: output columns written (V's head dim, <= D; the
@@ -118,7 +129,10 @@ struct TcCfg {
   static constexpr int kNumBars = 8 * NST + 2 * NSLOT + 1;
   static constexpr uint32_t kOffStats = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMisc = kOffStats + NST * BM * 8;
-  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
+  // varlen: the unit queue (kSchedDepth ints, then full and empty barriers)
+  static constexpr uint32_t kOffSched = kOffMisc + 16;
+  static constexpr uint32_t kSchedBytes = VARLEN_ ? 16 + 2 * kSchedDepth * 8 : 0;
+  static constexpr uint32_t kSmemBytes = kOffSched + kSchedBytes + 1024;  // + base alignment slack
   static constexpr uint32_t kIdescS = make_idesc(kTF32 ? 2u : 1u, 128, BN, 0, 0);
   static constexpr uint32_t kIdescO = make_idesc(kTF32 ? 2u : 1u, 128, D, 0, 1);
   static constexpr int kThreads = 512;
@@ -153,6 +167,10 @@ struct Bars {            // [NST]: one per query stage
   uint64_t* kv_full;    // [NSLOT]
   uint64_t* kv_empty;   // [NSLOT]
   uint64_t* teardown;   // [1]
+  // varlen: the unit queue (UnitSource)
+  volatile int* sq_unit;  // [kSchedDepth]
+  uint64_t* sq_full;      // [kSchedDepth] load warp -> roles (1 arrival)
+  uint64_t* sq_empty;     // [kSchedDepth] roles -> load warp (kSchedConsumers arrivals)
 };
 
 struct TileInfo {
@@ -274,6 +292,46 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// The CTA's work units.  Batched problems: u = blockIdx.x, then every
+// gridDim.x-th unit.  Packed batches: the units the load warp takes from the
+// launch's counter, in the order it takes them -- the load warp (kProducer)
+// pushes each into the queue, every other role pops them in the same order.
+// A unit >= n_units ends the sequence; so does an expired wait (the watchdog
+// has recorded it and the other roles' waits then give up too).
+template <class C, bool kProducer>
+struct UnitSource {
+  const TcParams& p;
+  const Bars& q;
+  const Watchdog& wd;
+  uint32_t k = 0;  // units taken so far
+  __device__ __forceinline__ int first() {
+    if constexpr (!C::kVarlen) return blockIdx.x;
+    else return take();
+  }
+  __device__ __forceinline__ int next(int u) {
+    if constexpr (!C::kVarlen) return u + gridDim.x;
+    else return take();
+  }
+  __device__ __forceinline__ int take() {
+    const uint32_t e = k % kSchedDepth, par = (k / kSchedDepth) & 1u;
+    ++k;
+    if constexpr (kProducer) {  // one thread
+      if (!mbar_wait(&q.sq_empty[e], par ^ 1u, wd, 0x18)) return p.n_units;
+      unsigned int* ctr = p.err + 1 + 2 * p.sched_slot;
+      const int u = min(static_cast<int>(atomicAdd(ctr, 1u)), p.n_units);
+      q.sq_unit[e] = u;
+      mbar_arrive(&q.sq_full[e]);  // (release: the unit is visible to the roles that wait on it)
+      return u;
+    } else {  // whole warps
+      if (!warp_wait(&q.sq_full[e], par, wd, 0x19)) return p.n_units;
+      const int u = q.sq_unit[e];
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&q.sq_empty[e]);
+      return u;
+    }
+  }
+};
+
 // ------------------------------------------------------------- load warp
 template <class C>
 __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
@@ -315,7 +373,8 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
   };
 
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, tile_k += counted) {
+  UnitSource<C, true> src{p, bars, wd};
+  for (int u = src.first(); ok && u < p.n_units; u = src.next(u), tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
@@ -410,7 +469,8 @@ __device__ void tc_mma_role(const TcParams& p, uint8_t* smem, uint32_t tmem, con
   auto slot_addr = [&](uint32_t i) -> uint32_t { return kv_base + (i % C::NSLOT) * C::kKVBytes; };
 
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, tile_k += counted) {
+  UnitSource<C, false> src{p, bars, wd};
+  for (int u = src.first(); ok && u < p.n_units; u = src.next(u), tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
@@ -539,7 +599,8 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
   uint32_t s_par = 0, tile_k = 0;
 
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
+  UnitSource<C, false> src{p, bars, wd};
+  for (int u = src.first(); u < p.n_units; u = src.next(u), tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
@@ -687,7 +748,8 @@ __device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& b
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   uint32_t tile_k = 0;
   uint32_t counted = 0;  // empty work units (split-KV) take no pipeline phase
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, tile_k += counted) {
+  UnitSource<C, false> src{p, bars, wd};
+  for (int u = src.first(); u < p.n_units; u = src.next(u), tile_k += counted) {
     const TileInfo ti = tile_info<C>(p, u);
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
@@ -724,6 +786,9 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   bars.kv_full = bar + 8 * S;
   bars.kv_empty = bar + 8 * S + C::NSLOT;
   bars.teardown = bar + 8 * S + 2 * C::NSLOT;
+  bars.sq_unit = reinterpret_cast<volatile int*>(smem + C::kOffSched);
+  bars.sq_full = reinterpret_cast<uint64_t*>(smem + C::kOffSched + 16);
+  bars.sq_empty = bars.sq_full + kSchedDepth;
   float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -746,6 +811,11 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.teardown[0], 1);
+    if constexpr (C::kVarlen)
+      for (int e = 0; e < kSchedDepth; ++e) {
+        mbar_init(&bars.sq_full[e], 1);
+        mbar_init(&bars.sq_empty[e], kSchedConsumers);
+      }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -783,6 +853,18 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if constexpr (C::kVarlen) {
+    // every role of this CTA is done with the launch's counters; the last
+    // CTA to get here zeroes them for the next launch that takes this slot
+    if (threadIdx.x == 0) {
+      unsigned int* ctr = p.err + 1 + 2 * p.sched_slot;
+      __threadfence();
+      if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+        atomicExch(ctr, 0u);
+        atomicExch(ctr + 1, 0u);
+      }
+    }
   }
 }
 

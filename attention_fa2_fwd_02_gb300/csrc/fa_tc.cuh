@@ -378,7 +378,7 @@ __device__ void tc_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     const TileInfo ti = tile_info<C>(p, u);
     counted = (C::kSplit || C::kVarlen) ? (ti.n_kv != 0) : 1u;
     if (!counted) continue;
-    const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
+    const bool inject = (p.debug_flags & 1) && u == 0;  // test hook: work unit 0 withholds its second K tile
     // Q_0, K_0 (the first S needs both), the other stages' Q, then V_0
     ok = load_q(0, ti) && load_kv(tmK, 0, ti, false);
 #pragma unroll

@@ -270,8 +270,9 @@ __device__ void wide_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
     const TileInfo ti = wide_tile_info<C>(p, u);
     if (!wide_counted<C>(ti)) continue;
-    // test hook (host-set flag): block 0 never delivers the second K tile of its first tile
-    const bool inject = (p.debug_flags & 1) && blockIdx.x == 0 && tile_k == 0;
+    // test hook (host-set flag): the second K tile of work unit 0 (the first
+    // tile of block 0; the longest tile under a causal mask) is never delivered
+    const bool inject = (p.debug_flags & 1) && u == 0;
     if constexpr (C::kQTmem) {
       // Q into the next ring slot; its bytes complete on q_full, kv_full[slot] gets a plain arrival
       const uint32_t slot = it % C::NSLOT;

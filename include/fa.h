@@ -400,9 +400,10 @@ const char* fa_last_error(void);
 /*
  * Test hooks (process-wide; not for production use).
  *   timeout_ns   limit of every device-side pipeline wait (0 = default, 1 s).
- *   debug_flags  bit 0: the tensor-core kernel's load warp withholds one K/V
- *                tile in block 0, so the consumer's bounded wait runs out and
- *                the launch ends with FA_ERR_TIMEOUT instead of a hang.
+ *   debug_flags  bit 0: the load warp of the forward kernels withholds one K
+ *                tile (the second of work unit 0) and the backward's one
+ *                Q/dO step of block 0, so the consumer's bounded wait runs
+ *                out and the launch ends with FA_ERR_TIMEOUT instead of a hang.
  */
 void fa_debug_set(uint64_t timeout_ns, int debug_flags);
 

@@ -146,3 +146,47 @@ def test_varlen_rejects_bad_arguments():
         fa.fwd_varlen(qd, kd, vd, cq, ck, 31)                 # max_seqlen_q above total_q
     with pytest.raises(fa.FaError):
         fa.fwd_varlen(qd.float(), kd.float(), vd.float(), cq, ck, 20)  # bf16 only
+
+
+def test_varlen_concurrent_streams_and_back_to_back(oracle_mod):
+    """Packed batches take their work units from per-launch counters (one of
+    64 slots, round robin, zeroed by each launch's last CTA): launches in
+    flight at once on four streams, and many back to back on one stream, must
+    each cover every unit exactly once -- every output equals the one-launch
+    result bit for bit, and that one matches the oracle."""
+    cases = []
+    for i, (lens, causal) in enumerate((([300, 700, 129, 1000], False), ([513, 64, 900], True),
+                                        ([1, 256, 257, 640], "bottom_right"), ([1200, 90], False))):
+        q, k, v, cu_q, cu_k = packed(lens, lens, 4, 2, 128, seed=7100 + i)
+        cases.append((q.cuda(), k.cuda(), v.cuda(), cu_q.cuda(), cu_k.cuda(), max(lens), causal))
+    refs = []
+    for q, k, v, cq, ck, ml, causal in cases:
+        O, L = fa.fwd_varlen(q, k, v, cq, ck, ml, is_causal=causal)
+        fa.check()
+        refs.append((O.clone(), L.clone()))
+    # the first case against the oracle as well
+    q, k, v, cq, ck, ml, causal = cases[0]
+    kx = k.float().repeat_interleave(2, dim=1).cpu().numpy()
+    vx = v.float().repeat_interleave(2, dim=1).cpu().numpy()
+    O_ref, L_ref = oracle_mod.attention_varlen(q.float().cpu().numpy(), kx, vx, cq.cpu().numpy(), ck.cpu().numpy(),
+                                               1 / math.sqrt(128), fa.causal_code(causal))
+    assert float(np.abs(refs[0][0].float().cpu().numpy() - O_ref).max()) <= TOL_O
+    # four streams at once, several rounds
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = [[None] * len(cases) for _ in range(3)]
+    torch.cuda.synchronize()
+    for r in range(3):
+        for c, (q, k, v, cq, ck, ml, causal) in enumerate(cases):
+            with torch.cuda.stream(streams[c]):
+                outs[r][c] = fa.fwd_varlen(q, k, v, cq, ck, ml, is_causal=causal, stream=streams[c])
+    torch.cuda.synchronize()
+    fa.check()
+    for r in range(3):
+        for c in range(len(cases)):
+            assert torch.equal(outs[r][c][0], refs[c][0]) and torch.equal(outs[r][c][1], refs[c][1]), (r, c)
+    # 100 launches back to back on one stream (every slot taken and reset more than once)
+    q, k, v, cq, ck, ml, causal = cases[1]
+    for _ in range(100):
+        O, L = fa.fwd_varlen(q, k, v, cq, ck, ml, is_causal=causal)
+    fa.check()
+    assert torch.equal(O, refs[1][0]) and torch.equal(L, refs[1][1])

@@ -314,6 +314,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 // max(a, b, c) in one instruction (three-input form of max.f32).
+// A compile-time flag passed by value: a generic lambda instantiated for
+// both values lets a warp-uniform branch pick between two specialised copies
+// of a loop (the predicated form of a per-element condition costs an integer
+// compare and a select on every element even when it never fires).
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

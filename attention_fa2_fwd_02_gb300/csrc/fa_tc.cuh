@@ -687,27 +687,33 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
       float2 sum2[kAcc / 2];
 #pragma unroll
       for (int a = 0; a < kAcc / 2; ++a) sum2[a] = make_float2(0.f, 0.f);
+      auto exp_tile = [&](auto masked) {
 #pragma unroll
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
-        float e[32];
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          float e[32];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int c = c0 + k;
-          const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
-          float v0 = ex2(x.x), v1 = ex2(x.y);
-          if (need_mask) {
-            if (c >= lim) v0 = 0.f;
-            if (c + 1 >= lim) v1 = 0.f;
+          for (int k = 0; k < 32; k += 2) {
+            const int c = c0 + k;
+            const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+            float v0 = ex2(x.x), v1 = ex2(x.y);
+            if constexpr (decltype(masked)::value) {
+              if (c >= lim) v0 = 0.f;
+              if (c + 1 >= lim) v1 = 0.f;
+            }
+            e[k] = v0;
+            e[k + 1] = v1;
+            sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
           }
-          e[k] = v0;
-          e[k + 1] = v1;
-          sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
-        }
-        uint32_t pw[16];
+          uint32_t pw[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
-        tmem_st16(tS + c0 / 2, pw);
-      }
+          for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
+          tmem_st16(tS + c0 / 2, pw);
+        }
+      };
+      if (need_mask)
+        exp_tile(BoolC<true>{});
+      else
+        exp_tile(BoolC<false>{});
 #pragma unroll
       for (int w = kAcc / 4; w > 0; w /= 2)
 #pragma unroll

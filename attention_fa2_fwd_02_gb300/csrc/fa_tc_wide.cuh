@@ -604,10 +604,16 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
       if (sc >= 0.f) {
 #pragma unroll
         for (int a = 0; a < kAcc; ++a) acc[a] = -INFINITY;
+        if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < C::BN; c += 2)
-          acc[(c / 2) % kAcc] = max3f(acc[(c / 2) % kAcc], c < lim ? __uint_as_float(s[c]) : -INFINITY,
-                                      c + 1 < lim ? __uint_as_float(s[c + 1]) : -INFINITY);
+          for (int c = 0; c < C::BN; c += 2)
+            acc[(c / 2) % kAcc] = max3f(acc[(c / 2) % kAcc], c < lim ? __uint_as_float(s[c]) : -INFINITY,
+                                        c + 1 < lim ? __uint_as_float(s[c + 1]) : -INFINITY);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::BN; c += 2)
+            acc[(c / 2) % kAcc] = max3f(acc[(c / 2) % kAcc], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+        }
 #pragma unroll
         for (int w = kAcc / 2; w > 0; w /= 2)
 #pragma unroll
@@ -656,42 +662,48 @@ __device__ void wide_softmax_role(const TcParams& p, uint32_t tmem, const WideBa
       float2 sum2[kAcc / 2];
 #pragma unroll
       for (int a = 0; a < kAcc / 2; ++a) sum2[a] = make_float2(0.f, 0.f);
+      auto exp_tile = [&](auto masked) {
 #pragma unroll
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
-        float e[32];
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          float e[32];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int c = c0 + k;
-          const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
-          float v0 = ex2(x.x), v1 = ex2(x.y);
-          if (need_mask) {
-            if (c >= lim) v0 = 0.f;
-            if (c + 1 >= lim) v1 = 0.f;
+          for (int k = 0; k < 32; k += 2) {
+            const int c = c0 + k;
+            const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+            float v0 = ex2(x.x), v1 = ex2(x.y);
+            if constexpr (decltype(masked)::value) {
+              if (c >= lim) v0 = 0.f;
+              if (c + 1 >= lim) v1 = 0.f;
+            }
+            if constexpr (C::kTF32) {
+              // P to tf32 by dropping the 13 low mantissa bits (one integer op,
+              // instead of a conversion on the special-function pipe, which ex2
+              // already keeps busy): l then sums exactly the P that P.V uses, so
+              // the common shrink of the weights cancels in O / l
+              v0 = __uint_as_float(__float_as_uint(v0) & 0xFFFFE000u);
+              v1 = __uint_as_float(__float_as_uint(v1) & 0xFFFFE000u);
+            }
+            e[k] = v0;
+            e[k + 1] = v1;
+            sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
           }
           if constexpr (C::kTF32) {
-            // P to tf32 by dropping the 13 low mantissa bits (one integer op,
-            // instead of a conversion on the special-function pipe, which ex2
-            // already keeps busy): l then sums exactly the P that P.V uses, so
-            // the common shrink of the weights cancels in O / l
-            v0 = __uint_as_float(__float_as_uint(v0) & 0xFFFFE000u);
-            v1 = __uint_as_float(__float_as_uint(v1) & 0xFFFFE000u);
+            uint32_t pw[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) pw[k] = __float_as_uint(e[k]);
+            tmem_st32(tS + c0, pw);
+          } else {
+            uint32_t pw[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
+            tmem_st16(tS + c0 / 2, pw);
           }
-          e[k] = v0;
-          e[k + 1] = v1;
-          sum2[(k / 2) % (kAcc / 2)] = fadd2(sum2[(k / 2) % (kAcc / 2)], make_float2(v0, v1));
         }
-        if constexpr (C::kTF32) {
-          uint32_t pw[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) pw[k] = __float_as_uint(e[k]);
-          tmem_st32(tS + c0, pw);
-        } else {
-          uint32_t pw[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
-          tmem_st16(tS + c0 / 2, pw);
-        }
-      }
+      };
+      if (need_mask)
+        exp_tile(BoolC<true>{});
+      else
+        exp_tile(BoolC<false>{});
 #pragma unroll
       for (int w = kAcc / 4; w > 0; w /= 2)
 #pragma unroll

@@ -159,11 +159,11 @@ struct Bars {            // [NST]: one per query stage
   uint64_t* q_full;     // [NST] TMA -> MMA
   uint64_t* q_empty;    // [NST] MMA -> TMA
   uint64_t* s_full;     // [NST] MMA -> softmax
-  uint64_t* p_full;     // [NST] softmax -> MMA  (128 arrivals)
+  uint64_t* p_full;     // [NST] softmax -> MMA  (one arrival per warp)
   uint64_t* o_full;     // [NST] MMA -> epilogue (last P.V of a tile done)
-  uint64_t* o_empty;    // [NST] epilogue -> MMA (128 arrivals)
-  uint64_t* st_full;    // [NST] softmax -> epilogue: row stats written (128 arrivals; two stages)
-  uint64_t* st_empty;   // [NST] epilogue -> softmax (128 arrivals; two stages)
+  uint64_t* o_empty;    // [NST] epilogue -> MMA (one arrival per warp)
+  uint64_t* st_full;    // [NST] softmax -> epilogue: row stats written (per warp; two stages)
+  uint64_t* st_empty;   // [NST] epilogue -> softmax (per warp; two stages)
   uint64_t* kv_full;    // [NSLOT]
   uint64_t* kv_empty;   // [NSLOT]
   uint64_t* teardown;   // [1]
@@ -578,7 +578,7 @@ __device__ __forceinline__ void store_stage(const TcParams& p, const TileInfo& t
     }
   }
   tc_fence_before();
-  mbar_arrive(&bars.o_empty[s]);
+  mbar_arrive_warp(&bars.o_empty[s]);
   if (partial && valid)
     p.ws_lse[wrow] = st.y;
   else if (valid && p.LSE)
@@ -722,7 +722,7 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
       l_run += sum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars.p_full[stage]);
+      mbar_arrive_warp(&bars.p_full[stage]);
     }
     // the row statistics: 1/l and LSE (natural log); l_run = 0 only for a row
     // that sees no key of the unit -- a split-KV unit, or bottom-right causal
@@ -738,7 +738,7 @@ __device__ void tc_softmax_role(const TcParams& p, int stage, uint32_t tmem, con
       // two stages: hand them to the epilogue warpgroup
       if (!warp_wait(&bars.st_empty[stage], (tile_k & 1u) ^ 1u, wd, 0x34 + stage)) return;
       stats[stage * C::BM + row] = st;
-      mbar_arrive(&bars.st_full[stage]);
+      mbar_arrive_warp(&bars.st_full[stage]);
     }
   }
 }
@@ -765,7 +765,7 @@ __device__ void tc_epilogue_role(const TcParams& p, uint32_t tmem, const Bars& b
       if (!warp_wait(&bars.st_full[s], tile_k & 1u, wd, 0x43 + s)) return;
       tc_fence_after();
       const float2 st = stats[s * C::BM + row];
-      mbar_arrive(&bars.st_empty[s]);
+      mbar_arrive_warp(&bars.st_empty[s]);
       store_stage<C>(p, ti, s, st, tmem, lane_base, row, bars);
     }
   }
@@ -806,11 +806,11 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.p_full[s], 4);  // one arrival per warp of a group
       mbar_init(&bars.o_full[s], 1);
-      mbar_init(&bars.o_empty[s], 128);
-      mbar_init(&bars.st_full[s], 128);
-      mbar_init(&bars.st_empty[s], 128);
+      mbar_init(&bars.o_empty[s], 4);
+      mbar_init(&bars.st_full[s], 4);
+      mbar_init(&bars.st_empty[s], 4);
     }
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&bars.kv_full[s], 1);

@@ -268,8 +268,7 @@ fa_status_t launch_tensor_core(fa_dtype_t dtype, const fa_problem_t& pb, const D
   } else if ((st = make_map(&L.tmV, pb.V, fp32, pb.B, kv_heads(pb), pb.N_k, dv, bn, "V")) != FA_OK) {
     return st;
   }
-  if (wide && n_split == 1 &&
-      (st = make_map(&L.tmO, pb.O, fp32, pb.B, pb.H, pb.N_q, dv, 32, "O")) != FA_OK)
+  if (n_split == 1 && (st = make_map(&L.tmO, pb.O, fp32, pb.B, pb.H, pb.N_q, dv, 32, "O")) != FA_OK)
     return st;
   TcParams& p = L.p;
   p.B = (int)pb.B;

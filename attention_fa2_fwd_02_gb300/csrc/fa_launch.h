@@ -18,7 +18,7 @@ constexpr int kMaxDevices = 64;
 
 struct TcLaunch {
   CUtensorMap tmQ, tmK, tmV;
-  CUtensorMap tmO;  // O, 32-row boxes (single-stage kernel, unsplit: TMA-store epilogue)
+  CUtensorMap tmO{};  // O, 32-row boxes (unsplit, not packed: TMA-store epilogue)
   TcParams p;
   int grid;
   int device;  // current device ordinal (per-device one-time setup)

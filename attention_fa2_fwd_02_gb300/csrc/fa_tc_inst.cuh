@@ -22,7 +22,7 @@ static cudaError_t launch_tc(const TcLaunch& L) {
     if (e != cudaSuccess) return e;
     ready[L.device].store(true, std::memory_order_release);
   }
-  fa_tc_fwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  fa_tc_fwd_kernel<C><<<L.grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmO, L.p);
   return cudaGetLastError();
 }
 

@@ -925,6 +925,7 @@ fa_status_t fa_fwd_varlen(fa_dtype_t dtype, int64_t B, int64_t H, int64_t H_kv, 
   if ((st = make_map(&L.tmQ, pb.Q, false, 1, H, total_q, d, 128, "Q")) != FA_OK) return st;
   if ((st = make_map(&L.tmK, pb.K, false, 1, H_kv, total_k, d, 128, "K")) != FA_OK) return st;
   if ((st = make_map(&L.tmV, pb.V, false, 1, H_kv, total_k, dv, 128, "V")) != FA_OK) return st;
+  if ((st = make_map(&L.tmO, pb.O, false, 1, H, total_q, dv, 32, "O")) != FA_OK) return st;
   TcParams& p = L.p;
   p.B = (int)B;
   p.H = (int)H;

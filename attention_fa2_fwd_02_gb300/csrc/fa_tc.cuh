@@ -125,13 +125,13 @@ struct TcCfg {
   // shared memory
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = NST * kQBytes;
-  // plain tiles (not split, not packed): O leaves through TMA stores from a
-  // 4 KB buffer per storing warp (32 rows x 128 bytes, 128-byte swizzle);
-  // split units write fp32 partials, and a packed tile may end inside
-  // another sequence, so both keep per-row stores.  Measured: +1..2 % at
-  // d = 128 and on three stages, -4 % on the two-stage d = 64 (causal)
-  // tiles, which keep the per-row stores.
-  static constexpr bool kTmaStore = !SPLIT_ && !VARLEN_ && (D_ == 128 || NST_ == 3);
+  // O leaves through TMA stores from a 4 KB buffer per storing warp (32 rows
+  // x 128 bytes, 128-byte swizzle).  Split units write fp32 partials and keep
+  // per-row stores; in a packed batch, a warp whose 32 rows run past the end
+  // of its sequence stores its rows one by one.  Measured: +1..2 % at d = 128
+  // and on three stages, -4 % on the two-stage d = 64 (causal) tiles, which
+  // keep the per-row stores.
+  static constexpr bool kTmaStore = !SPLIT_ && (D_ == 128 || NST_ == 3);
   static constexpr int kStoreWarps = NST == 2 ? 4 : 4 * NST;
   static constexpr uint32_t kStoreBufBytes = 32 * 128;
   static constexpr uint32_t kOffStage = kOffKV + NSLOT * kKVBytes;
@@ -565,12 +565,16 @@ __device__ __forceinline__ void store_stage(const TcParams& p, const TileInfo& t
   const long long wrow = (static_cast<long long>(ti.split) * p.B * p.H + ti.b * p.H + ti.h) * p.N_q + q;
   const uint32_t tO = tmem + lane_base + C::col_o(s);
   const int dv = C::kSplit ? C::D : p.dv;  // columns of O to store
-  if constexpr (C::kTmaStore) {
-    // this warp's 32 rows, 64 columns (one swizzle row) per store; the TMA
-    // drops rows past N_q and columns past Dv
+  // this warp's 32 rows (warp-uniform choices)
+  const int r0 = ti.q0 + s * C::BM + (row & ~31);
+  const bool rows_one_by_one = !C::kTmaStore || (C::kVarlen && r0 + 32 > ti.len_q && r0 < ti.len_q);
+  if (C::kTmaStore && !rows_one_by_one) {
+    // 64 columns (one swizzle row) per store; the TMA drops rows past the
+    // tensor's end and columns past Dv.  Packed batches: rows r0 .. r0 + 31
+    // all belong to the sequence here (or none does), at packed rows
+    // qrow0 + r0 ..; a negative offset (bad cu_seqlens) stores nothing
     const int lane = row & 31;
-    const int r0 = ti.q0 + s * C::BM + (row & ~31);
-    const bool any_row = r0 < p.N_q;
+    const bool any_row = C::kVarlen ? (r0 < ti.len_q && ti.qrow0 >= 0) : r0 < p.N_q;
 #pragma unroll 1
     for (int c = 0; c < dv; c += 64) {
       if (any_row) {  // the store that last read the buffer
@@ -596,13 +600,13 @@ __device__ __forceinline__ void store_stage(const TcParams& p, const TileInfo& t
       fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine's reads
       __syncwarp();
       if (lane == 0) {
-        tma_store_4d(tmO, store_buf, c, r0, ti.h, ti.b);
+        tma_store_4d(tmO, store_buf, c, ti.qrow0 + r0, ti.h, ob);
         bulk_commit();
       }
     }
   }
 #pragma unroll 1
-  for (int c = 0; !C::kTmaStore && c < dv; c += 32) {
+  for (int c = 0; rows_one_by_one && c < dv; c += 32) {
     uint32_t o[32];
     tmem_ld32(tO + c, o);
     tmem_ld_wait32(o);

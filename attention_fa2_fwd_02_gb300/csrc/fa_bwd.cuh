@@ -72,7 +72,16 @@ struct BwdCfg {
   static constexpr int BN = 128;             // keys per work unit (tensor-memory lanes)
   static constexpr int BM = D == 128 ? 64 : 128;  // query rows per step
   static constexpr bool kDqT = D == 128;     // dQ computed transposed (lanes = head dim)
-  static constexpr int NST = 2;              // Q/dO ring depth
+  // d = 128: two S^T / dP^T buffers, so the tensor core computes the next
+  // step's S^T and dP^T while the compute warpgroups work on this step's; a
+  // step's dQ^T lands in its own S^T columns (issued after the dV product
+  // that reads P^T there).  d = 64 (128-row steps) has no room for them.
+  static constexpr bool kPipe = D == 128;
+  static constexpr int kSBufs = kPipe ? 2 : 1;
+  // Q/dO ring depth: step g + 1's S^T is issued right after step g - 1's
+  // products free their slot, so the pipelined order needs a third slot to
+  // keep the next Q/dO copy off its path
+  static constexpr int NST = kPipe ? 3 : 2;
   static constexpr int kPanels = D / 64;     // 128-byte swizzle panels of 64 bf16 (head dim)
   static constexpr int kQPanels = BM / 64;   // panels of the dS^T tile (queries)
   static constexpr uint32_t kKVTileBytes = BN * D * 2;
@@ -83,25 +92,32 @@ struct BwdCfg {
   static constexpr uint32_t kOffV = kOffK + kKVTileBytes;
   static constexpr uint32_t kOffQ = kOffV + kKVTileBytes;          // [NST]
   static constexpr uint32_t kOffdO = kOffQ + NST * kQTileBytes;    // [NST]
-  static constexpr uint32_t kOffdS = kOffdO + NST * kQTileBytes;   // dS^T [keys][queries]
-  static constexpr uint32_t kOffVec = kOffdS + BN * BM * 2;        // [NST] -lse2[BM], delta[BM]
+  static constexpr uint32_t kDsBytes = BN * BM * 2;
+  static constexpr uint32_t kOffdS = kOffdO + NST * kQTileBytes;   // [kSBufs] dS^T [keys][queries]
+  static constexpr uint32_t kOffDsEnd = kOffdS + kSBufs * kDsBytes;
   // The epilogue hands each step's dQ to the TMA engine as fp32 reduce-adds,
-  // through two 8 KB buffers per epilogue warp: d = 128 (dQ^T, lanes = head
-  // dims) 64 queries x the warp's 32 head dims, unswizzled; d = 64 (lanes =
-  // queries) the warp's 32 queries x 64 head dims, as two 128-byte-swizzled
-  // 32 x 32 halves
+  // through 8 KB buffers per epilogue warp (two; one at d = 128, for shared
+  // memory): d = 128 (dQ^T, lanes = head dims) 64 queries x the warp's 32
+  // head dims, unswizzled; d = 64 (lanes = queries) the warp's 32 queries x
+  // 64 head dims, as two 128-byte-swizzled 32 x 32 halves
   static constexpr uint32_t kDqStageBytes = 8192;
+  static constexpr int kDqBufs = kPipe ? 1 : 2;
   static_assert(BM * 32 * 4 == kDqStageBytes || !kDqT, "d = 128 buffer: BM queries x 32 head dims");
   static_assert(32 * D * 4 == kDqStageBytes || kDqT, "d = 64 buffer: 32 queries x 64 head dims");
-  static constexpr uint32_t kOffDqStage = (kOffVec + NST * 2 * BM * 4 + 1023) / 1024 * 1024;
-  static constexpr uint32_t kOffBar = kOffDqStage + 4 * 2 * kDqStageBytes;
-  static constexpr int kNumBars = 11 + 2 * NST;  // + teardown
+  static constexpr uint32_t kOffDqStage = (kOffDsEnd + 1023) / 1024 * 1024;
+  static constexpr uint32_t kOffVec = kOffDqStage + 4 * kDqBufs * kDqStageBytes;  // [NST] -lse2[BM], delta[BM]
+  static constexpr uint32_t kOffBar = kOffVec + NST * 2 * BM * 4;
+  static constexpr int kNumBars = 13 + 2 * NST;  // + teardown
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static constexpr uint32_t kThreads = 512;
-  // tensor memory columns
-  static constexpr uint32_t kColS = 0, kColdP = BM, kColdV = 2 * BM, kColdK = 2 * BM + D;
-  static constexpr uint32_t kColdQ = 2 * BM + 2 * D;  // two 64-column buffers
+  // tensor memory columns: S^T (P^T) and dP^T (dS^T) of buffer b, dV, dK,
+  // and dQ buffer b (d = 128: dQ^T in the S^T columns of its step's buffer;
+  // d = 64: two 64-column buffers of their own)
+  __host__ __device__ static constexpr uint32_t col_s(uint32_t b) { return kPipe ? b * BM : 0; }
+  __host__ __device__ static constexpr uint32_t col_dp(uint32_t b) { return kPipe ? (2 + b) * BM : BM; }
+  static constexpr uint32_t kColdV = 2 * kSBufs * BM, kColdK = kColdV + D;
+  __host__ __device__ static constexpr uint32_t col_dq(uint32_t b) { return kPipe ? col_s(b) : kColdK + D + b * 64; }
   static constexpr uint32_t kTmemCols = 512;
   // instruction descriptors (bf16 inputs, fp32 accumulators)
   static constexpr uint32_t kIdescS = make_idesc(1u, 128, BM, 0, 0);    // K-major A and B
@@ -110,14 +126,16 @@ struct BwdCfg {
   static constexpr uint32_t kKVBytes = 2 * kKVTileBytes;
   static constexpr uint32_t kStepBytes = 2 * kQTileBytes + 2 * BM * 4;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kColdQ + 128 == 512, "tensor memory layout");
+  static_assert(kColdK + D + (kPipe ? 0 : 128) == 512, "tensor memory layout");
+  static_assert(!kPipe || BM == 64, "dQ^T (64 query columns) fills one S^T buffer");
+  static_assert(kOffdS % 1024 == 0 && kDsBytes % 1024 == 0, "swizzled dS^T buffers");
 };
 
 struct BwdBars {
   uint64_t* kv_full;    // [1] K_j, V_j landed
   uint64_t* kv_empty;   // [1] unit's MMAs done with K_j, V_j
-  uint64_t* s_full;     // [1] S^T, dP^T ready
-  uint64_t* p_full;     // [1] P^T, dS^T written (256 arrivals)
+  uint64_t* s_full;     // [kSBufs] S^T, dP^T ready
+  uint64_t* p_full;     // [kSBufs] P^T, dS^T written (256 arrivals)
   uint64_t* dkv_full;   // [1] unit's dK, dV complete
   uint64_t* dkv_empty;  // [1] dK, dV read out (128 arrivals)
   uint64_t* dq_full;    // [2] dQ buffer ready
@@ -346,76 +364,99 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, c
                              const Watchdog& wd, uint64_t* teardown) {
   const uint32_t k_addr = smem_u32(smem + C::kOffK);
   const uint32_t v_addr = smem_u32(smem + C::kOffV);
-  const uint32_t ds_addr = smem_u32(smem + C::kOffdS);
   uint32_t ku = 0, gs = 0;
   bool ok = true;
+  // S^T(g) = K Q_g^T and dP^T(g) = V dO_g^T into buffer g mod kSBufs.  The
+  // buffer's previous contents: P^T / dS^T of step g - kSBufs, whose dV and
+  // dK products were issued before (in-order execution), and (d = 128) its
+  // dQ^T, which the epilogue must have read out.
+  auto issue_s = [&](uint32_t g) -> bool {
+    const uint32_t st = g % C::NST, b = g % C::kSBufs;
+    if (!bwd_warp_wait(&bars.q_full[st], (g / C::NST) & 1u, wd, 0x63)) return false;
+    if (C::kPipe && g >= 2 && !bwd_warp_wait(&bars.dq_empty[b], ((g >> 1) - 1) & 1u, wd, 0x64)) return false;
+    tc_fence_after();
+    if (elect_one()) {
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ + st * C::kQTileBytes);
+      const uint32_t do_addr = smem_u32(smem + C::kOffdO + st * C::kQTileBytes);
+      const uint64_t ak = sdesc_sw128<16, 1024>(k_addr), av = sdesc_sw128<16, 1024>(v_addr);
+      const uint64_t bq = sdesc_sw128<16, 1024>(q_addr), bdo = sdesc_sw128<16, 1024>(do_addr);
+#pragma unroll
+      for (int kk = 0; kk < C::D / 16; ++kk)
+        mma_ss<false>(tmem + C::col_s(b), ak + kmajor_off<C::kKVPanelBytes>(kk), bq + kmajor_off<C::kQPanelBytes>(kk),
+                      C::kIdescS, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < C::D / 16; ++kk)
+        mma_ss<false>(tmem + C::col_dp(b), av + kmajor_off<C::kKVPanelBytes>(kk),
+                      bdo + kmajor_off<C::kQPanelBytes>(kk), C::kIdescS, kk > 0);
+      tc_commit(&bars.s_full[b]);
+    }
+    __syncwarp();
+    return true;
+  };
+  // dV += P^T dO_g, dK += dS^T Q_g and dQ of step g, once the compute
+  // warpgroups have written P^T(g) and dS^T(g)
+  auto finish = [&](uint32_t g, bool first, bool last) -> bool {
+    const uint32_t st = g % C::NST, b = g % C::kSBufs, qb = g & 1u;
+    if (!bwd_warp_wait(&bars.p_full[b], (g / C::kSBufs) & 1u, wd, 0x65)) return false;
+    // the first accumulation of a unit overwrites dK, dV: the previous
+    // unit's must have been read out
+    if (first && ku > 0 && !bwd_warp_wait(&bars.dkv_empty[0], (ku - 1) & 1u, wd, 0x66)) return false;
+    // d = 64: the dQ buffer of two steps ago must have been read out
+    if (!C::kPipe && g >= 2 && !bwd_warp_wait(&bars.dq_empty[qb], ((g >> 1) - 1) & 1u, wd, 0x64)) return false;
+    tc_fence_after();
+    if (elect_one()) {
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ + st * C::kQTileBytes);
+      const uint32_t do_addr = smem_u32(smem + C::kOffdO + st * C::kQTileBytes);
+      // dV += P^T dO_g and dK += dS^T Q_g: A in tensor memory (bf16 pairs),
+      // B MN-major (head dim contiguous, k = query rows in 16-row steps)
+      const uint64_t bdo = sdesc_sw128<C::kQPanelBytes, 1024>(do_addr);
+      const uint64_t bq = sdesc_sw128<C::kQPanelBytes, 1024>(q_addr);
+#pragma unroll
+      for (int kk = 0; kk < C::BM / 16; ++kk)
+        mma_ts<false>(tmem + C::kColdV, tmem + C::col_s(b) + pcol<C>(kk), bdo + ((kk * 16 * 128) >> 4), C::kIdescAcc,
+                      (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < C::BM / 16; ++kk)
+        mma_ts<false>(tmem + C::kColdK, tmem + C::col_dp(b) + pcol<C>(kk), bq + ((kk * 16 * 128) >> 4), C::kIdescAcc,
+                      (!first || kk > 0) ? 1u : 0u);
+      // dQ over the keys (k = 16-key steps of 16 rows x 128 bytes):
+      //  d = 128: dQ_g^T = K_j^T dS_g^T, A = K_j MN-major (head dim
+      //           contiguous), B = dS^T MN-major (queries contiguous);
+      //  d = 64:  dQ_g = dS_g K_j, A = dS^T MN-major, B = K_j MN-major.
+      const uint32_t ds_addr = smem_u32(smem + C::kOffdS + b * C::kDsBytes);
+      const uint64_t dsd = sdesc_sw128<C::BN * 128, 1024>(ds_addr);
+      const uint64_t kd = sdesc_sw128<C::kKVPanelBytes, 1024>(k_addr);
+      const uint64_t a0 = C::kDqT ? kd : dsd, b0 = C::kDqT ? dsd : kd;
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_ss<false>(tmem + C::col_dq(qb), a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * 128) >> 4), C::kIdescdQ,
+                      kk > 0 ? 1u : 0u);
+      tc_commit(&bars.dq_full[qb]);
+      tc_commit(&bars.q_empty[st]);
+      if (last) {
+        tc_commit(&bars.dkv_full[0]);
+        tc_commit(&bars.kv_empty[0]);
+      }
+    }
+    __syncwarp();
+    return true;
+  };
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
     const BwdUnit w = bwd_unit<C>(p, u);
     if (w.n_steps == 0) continue;
     if (!(ok = bwd_warp_wait(&bars.kv_full[0], ku & 1u, wd, 0x62))) break;
+    const uint32_t g0 = gs;
     for (int s = 0; ok && s < w.n_steps; ++s, ++gs) {
-      const uint32_t st = gs % C::NST, qb = gs & 1u;
-      const bool first = (s == 0), last = (s == w.n_steps - 1);
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ + st * C::kQTileBytes);
-      const uint32_t do_addr = smem_u32(smem + C::kOffdO + st * C::kQTileBytes);
-      if (!(ok = bwd_warp_wait(&bars.q_full[st], (gs / C::NST) & 1u, wd, 0x63))) break;
-      tc_fence_after();
-      // S^T and dP^T overwrite P^T and dS^T of the previous step, whose dV
-      // and dK MMAs were issued before (in-order execution).
-      if (elect_one()) {
-        const uint64_t ak = sdesc_sw128<16, 1024>(k_addr), av = sdesc_sw128<16, 1024>(v_addr);
-        const uint64_t bq = sdesc_sw128<16, 1024>(q_addr), bdo = sdesc_sw128<16, 1024>(do_addr);
-#pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk)
-          mma_ss<false>(tmem + C::kColS, ak + kmajor_off<C::kKVPanelBytes>(kk), bq + kmajor_off<C::kQPanelBytes>(kk),
-                        C::kIdescS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk)
-          mma_ss<false>(tmem + C::kColdP, av + kmajor_off<C::kKVPanelBytes>(kk),
-                        bdo + kmajor_off<C::kQPanelBytes>(kk), C::kIdescS, kk > 0);
-        tc_commit(&bars.s_full[0]);
+      if (!(ok = issue_s(gs))) break;
+      if constexpr (C::kPipe) {
+        // the previous step's products after this step's S^T, dP^T: the
+        // tensor core works on them while the compute warpgroups run step s
+        if (s > 0) ok = finish(gs - 1, s == 1, false);
+      } else {
+        ok = finish(gs, s == 0, s == w.n_steps - 1);
       }
-      __syncwarp();
-      if (!(ok = bwd_warp_wait(&bars.p_full[0], gs & 1u, wd, 0x65))) break;
-      // the first accumulation of a unit overwrites dK, dV: the previous
-      // unit's must have been read out
-      if (first && ku > 0 && !(ok = bwd_warp_wait(&bars.dkv_empty[0], (ku - 1) & 1u, wd, 0x66))) break;
-      // the dQ buffer of two steps ago must have been read out
-      if (gs >= 2 && !(ok = bwd_warp_wait(&bars.dq_empty[qb], ((gs >> 1) - 1) & 1u, wd, 0x64))) break;
-      tc_fence_after();
-      if (elect_one()) {
-        // dV += P^T dO_i and dK += dS^T Q_i: A in tensor memory (bf16 pairs),
-        // B MN-major (head dim contiguous, k = query rows in 16-row steps)
-        const uint64_t bdo = sdesc_sw128<C::kQPanelBytes, 1024>(do_addr);
-        const uint64_t bq = sdesc_sw128<C::kQPanelBytes, 1024>(q_addr);
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ts<false>(tmem + C::kColdV, tmem + C::kColS + pcol<C>(kk), bdo + ((kk * 16 * 128) >> 4), C::kIdescAcc,
-                        (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ts<false>(tmem + C::kColdK, tmem + C::kColdP + pcol<C>(kk), bq + ((kk * 16 * 128) >> 4), C::kIdescAcc,
-                        (!first || kk > 0) ? 1u : 0u);
-        // dQ over the keys (k = 16-key steps of 16 rows x 128 bytes):
-        //  d = 128: dQ_i^T = K_j^T dS_i^T, A = K_j MN-major (head dim
-        //           contiguous), B = dS^T MN-major (queries contiguous);
-        //  d = 64:  dQ_i = dS_i K_j, A = dS^T MN-major, B = K_j MN-major.
-        const uint64_t dsd = sdesc_sw128<C::BN * 128, 1024>(ds_addr);
-        const uint64_t kd = sdesc_sw128<C::kKVPanelBytes, 1024>(k_addr);
-        const uint64_t a0 = C::kDqT ? kd : dsd, b0 = C::kDqT ? dsd : kd;
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ss<false>(tmem + C::kColdQ + qb * 64, a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * 128) >> 4),
-                        C::kIdescdQ, kk > 0 ? 1u : 0u);
-        tc_commit(&bars.dq_full[qb]);
-        tc_commit(&bars.q_empty[st]);
-        if (last) {
-          tc_commit(&bars.dkv_full[0]);
-          tc_commit(&bars.kv_empty[0]);
-        }
-      }
-      __syncwarp();
     }
+    if (C::kPipe && ok) ok = finish(gs - 1, gs - 1 == g0, true);
     ++ku;
   }
   if (!ok) {
@@ -435,9 +476,7 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
   const int lane = threadIdx.x & 31;
   const int r = wq * 32 + lane;  // key row of the tile = tensor-memory lane
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_base + C::kColS;
-  const uint32_t tdP = tmem + lane_base + C::kColdP;
-  uint8_t* ds_row = smem + C::kOffdS + r * 128;
+  uint8_t* const ds_row0 = smem + C::kOffdS + r * 128;
   const float sc = p.scale_log2;
   const float2 sc2 = make_float2(sc, sc);
   uint32_t gs = 0;
@@ -450,7 +489,11 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
       const uint32_t st = gs % C::NST;
       const float* nl2 = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * C::BM * 4) + cg * kCols;
       const float* dlt = nl2 + C::BM;
-      if (!bwd_warp_wait(&bars.s_full[0], gs & 1u, wd, 0x67)) return;
+      const uint32_t b = gs % C::kSBufs;
+      const uint32_t tS = tmem + lane_base + C::col_s(b);
+      const uint32_t tdP = tmem + lane_base + C::col_dp(b);
+      uint8_t* const ds_row = ds_row0 + b * C::kDsBytes;
+      if (!bwd_warp_wait(&bars.s_full[b], (gs / C::kSBufs) & 1u, wd, 0x67)) return;
       tc_fence_after();
       // per-element masking only where needed: the key tail and tiles that
       // reach above the diagonal (query tails have -lse2 = -inf)
@@ -504,7 +547,7 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, uint32_t tme
       tmem_st_wait();
       fence_proxy_async_smem();  // dS^T stores -> the tensor core's reads
       tc_fence_before();
-      mbar_arrive(&bars.p_full[0]);
+      mbar_arrive(&bars.p_full[b]);
     }
   }
 }
@@ -516,7 +559,7 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
   const int lane = threadIdx.x & 31;
   const int r = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  uint8_t* dq_stage = smem + C::kOffDqStage + wq * 2 * C::kDqStageBytes;  // this warp's two buffers
+  uint8_t* dq_stage = smem + C::kOffDqStage + wq * C::kDqBufs * C::kDqStageBytes;  // this warp's buffers
   uint32_t n_red = 0;                                                     // reductions issued
   uint32_t ku = 0, gs = 0;
   auto run = [&]() {
@@ -542,8 +585,8 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
       if (!bwd_warp_wait(&bars.dq_full[qb], (gs >> 1) & 1u, wd, 0x68)) return;
       tc_fence_after();
       uint32_t v[64];
-      tmem_ld32(tmem + lane_base + C::kColdQ + qb * 64, v);
-      tmem_ld32(tmem + lane_base + C::kColdQ + qb * 64 + 32, v + 32);
+      tmem_ld32(tmem + lane_base + C::col_dq(qb), v);
+      tmem_ld32(tmem + lane_base + C::col_dq(qb) + 32, v + 32);
       tmem_ld_wait32(v);
       reg_fence32(v + 32);
       tc_fence_before();
@@ -553,6 +596,7 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
         // warp's 32 x 64 block in two 32 x 32 halves, each row a 128-byte
         // swizzle row (16-byte chunk i at i ^ (row mod 8): conflict-free
         // quarter-warps), and one lane adds them with two TMA reductions
+        static_assert(C::kDqBufs == 2, "d = 64: two staging buffers per warp");
         uint8_t* buf = dq_stage + (n_red & 1u) * C::kDqStageBytes;
         if (n_red >= 2) {  // the reductions that last read this buffer
           if (lane == 0) bulk_wait_read<1>();
@@ -579,9 +623,10 @@ __device__ void bwd_epilogue_role(const CUtensorMap* tmDq, const BwdParams& p, u
         // 32 consecutive head dims: every store instruction covers one
         // 128-byte row) and one lane adds it into the accumulator with a TMA
         // reduction
-        float* buf = reinterpret_cast<float*>(dq_stage + (n_red & 1u) * C::kDqStageBytes);
-        if (n_red >= 2) {  // the reduction that last read this buffer
-          if (lane == 0) bulk_wait_read<1>();
+        static_assert(C::kDqBufs == 1, "d = 128: one staging buffer per warp");
+        float* buf = reinterpret_cast<float*>(dq_stage);
+        if (n_red >= 1) {  // the reduction that last read this buffer
+          if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
         }
 #pragma unroll
@@ -647,15 +692,15 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   BwdBars bars;
   bars.kv_full = bar + 0;
   bars.kv_empty = bar + 1;
-  bars.s_full = bar + 2;
-  bars.p_full = bar + 3;
-  bars.dkv_full = bar + 4;
-  bars.dkv_empty = bar + 5;
-  bars.dq_full = bar + 6;
-  bars.dq_empty = bar + 8;
-  bars.q_full = bar + 10;
-  bars.q_empty = bar + 10 + C::NST;
-  uint64_t* teardown = bar + 10 + 2 * C::NST;
+  bars.s_full = bar + 2;     // [2]
+  bars.p_full = bar + 4;     // [2]
+  bars.dkv_full = bar + 6;
+  bars.dkv_empty = bar + 7;
+  bars.dq_full = bar + 8;    // [2]
+  bars.dq_empty = bar + 10;  // [2]
+  bars.q_full = bar + 12;
+  bars.q_empty = bar + 12 + C::NST;
+  uint64_t* teardown = bar + 12 + 2 * C::NST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int warp = threadIdx.x / 32;
@@ -663,8 +708,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full[0], 1);
     mbar_init(&bars.kv_empty[0], 1);
-    mbar_init(&bars.s_full[0], 1);
-    mbar_init(&bars.p_full[0], 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.s_full[b], 1);
+      mbar_init(&bars.p_full[b], 256);
+    }
     mbar_init(&bars.dkv_full[0], 1);
     mbar_init(&bars.dkv_empty[0], 128);
     for (int b = 0; b < 2; ++b) {

@@ -415,14 +415,23 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, c
       for (int kk = 0; kk < C::BM / 16; ++kk)
         mma_ts<false>(tmem + C::kColdV, tmem + C::col_s(b) + pcol<C>(kk), bdo + ((kk * 16 * 128) >> 4), C::kIdescAcc,
                       (!first || kk > 0) ? 1u : 0u);
+      auto issue_dk = [&]() {
 #pragma unroll
-      for (int kk = 0; kk < C::BM / 16; ++kk)
-        mma_ts<false>(tmem + C::kColdK, tmem + C::col_dp(b) + pcol<C>(kk), bq + ((kk * 16 * 128) >> 4), C::kIdescAcc,
-                      (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_ts<false>(tmem + C::kColdK, tmem + C::col_dp(b) + pcol<C>(kk), bq + ((kk * 16 * 128) >> 4),
+                        C::kIdescAcc, (!first || kk > 0) ? 1u : 0u);
+      };
       // dQ over the keys (k = 16-key steps of 16 rows x 128 bytes):
       //  d = 128: dQ_g^T = K_j^T dS_g^T, A = K_j MN-major (head dim
       //           contiguous), B = dS^T MN-major (queries contiguous);
       //  d = 64:  dQ_g = dS_g K_j, A = dS^T MN-major, B = K_j MN-major.
+      // Without a causal mask dQ goes before dK (it only has to follow dV,
+      // which reads P^T where dQ^T lands at d = 128), so that the epilogue
+      // reads it out sooner: measured +8.5 % on the non-causal backward, but
+      // -3 % on the causal one (also with dK first on a unit's last step), so
+      // causal problems keep dK first.
+      const bool dq_first = !p.causal;
+      if (!dq_first) issue_dk();
       const uint32_t ds_addr = smem_u32(smem + C::kOffdS + b * C::kDsBytes);
       const uint64_t dsd = sdesc_sw128<C::BN * 128, 1024>(ds_addr);
       const uint64_t kd = sdesc_sw128<C::kKVPanelBytes, 1024>(k_addr);
@@ -432,6 +441,7 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, uint32_t tmem, c
         mma_ss<false>(tmem + C::col_dq(qb), a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * 128) >> 4), C::kIdescdQ,
                       kk > 0 ? 1u : 0u);
       tc_commit(&bars.dq_full[qb]);
+      if (dq_first) issue_dk();
       tc_commit(&bars.q_empty[st]);
       if (last) {
         tc_commit(&bars.dkv_full[0]);

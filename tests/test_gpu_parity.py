@@ -141,6 +141,27 @@ def test_small_head_ragged(oracle_mod, dtype, d, causal, nq, nk):
                  f"small {dtype} d={d} {nq}x{nk} causal={causal}")
 
 
+@pytest.mark.parametrize("d,causal", [(128, False), (128, True), (64, False)], ids=["d128_nc", "d128_causal", "d64_nc"])
+def test_output_view_inside_wider_buffer(oracle_mod, d, causal):
+    """O as a view into a larger buffer (row pitch d + 24, five spare rows per
+    head) with a ragged N: the tiles' O stores (TMA stores clipped to the
+    view) write every element of the view and nothing outside it."""
+    B, H, N = 2, 3, 300
+    Q = normal((B, H, N, d), 41, torch.bfloat16)
+    K = normal((B, H, N, d), 42, torch.bfloat16)
+    V = normal((B, H, N, d), 43, torch.bfloat16)
+    big = torch.full((B, H, N + 5, d + 24), 7.0, dtype=torch.bfloat16, device="cuda")
+    O = big[:, :, :N, :d]
+    O.fill_(float("nan"))
+    L = _poisoned((B, H, N), torch.float32)
+    fa.fwd(Q.cuda(), K.cuda(), V.cuda(), scale=0.1, is_causal=causal, out=O, lse=L)
+    fa.check()
+    O_ref, L_ref = oracle_mod.attention(Q, K, V, 0.1, causal)
+    assert_close(O.float().cpu().numpy(), L.cpu().numpy(), O_ref, L_ref, torch.bfloat16, f"view d={d}")
+    assert bool((big[:, :, N:, :] == 7).all()), "a store wrote past the view's last row"
+    assert bool((big[:, :, :N, d:] == 7).all()), "a store wrote past the view's last column"
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 def test_strided_heads_major_layout(oracle_mod, dtype):
     """Q, K, V, O as [B, N, H, d] storage viewed as [B, H, N, d] (non-monotonic strides)."""

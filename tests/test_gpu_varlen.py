@@ -190,3 +190,31 @@ def test_varlen_concurrent_streams_and_back_to_back(oracle_mod):
         O, L = fa.fwd_varlen(q, k, v, cq, ck, ml, is_causal=causal)
     fa.check()
     assert torch.equal(O, refs[1][0]) and torch.equal(L, refs[1][1])
+
+@pytest.mark.parametrize("causal", [False, True], ids=["nc", "top_left"])
+def test_varlen_output_view_inside_wider_buffer(oracle_mod, causal):
+    """Packed O as a view into a larger buffer (row pitch H x (d + 24), spare
+    rows after the last sequence).  Sequence ends fall inside 32-row blocks,
+    so some warps store by TMA and the one straddling each end row by row:
+    every packed row of the view is written and nothing outside it."""
+    d, H = 128, 3
+    lq = [300, 17, 129, 64]
+    q, k, v, cu_q, cu_k = packed(lq, lq, H, H, d, 1777, torch.bfloat16)
+    total = q.shape[0]
+    big = torch.full((total + 7, H, d + 24), 7.0, dtype=torch.bfloat16, device="cuda")
+    O = big[:total, :, :d]
+    O.fill_(float("nan"))
+    L = torch.full((H, total), float("nan"), dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    fa.fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_q.cuda(), cu_k.cuda(), max(lq), scale=scale,
+                  is_causal=causal, out=O, lse=L)
+    fa.check()
+    O_ref, L_ref = oracle_mod.attention_varlen(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                                               cu_q.numpy(), cu_k.numpy(), scale, fa.causal_code(causal))
+    Og = O.float().cpu().numpy()
+    assert np.isfinite(Og).all(), "a packed output row was not written"
+    eo = float(np.abs(Og - O_ref).max())
+    el = float(np.abs(L.cpu().numpy() - L_ref).max())
+    assert eo <= TOL_O and el <= TOL_LSE, f"max|dO|={eo:.3e} max|dLSE|={el:.3e}"
+    assert bool((big[total:] == 7).all()), "a store wrote past the last packed row"
+    assert bool((big[:total, :, d:] == 7).all()), "a store wrote past the view's last column"

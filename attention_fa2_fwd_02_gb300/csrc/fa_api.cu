@@ -436,7 +436,7 @@ cudaError_t launch_small_typed(const SmallParams& P, DevState& ds, cudaStream_t 
     }
   }
   if constexpr (kMma)
-    fa_small_mma_kernel<D><<<(unsigned)((P.n_items + 3) / 4), 128, smem, stream>>>(P);
+    fa_small_mma_kernel<D><<<(unsigned)((P.n_items + 1) / 2), 128, smem, stream>>>(P);
   else
     fa_small_fwd_kernel<T, D, kSmallSplit><<<(unsigned)P.n_items, 32 * kSmallSplit, smem, stream>>>(P);
   return cudaGetLastError();

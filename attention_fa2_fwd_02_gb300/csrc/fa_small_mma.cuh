@@ -13,8 +13,9 @@
 // set-up): at this size the set-up of the 5th-generation path would cost more
 // than the arithmetic.
 //
-//  * one warp owns 32 query rows of one (problem, b, h); Q, K and V arrive 32
-//    rows at a time through shared memory (row pitch D + 4 floats: every
+//  * two warps own 32 query rows of one (problem, b, h), 16 rows each; Q, K
+//    and V arrive 32 rows at a time through shared memory shared by the
+//    pair (row pitch D + 4 floats: every
 //    fragment load below hits 32 distinct banks), with the loads of the Q
 //    block and of the first K/V chunk all in flight before any is used;
 //  * fp32 to tf32 without losing accuracy: x = hi + lo with hi = x with its

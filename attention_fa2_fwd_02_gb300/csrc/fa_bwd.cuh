@@ -23,7 +23,11 @@
 //    steps: the epilogue warps stage it in shared memory and add it into the
 //    fp32 accumulator with TMA reductions (cp.reduce.async.bulk.tensor), one
 //    per warp and 8 KB block -- per-element global reductions cost 6 % (d =
-//    128) and 27 % (d = 64) of the whole backward;
+//    128) and 27 % (d = 64) of the whole backward.  At d = 128, S^T and dP^T
+//    are double-buffered as well and the MMA warp issues step g's S^T and
+//    dP^T before step g - 1's dV, dK and dQ, so that the tensor core works
+//    while the compute warpgroups run (the step's dQ^T then lands in its own
+//    S^T columns: see BwdCfg);
 //  * fa_bwd_post_kernel: dQ = scale * accumulator in the output dtype.
 //
 // The dQ product: d = 128 uses 64-row query steps and computes dQ_i^T =
@@ -34,8 +38,9 @@
 // Warp roles (512 threads): warpgroups 0 and 1 = compute (thread = key row =
 // tensor-memory lane), warpgroup 2 = epilogue (dQ reductions; dK, dV stores
 // at the end of a unit), warp 12 = TMA loads, warp 13 = MMA issue.  Tensor
-// memory: S^T (then P^T) | dP^T (then dS^T) | dV | dK | dQ x 2.  Every wait
-// is bounded (Watchdog).
+// memory: d = 64: S^T (then P^T) | dP^T (then dS^T) | dV | dK | dQ x 2;
+// d = 128: S^T x 2 (then P^T, then dQ^T) | dP^T x 2 (then dS^T) | dV | dK.
+// Every wait is bounded (Watchdog).
 #pragma once
 
 #include "fa_ptx.cuh"

@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -69,11 +70,21 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and whitespace: what the compiler
+    sees of the kernels (string literals are left alone; none holds '//')."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments and whitespace ignored), the
+    key under which the committed DRAM-traffic records were taken."""
     h = hashlib.sha256()
     for f in sorted((ROOT / "attention_fa2_fwd_02_gb300" / "csrc").glob("*")):
         h.update(f.name.encode())
-        h.update(f.read_bytes())
+        h.update(_code_only(f.read_text(errors="replace")).encode())
     return h.hexdigest()[:16]
 
 
